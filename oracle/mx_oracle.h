@@ -1,0 +1,119 @@
+/*
+ * mx_oracle.h -- plain CPU oracle for the MXFP4 weight-gradient path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and the
+ * cpu_baseline / reference arm of bench.py may load or call this library.
+ * The product (mxfp4_precision_gb300/) never links, imports or executes it,
+ * and shares no code, header or table with it.
+ *
+ * Sources followed (cited by page title and section):
+ *   [36kr]  "Neue Studie von AMD durchbricht die bestehende Erkenntnis: Die
+ *           Instabilitaet von FP4-Training liegt nicht an unzureichender
+ *           Zufaelligkeit" (eu.36kr.com), sections "Was ist MXFP4?",
+ *           "Fehlerdiagnoseexperiment", "Ende-zu-Ende-Effizienz".
+ *   [htx]   the Indonesian rendering of the same article (htx.com), sections
+ *           "Apa itu MXFP4", "Eksperimen Investigasi".
+ *   [show]  "AMD颠覆认知：FP4不稳定性的真正原因" (showapi.com), section 2.2
+ *           (FP4 = 1 sign, 2 exponent, 1 mantissa bit).
+ *   OCP Microscaling (MX) standard, named in [36kr] "Fazit": E8M0 scale
+ *           (bias 127), E2M1 element (bias 1, max 6, no Inf/NaN).
+ *   Philox4x64-10: Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As
+ *           Easy as 1, 2, 3", SC'11.
+ *
+ * Every routine is single-threaded and written for readability, not speed.
+ */
+#ifndef MX_ORACLE_H
+#define MX_ORACLE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Philox4x64 with 10 rounds (Salmon et al. SC'11): out = philox(ctr, key). */
+void oracle_philox4x64_10(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4]);
+
+/* Random sign d_t in {+1,-1} for absolute contraction position t, key (seed, 0).
+ * Reading of [36kr] "Fehlerdiagnoseexperiment" (Hadamard with random sign flip). */
+int oracle_sign(uint64_t seed, int64_t t);
+
+/* 24-bit stochastic-rounding draw for flat element index e, key (seed, tag). */
+uint32_t oracle_sr_u24(uint64_t seed, uint64_t tag, uint64_t e);
+
+/* Canonical fp32 Walsh-Hadamard of one block of n floats, in place:
+ * butterfly stages h = 1, 2, ..., n/2 (Sylvester / natural order), each
+ * (a, b) -> (a + b, a - b) rounded to fp32, then one fp32 multiply by the
+ * fp32 value nearest to 1/sqrt(n). */
+void oracle_fwht_f32(float *x, int n);
+
+/* Mathematical rotation in double: y = n^(-1/2) * H_n * x with the dense
+ * Sylvester matrix H_n[i][j] = (-1)^popcount(i & j). */
+void oracle_hadamard_f64(const double *x, int n, double *y);
+
+/* E8M0 shared-scale byte for a block whose largest magnitude is amax:
+ * s = floor(log2 amax) - 2 clamped to [-127, 127], byte = s + 127;
+ * amax == 0 -> 0x00; non-finite amax -> 0xFF. */
+uint8_t oracle_scale_byte(float amax);
+
+/* E2M1 code of v (already divided by the block scale), round to nearest,
+ * ties to the even code, saturating at +-6, sign of v kept. */
+uint8_t oracle_e2m1_rne(float v);
+
+/* E2M1 code of v with stochastic rounding: round away from the lower grid
+ * neighbour iff u24 < frac * 2^24, frac = (|v| - lo) / (hi - lo). */
+uint8_t oracle_e2m1_sr(float v, uint32_t u24);
+
+/* Exact value of a 4-bit E2M1 code (bit 3 = sign). */
+double oracle_e2m1_value(uint8_t code);
+
+/* Vector helpers over the scalar routines above (for exhaustive tests). */
+void oracle_scale_bytes(const float *amax, int64_t n, uint8_t *out);
+void oracle_e2m1_rne_vec(const float *v, int64_t n, uint8_t *out);
+void oracle_e2m1_sr_vec(const float *v, const uint32_t *u24, int64_t n, uint8_t *out);
+
+/* Rotation mode / rounding mode / contraction direction. */
+enum { ORACLE_ROT_NONE = 0, ORACLE_ROT_HADAMARD_DET = 1, ORACLE_ROT_HADAMARD_RAND = 2 };
+enum { ORACLE_ROUND_RNE = 0, ORACLE_ROUND_SR = 1 };
+enum { ORACLE_CONTRACT_ROWS = 0, ORACLE_CONTRACT_COLS = 1 };
+
+/* Rotated fp32 values of one contraction line (length L) of a bf16 matrix.
+ * precise == 0: canonical fp32 FWHT (the bit-exact contract);
+ * precise == 1: dense double product rounded once to fp32 (diagnostic). */
+int oracle_rotate_line(const uint16_t *line_bf16, int64_t stride, int64_t L, int64_t t0,
+                       int rot, int rot_block, uint64_t seed, int precise, float *out);
+
+/* MXFP4-encode a bf16 matrix src[rows][cols] (row-major).
+ *  contract == ROWS: blocks of 32 run down each column; line c = column c,
+ *      codes[c][rows/2], scales[c][rows/32]  (transposed, contraction-major).
+ *  contract == COLS: blocks run along each row; line r = row r,
+ *      codes[r][cols/2], scales[r][cols/32].
+ * Codes: element 2i in bits [3:0], element 2i+1 in bits [7:4].
+ * Scales: canonical layout, one E8M0 byte per block.
+ * SR draws use key (seed, sr_tag) and flat index line*L + t.
+ * Only the lines listed in `lines` (nlines of them) are produced when lines
+ * is non-NULL; outputs are then [nlines][...] in that order.
+ * Returns 0, or -1 on bad arguments. */
+int oracle_quantize(const uint16_t *src, int64_t rows, int64_t cols, int contract,
+                    int rot, int rot_block, int rnd, uint64_t seed, uint64_t sr_tag,
+                    const int64_t *lines, int64_t nlines, int precise,
+                    uint8_t *codes, uint8_t *scales);
+
+/* Decode codes[mn][k/2] + canonical scales[mn][k/32] into double out[mn][k]. */
+void oracle_dequantize(const uint8_t *codes, const uint8_t *scales, int64_t mn, int64_t k,
+                       double *out);
+
+/* C[i][j] = sum_t a[i][t] * b[j][t] over decoded operands, in double, for
+ * the n requested (i, j) pairs; also Cabs = sum_t |a| |b|. */
+void oracle_gemm_entries(const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq,
+                         const uint8_t *Bs, int64_t K, const int64_t *ii, const int64_t *jj,
+                         int64_t n, double *C, double *Cabs);
+
+/* Full C[M][N] (and Cabs) for rows [m0, m1) of A; decoded row by row. */
+void oracle_gemm_rows(const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq,
+                      const uint8_t *Bs, int64_t M, int64_t N, int64_t K, int64_t m0,
+                      int64_t m1, double *C, double *Cabs);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
