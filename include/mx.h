@@ -1,0 +1,186 @@
+/*
+ * mx.h -- C ABI of the GB300 (sm_103a) MXFP4 linear-layer library.
+ *
+ * What the library computes (cited by page title and section):
+ *   [36kr] "Neue Studie von AMD durchbricht die bestehende Erkenntnis: Die
+ *          Instabilitaet von FP4-Training liegt nicht an unzureichender
+ *          Zufaelligkeit" (eu.36kr.com); [htx] its Indonesian rendering
+ *          (htx.com); [show] "AMD颠覆认知：FP4不稳定性的真正原因" (showapi.com).
+ *   - MXFP4 encoding: blocks of 32 consecutive elements along the contraction
+ *     dimension share one E8M0 exponent, the block's largest exponent; each
+ *     element is rounded to the nearest FP4 (E2M1: 1 sign, 2 exponent, 1
+ *     mantissa bit) value ([36kr] "Was ist MXFP4?", [htx] "Apa itu MXFP4",
+ *     [show] 2.2).  Reading of the lost reconstruction formula:
+ *     x_hat = 2^s * Q(x / 2^s), s = floor(log2 amax) - 2 (OCP MX, [36kr] "Fazit").
+ *   - The three GEMMs of a linear layer, Fprop Y = X W^T, Dgrad dX = dY W,
+ *     Wgrad dW = dY^T X, computed from MXFP4 operands on the FP4 tensor cores
+ *     with fp32 accumulation ([36kr] "Fehlerdiagnoseexperiment").
+ *   - Rotation before quantisation: deterministic block Hadamard (the
+ *     stabiliser; "H16" in [36kr] "Ende-zu-Ende-Effizienz" figure caption),
+ *     Hadamard with a random sign flip, and stochastic rounding (the two
+ *     randomised ablations of [36kr] "Fehlerdiagnoseexperiment").
+ *
+ * Conventions for every entry point:
+ *   - Pointers named d_* are DEVICE pointers; h_* are HOST pointers.  The
+ *     caller owns every buffer.  Nothing on the compute path allocates memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     All compute entry points are asynchronous on `stream`.
+ *   - Argument errors are detected on the host BEFORE anything is launched
+ *     and returned as mx_status; nothing is written in that case.
+ *   - A device-side wait that exceeds its time limit (a stalled pipeline)
+ *     records MX_ERR_TIMEOUT in a per-device status word; the kernel then
+ *     returns without faulting.  mx_check_status() reports and clears it.
+ *   - bf16 inputs are raw IEEE bfloat16 bit patterns (uint16), row-major.
+ *   - Alignment: every device pointer must be 16-byte aligned.  The
+ *     contiguous (last) dimension of a bf16 input must be a multiple of 8
+ *     elements so that each row starts on a 16-byte boundary (TMA rule).
+ */
+#ifndef MX_H
+#define MX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MX_OK = 0,
+    MX_ERR_INVALID_ARG = 1, /* null pointer, bad enum, unsupported rot_block */
+    MX_ERR_SHAPE = 2,       /* negative size or contraction length not a multiple of 32
+                               (or of rot_block when rotating) */
+    MX_ERR_ALIGN = 3,       /* pointer or row pitch not 16-byte aligned */
+    MX_ERR_WORKSPACE = 4,   /* workspace smaller than mx_linear_workspace_bytes() */
+    MX_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed */
+    MX_ERR_TIMEOUT = 6,     /* a device-side bounded wait expired (see mx_check_status) */
+    MX_ERR_UNSUPPORTED = 7  /* the current device is not sm_103 / sm_100 family */
+} mx_status;
+
+typedef enum {
+    MX_ROT_NONE = 0,          /* no rotation */
+    MX_ROT_HADAMARD_DET = 1,  /* deterministic block Hadamard along the contraction dim */
+    MX_ROT_HADAMARD_RAND = 2  /* random sign flip d_t, then block Hadamard */
+} mx_rot;
+
+typedef enum {
+    MX_ROUND_RNE = 0,  /* round to nearest, ties to the even code */
+    MX_ROUND_SR = 1    /* stochastic rounding (zero-mean error) */
+} mx_round;
+
+typedef enum {
+    MX_CONTRACT_ROWS = 0, /* src[rows, cols]: blocks run down each column (the
+                             contraction dim is `rows`); output is transposed to
+                             codes[cols][rows/2] so the contraction dim is contiguous */
+    MX_CONTRACT_COLS = 1  /* blocks run along each row; codes[rows][cols/2] */
+} mx_contract;
+
+typedef enum { MX_OP_FPROP = 0, MX_OP_DGRAD = 1, MX_OP_WGRAD = 2 } mx_op;
+
+/* ------------------------------------------------------------------------ */
+/* Encoded operand layout                                                    */
+/* ------------------------------------------------------------------------ */
+/*
+ * An encoded operand has `mn` lines (rows of the GEMM operand) and contraction
+ * length `k` (a multiple of 32).
+ *
+ * Codes: uint8 [mn][k/2], row-major; element 2i of a line in bits [3:0] of
+ * byte i, element 2i+1 in bits [7:4].  E2M1 code: bit 3 sign, bits [2:1]
+ * exponent (bias 1), bit 0 mantissa; magnitudes 0,.5,1,1.5,2,3,4,6.
+ *
+ * Scales: one E8M0 byte (2^(byte-127); 0xFF = NaN) per 32-element block,
+ * tiled for the tensor cores' scale-factor path.  Lines are padded to
+ * MP = 128*ceil(mn/128) and blocks to KB = 8*ceil(k/256).  The byte of line
+ * r, block b lives at
+ *     ((r/128) * (KB/4) + b/4) * 512 + (r%32)*16 + ((r%128)/32)*4 + (b%4).
+ * i.e. 512-byte atoms of 128 lines x 4 blocks; atoms of one 128-line group
+ * are contiguous along k.  Padding bytes are zero (mx_quantize writes them).
+ */
+size_t mx_codes_bytes(int64_t mn, int64_t k);
+size_t mx_scales_bytes(int64_t mn, int64_t k);
+
+/*
+ * mx_quantize -- rotate and MXFP4-encode a bf16 matrix d_src[rows][cols].
+ *   contract   MX_CONTRACT_ROWS: lines = columns, k = rows (needs cols % 8 == 0)
+ *              MX_CONTRACT_COLS: lines = rows,    k = cols
+ *   rot        mx_rot; rot_block in {16, 32, 64, 128, 256} must divide k
+ *              (ignored for MX_ROT_NONE).  The Hadamard is Sylvester-ordered,
+ *              normalised by 1/sqrt(rot_block), evaluated in fp32 as butterfly
+ *              stages of stride 1, 2, ..., rot_block/2 then one multiply.
+ *   rnd        mx_round.  SR draws: Philox4x64-10, key (seed, 1), counter
+ *              (e/8, 0, 0, 0), e = line*k + position; 24-bit draw u; round away
+ *              from the lower grid neighbour iff u < frac * 2^24.
+ *   seed       key for the random sign (key (seed, 0), bit t%256 of the 256-bit
+ *              block t/256, t = position along k) and for SR.
+ *   d_codes    mx_codes_bytes(lines, k) bytes; d_scales mx_scales_bytes(lines, k).
+ * rows == 0 or cols == 0: returns MX_OK and launches nothing.
+ */
+mx_status mx_quantize(const void *d_src, int64_t rows, int64_t cols, int contract, int rot,
+                      int rot_block, int rnd, uint64_t seed, void *d_codes, void *d_scales,
+                      void *stream);
+
+/*
+ * mx_gemm -- C[M][N] (fp32, row-major, overwritten) = A . B^T, where A is an
+ * encoded operand with M lines and B one with N lines, both of contraction
+ * length K (K % 32 == 0).  Block-scaled FP4 tensor-core contraction with fp32
+ * accumulation.  Needs N % 4 == 0 (16-byte output rows).  M, N or K == 0: C is
+ * zero-filled (K == 0) or untouched (M or N == 0) and MX_OK is returned.
+ */
+mx_status mx_gemm(const void *d_Aq, const void *d_As, const void *d_Bq, const void *d_Bs,
+                  float *d_C, int64_t M, int64_t N, int64_t K, void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* Linear-layer GEMMs ([36kr] "Fehlerdiagnoseexperiment")                     */
+/* ------------------------------------------------------------------------ */
+/*
+ * Workspace (device, caller-owned) for one call of the given op: the two
+ * encoded operands, each 256-byte aligned.
+ *   FPROP: X[T][K], W[N][K] -> Y[T][N]       contraction K
+ *   DGRAD: dY[T][N], W[N][K] -> dX[T][K]     contraction N
+ *   WGRAD: dY[T][N], X[T][K] -> dW[N][K]     contraction T
+ */
+size_t mx_linear_workspace_bytes(int op, int64_t T, int64_t N, int64_t K);
+
+/*
+ * mx_linear_wgrad -- dW[N][K] = dY^T X.  Both operands are rotated along T
+ * with the same rotation (same sign vector in MX_ROT_HADAMARD_RAND) and
+ * encoded along T; operand dY uses SR key (seed, 1), X uses (seed, 2).
+ * T % 32 == 0 (and % rot_block); N, K % 8 == 0.
+ */
+mx_status mx_linear_wgrad(const void *d_dY, const void *d_X, float *d_dW, int64_t T,
+                          int64_t N, int64_t K, int rot, int rot_block, int rnd, uint64_t seed,
+                          void *d_ws, size_t ws_bytes, void *stream);
+
+/* mx_linear_fprop -- Y[T][N] = X W^T, contraction K (K % 32 == 0, N % 4 == 0). */
+mx_status mx_linear_fprop(const void *d_X, const void *d_W, float *d_Y, int64_t T, int64_t N,
+                          int64_t K, int rot, int rot_block, int rnd, uint64_t seed,
+                          void *d_ws, size_t ws_bytes, void *stream);
+
+/* mx_linear_dgrad -- dX[T][K] = dY W, contraction N (N % 32 == 0, K % 8 == 0). */
+mx_status mx_linear_dgrad(const void *d_dY, const void *d_W, float *d_dX, int64_t T, int64_t N,
+                          int64_t K, int rot, int rot_block, int rnd, uint64_t seed,
+                          void *d_ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* Status and diagnostics                                                    */
+/* ------------------------------------------------------------------------ */
+/* Synchronises `stream`, then returns and clears the current device's status
+ * word: MX_ERR_TIMEOUT if a bounded device wait expired since the last call,
+ * MX_ERR_CUDA if the stream reported an error, else MX_OK. */
+mx_status mx_check_status(void *stream);
+
+/* Launches one CTA that waits on a barrier nothing will ever complete; its
+ * bounded wait gives up after `limit_us` microseconds and records
+ * MX_ERR_TIMEOUT.  Exists to test the timeout path without hanging a GPU. */
+mx_status mx_debug_timeout_probe(int64_t limit_us, void *stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *mx_status_string(int status);
+
+/* Library ABI version (major*100 + minor). */
+int mx_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MX_H */

@@ -1,0 +1,206 @@
+"""ctypes declarations of include/mx.h and torch-tensor marshalling.
+
+Functions here only check that tensors have the dtype/device/contiguity the C
+ABI documents, pass raw data pointers and the current CUDA stream, and turn
+a non-zero mx_status into an exception.  Output buffers are allocated with
+torch (device memory plumbing); all compute happens in the library.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from .build import LIB
+
+ROT_NONE, ROT_HADAMARD_DET, ROT_HADAMARD_RAND = 0, 1, 2
+ROUND_RNE, ROUND_SR = 0, 1
+CONTRACT_ROWS, CONTRACT_COLS = 0, 1
+OP_FPROP, OP_DGRAD, OP_WGRAD = 0, 1, 2
+
+EXPORTED = [
+    "mx_codes_bytes", "mx_scales_bytes", "mx_quantize", "mx_gemm", "mx_linear_workspace_bytes",
+    "mx_linear_wgrad", "mx_linear_fprop", "mx_linear_dgrad", "mx_check_status",
+    "mx_debug_timeout_probe", "mx_status_string", "mx_version",
+]
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MXError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+def library_path() -> str:
+    return LIB
+
+
+def lib() -> ctypes.CDLL:
+    """Load the in-tree C-ABI library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB):
+                raise RuntimeError(
+                    f"MXFP4 CUDA library not found at {LIB}; build it with "
+                    "`python -c 'import __graft_entry__ as g; g.build()'`")
+            L = ctypes.CDLL(LIB)
+            P, i64, u64, i32, sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64,
+                                    ctypes.c_int, ctypes.c_size_t)
+            L.mx_codes_bytes.argtypes = [i64, i64]
+            L.mx_codes_bytes.restype = sz
+            L.mx_scales_bytes.argtypes = [i64, i64]
+            L.mx_scales_bytes.restype = sz
+            L.mx_quantize.argtypes = [P, i64, i64, i32, i32, i32, i32, u64, P, P, P]
+            L.mx_quantize.restype = i32
+            L.mx_gemm.argtypes = [P, P, P, P, P, i64, i64, i64, P]
+            L.mx_gemm.restype = i32
+            L.mx_linear_workspace_bytes.argtypes = [i32, i64, i64, i64]
+            L.mx_linear_workspace_bytes.restype = sz
+            for name in ("mx_linear_wgrad", "mx_linear_fprop", "mx_linear_dgrad"):
+                fn = getattr(L, name)
+                fn.argtypes = [P, P, P, i64, i64, i64, i32, i32, i32, u64, P, sz, P]
+                fn.restype = i32
+            L.mx_check_status.argtypes = [P]
+            L.mx_check_status.restype = i32
+            L.mx_debug_timeout_probe.argtypes = [i64, P]
+            L.mx_debug_timeout_probe.restype = i32
+            L.mx_status_string.argtypes = [i32]
+            L.mx_status_string.restype = ctypes.c_char_p
+            L.mx_version.argtypes = []
+            L.mx_version.restype = i32
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().mx_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise MXError(status, what)
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _dev_ptr(t: torch.Tensor, name: str) -> int:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return int(t.data_ptr())
+
+
+def codes_bytes(mn: int, k: int) -> int:
+    return int(lib().mx_codes_bytes(mn, k))
+
+
+def scales_bytes(mn: int, k: int) -> int:
+    return int(lib().mx_scales_bytes(mn, k))
+
+
+def linear_workspace_bytes(op: int, T: int, N: int, K: int) -> int:
+    return int(lib().mx_linear_workspace_bytes(op, T, N, K))
+
+
+def _as_bf16_bits(x: torch.Tensor) -> torch.Tensor:
+    if x.dtype == torch.bfloat16:
+        return x
+    if x.dtype in (torch.int16, torch.uint16):
+        return x
+    raise ValueError("bf16 input expected (torch.bfloat16 or raw 16-bit patterns)")
+
+
+# ---------------------------------------------------------------------------
+def quantize_into(src: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor, contract: int,
+                  rot: int = ROT_NONE, rot_block: int = 32, rnd: int = ROUND_RNE, seed: int = 0,
+                  stream=None) -> None:
+    src = _as_bf16_bits(src)
+    rows, cols = src.shape
+    st = lib().mx_quantize(_dev_ptr(src, "src"), rows, cols, contract, rot, rot_block, rnd,
+                           seed, _dev_ptr(codes, "codes"), _dev_ptr(scales, "scales"),
+                           _stream(stream))
+    _check(st, "mx_quantize")
+
+
+def quantize(src: torch.Tensor, contract: int, rot: int = ROT_NONE, rot_block: int = 32,
+             rnd: int = ROUND_RNE, seed: int = 0, stream=None):
+    """Returns (codes uint8 [lines, k/2], scales uint8 [mx_scales_bytes] in the tiled layout)."""
+    rows, cols = src.shape
+    L, lines = (rows, cols) if contract == CONTRACT_ROWS else (cols, rows)
+    codes = torch.empty((lines, L // 2), dtype=torch.uint8, device=src.device)
+    scales = torch.empty((max(1, scales_bytes(lines, L)),), dtype=torch.uint8, device=src.device)
+    quantize_into(src, codes, scales, contract, rot, rot_block, rnd, seed, stream)
+    return codes, scales
+
+
+def gemm_into(Aq, As, Bq, Bs, C: torch.Tensor, M: int, N: int, K: int, stream=None) -> None:
+    st = lib().mx_gemm(_dev_ptr(Aq, "Aq"), _dev_ptr(As, "As"), _dev_ptr(Bq, "Bq"),
+                       _dev_ptr(Bs, "Bs"), _dev_ptr(C, "C"), M, N, K, _stream(stream))
+    _check(st, "mx_gemm")
+
+
+def gemm(Aq, As, Bq, Bs, M: int, N: int, K: int, stream=None) -> torch.Tensor:
+    C = torch.empty((M, N), dtype=torch.float32, device=Aq.device)
+    gemm_into(Aq, As, Bq, Bs, C, M, N, K, stream)
+    return C
+
+
+def _linear(fn_name, op, a, b, out_shape, T, N, K, rot, rot_block, rnd, seed, ws, out, stream):
+    a, b = _as_bf16_bits(a), _as_bf16_bits(b)
+    need = linear_workspace_bytes(op, T, N, K)
+    if ws is None:
+        ws = torch.empty((max(need, 256),), dtype=torch.uint8, device=a.device)
+    if out is None:
+        out = torch.empty(out_shape, dtype=torch.float32, device=a.device)
+    fn = getattr(lib(), fn_name)
+    st = fn(_dev_ptr(a, "a"), _dev_ptr(b, "b"), _dev_ptr(out, "out"), T, N, K, rot, rot_block,
+            rnd, seed, _dev_ptr(ws, "workspace"), ws.numel() * ws.element_size(), _stream(stream))
+    _check(st, fn_name)
+    return out
+
+
+def linear_wgrad(dY, X, rot=ROT_HADAMARD_DET, rot_block=32, rnd=ROUND_RNE, seed=0, ws=None,
+                 out=None, stream=None) -> torch.Tensor:
+    """dW[N, K] = dY^T X with dY [T, N], X [T, K] (bf16); fp32 output."""
+    T, N = dY.shape
+    K = X.shape[1]
+    return _linear("mx_linear_wgrad", OP_WGRAD, dY, X, (N, K), T, N, K, rot, rot_block, rnd,
+                   seed, ws, out, stream)
+
+
+def linear_fprop(X, W, rot=ROT_NONE, rot_block=32, rnd=ROUND_RNE, seed=0, ws=None, out=None,
+                 stream=None) -> torch.Tensor:
+    """Y[T, N] = X W^T with X [T, K], W [N, K] (bf16); fp32 output."""
+    T, K = X.shape
+    N = W.shape[0]
+    return _linear("mx_linear_fprop", OP_FPROP, X, W, (T, N), T, N, K, rot, rot_block, rnd, seed,
+                   ws, out, stream)
+
+
+def linear_dgrad(dY, W, rot=ROT_NONE, rot_block=32, rnd=ROUND_RNE, seed=0, ws=None, out=None,
+                 stream=None) -> torch.Tensor:
+    """dX[T, K] = dY W with dY [T, N], W [N, K] (bf16); fp32 output."""
+    T, N = dY.shape
+    K = W.shape[1]
+    return _linear("mx_linear_dgrad", OP_DGRAD, dY, W, (T, K), T, N, K, rot, rot_block, rnd,
+                   seed, ws, out, stream)
+
+
+def check_status(stream=None) -> None:
+    _check(lib().mx_check_status(_stream(stream)), "mx_check_status")
+
+
+def debug_timeout_probe(limit_us: int, stream=None) -> int:
+    """Launch the never-completed-barrier probe; returns mx_check_status's code."""
+    _check(lib().mx_debug_timeout_probe(limit_us, _stream(stream)), "mx_debug_timeout_probe")
+    return int(lib().mx_check_status(_stream(stream)))

@@ -1,0 +1,332 @@
+// mx_api.cu -- the library's C ABI (include/mx.h): argument checks, workspace
+// carving, tensor-map encoding, per-device status word, and the launches.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "../../include/mx.h"
+#include "mx_internal.h"
+#include "mx_ptx.cuh"
+
+// One status word per device (lives as long as the module is loaded).
+static __device__ int g_mx_status;
+
+namespace mx {
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+DeviceInfo g_devices[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool load_encode_fn() {
+    if (g_encode != nullptr) return true;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return false;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return true;
+}
+
+__global__ void timeout_probe_kernel(int *status, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    // Nothing ever arrives on `bar`: the bounded wait must give up.
+    if (threadIdx.x == 0) mbar_wait(&bar, 0, status, nullptr, limit_ns);
+    __syncthreads();
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool valid_rot(int rot, int rot_block) {
+    if (rot == MX_ROT_NONE) return true;
+    if (rot != MX_ROT_HADAMARD_DET && rot != MX_ROT_HADAMARD_RAND) return false;
+    return rot_block == 16 || rot_block == 32 || rot_block == 64 || rot_block == 128 ||
+           rot_block == 256;
+}
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+mx_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MX_OK : MX_ERR_CUDA; }
+
+// Checks shared by every encode: enums, shape (contraction length multiple of
+// 32 and of rot_block), pointer alignment.
+mx_status check_encode(const void *src, int64_t rows, int64_t cols, int contract, int rot,
+                       int rot_block, int rnd, const void *codes, const void *scales) {
+    if (contract != MX_CONTRACT_ROWS && contract != MX_CONTRACT_COLS) return MX_ERR_INVALID_ARG;
+    if (!valid_rot(rot, rot_block)) return MX_ERR_INVALID_ARG;
+    if (rnd != MX_ROUND_RNE && rnd != MX_ROUND_SR) return MX_ERR_INVALID_ARG;
+    if (rows < 0 || cols < 0) return MX_ERR_SHAPE;
+    if (rows > 0x7FFFFFFF || cols > 0x7FFFFFFF) return MX_ERR_SHAPE;
+    if (rows == 0 || cols == 0) return MX_OK;
+    if (src == nullptr || codes == nullptr || scales == nullptr) return MX_ERR_INVALID_ARG;
+    const int64_t L = contract == MX_CONTRACT_ROWS ? rows : cols;
+    if (L % 32 != 0) return MX_ERR_SHAPE;
+    if (rot != MX_ROT_NONE && L % rot_block != 0) return MX_ERR_SHAPE;
+    if (!aligned16(src) || !aligned16(codes) || !aligned16(scales)) return MX_ERR_ALIGN;
+    if (cols % 8 != 0) return MX_ERR_ALIGN;  // 16-byte rows for the TMA
+    return MX_OK;
+}
+
+mx_status check_gemm(const void *Aq, const void *As, const void *Bq, const void *Bs,
+                     const float *C, int64_t M, int64_t N, int64_t K) {
+    if (M < 0 || N < 0 || K < 0) return MX_ERR_SHAPE;
+    if (M > 0x7FFFFFFF || N > 0x7FFFFFFF || K > 0x7FFFFFFF) return MX_ERR_SHAPE;
+    if (M == 0 || N == 0) return MX_OK;
+    if (C == nullptr) return MX_ERR_INVALID_ARG;
+    if (K % 32 != 0) return MX_ERR_SHAPE;
+    if (N % 4 != 0 || !aligned16(C)) return MX_ERR_ALIGN;
+    if (K == 0) return MX_OK;
+    if (!Aq || !As || !Bq || !Bs) return MX_ERR_INVALID_ARG;
+    if (!aligned16(Aq) || !aligned16(As) || !aligned16(Bq) || !aligned16(Bs)) return MX_ERR_ALIGN;
+    return MX_OK;
+}
+
+// Lines and contraction length of both operands of a linear op.
+struct OpShape {
+    int64_t a_lines, b_lines, k;
+};
+bool op_shape(int op, int64_t T, int64_t N, int64_t K, OpShape *s) {
+    switch (op) {
+        case MX_OP_FPROP: *s = {T, N, K}; return true;
+        case MX_OP_DGRAD: *s = {T, K, N}; return true;
+        case MX_OP_WGRAD: *s = {N, K, T}; return true;
+        default: return false;
+    }
+}
+
+}  // namespace
+
+const DeviceInfo *current_device(cudaError_t *err) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        *err = e != cudaSuccess ? e : cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo &d = g_devices[dev];
+    if (d.ordinal == dev) return &d;
+    cudaDeviceProp prop;
+    if ((e = cudaGetDeviceProperties(&prop, dev)) != cudaSuccess) {
+        *err = e;
+        return nullptr;
+    }
+    void *status = nullptr;
+    if ((e = cudaGetSymbolAddress(&status, g_mx_status)) != cudaSuccess) {
+        *err = e;
+        return nullptr;
+    }
+    if (!load_encode_fn()) {
+        *err = cudaErrorSymbolNotFound;
+        return nullptr;
+    }
+    d.sm_count = prop.multiProcessorCount;
+    d.cc_major = prop.major;
+    d.cc_minor = prop.minor;
+    d.status = static_cast<int *>(status);
+    d.ordinal = dev;
+    return &d;
+}
+
+bool encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base,
+                    uint64_t inner_elems, uint64_t outer_elems, uint64_t row_bytes,
+                    uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+    if (g_encode == nullptr) return false;
+    cuuint64_t dims[2] = {inner_elems, outer_elems};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace mx
+
+using namespace mx;
+
+namespace {
+mx_status device_or_error(const DeviceInfo **out) {
+    cudaError_t e = cudaSuccess;
+    const DeviceInfo *d = current_device(&e);
+    if (d == nullptr) return MX_ERR_CUDA;
+    if (!(d->cc_major == 10 && d->cc_minor == 3)) return MX_ERR_UNSUPPORTED;
+    *out = d;
+    return MX_OK;
+}
+
+mx_status quantize_impl(const void *src, int64_t rows, int64_t cols, int contract, int rot,
+                        int rot_block, int rnd, uint64_t seed, uint64_t sr_tag, void *codes,
+                        void *scales, cudaStream_t stream) {
+    mx_status st = check_encode(src, rows, cols, contract, rot, rot_block, rnd, codes, scales);
+    if (st != MX_OK || rows == 0 || cols == 0) return st;
+    const DeviceInfo *dev = nullptr;
+    if ((st = device_or_error(&dev)) != MX_OK) return st;
+    return from_cuda(launch_quantize(src, rows, cols, contract, rot, rot_block, rnd, seed, sr_tag,
+                                     codes, scales, *dev, stream));
+}
+
+mx_status gemm_impl(const void *Aq, const void *As, const void *Bq, const void *Bs, float *C,
+                    int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+    mx_status st = check_gemm(Aq, As, Bq, Bs, C, M, N, K);
+    if (st != MX_OK || M == 0 || N == 0) return st;
+    if (K == 0)
+        return from_cuda(cudaMemsetAsync(C, 0, static_cast<size_t>(M) * N * sizeof(float), stream));
+    const DeviceInfo *dev = nullptr;
+    if ((st = device_or_error(&dev)) != MX_OK) return st;
+    return from_cuda(launch_gemm(Aq, As, Bq, Bs, C, M, N, K, *dev, stream));
+}
+
+// Quantise both operands of a linear op into the workspace, then contract.
+mx_status linear_impl(int op, const void *a_src, int64_t a_rows, int64_t a_cols, int a_contract,
+                      const void *b_src, int64_t b_rows, int64_t b_cols, int b_contract, float *out,
+                      int64_t T, int64_t N, int64_t K, int rot, int rot_block, int rnd,
+                      uint64_t seed, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    OpShape s;
+    if (!op_shape(op, T, N, K, &s)) return MX_ERR_INVALID_ARG;
+    if (T < 0 || N < 0 || K < 0) return MX_ERR_SHAPE;
+    if (s.a_lines == 0 || s.b_lines == 0) return MX_OK;
+    if (out == nullptr) return MX_ERR_INVALID_ARG;
+    if (s.k == 0) return gemm_impl(nullptr, nullptr, nullptr, nullptr, out, s.a_lines, s.b_lines, 0, stream);
+    // Operand checks (the workspace is checked separately below).
+    mx_status st = check_encode(a_src, a_rows, a_cols, a_contract, rot, rot_block, rnd, a_src,
+                                a_src);
+    if (st != MX_OK) return st;
+    st = check_encode(b_src, b_rows, b_cols, b_contract, rot, rot_block, rnd, b_src, b_src);
+    if (st != MX_OK) return st;
+    if (s.b_lines % 4 != 0 || !aligned16(out)) return MX_ERR_ALIGN;
+    const size_t need = mx_linear_workspace_bytes(op, T, N, K);
+    if (ws == nullptr || ws_bytes < need) return MX_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MX_ERR_ALIGN;
+    uint8_t *p = static_cast<uint8_t *>(ws);
+    uint8_t *aq = p;
+    p += align256(mx_codes_bytes(s.a_lines, s.k));
+    uint8_t *as = p;
+    p += align256(mx_scales_bytes(s.a_lines, s.k));
+    uint8_t *bq = p;
+    p += align256(mx_codes_bytes(s.b_lines, s.k));
+    uint8_t *bs = p;
+    st = quantize_impl(a_src, a_rows, a_cols, a_contract, rot, rot_block, rnd, seed, 1, aq, as,
+                       stream);
+    if (st != MX_OK) return st;
+    st = quantize_impl(b_src, b_rows, b_cols, b_contract, rot, rot_block, rnd, seed, 2, bq, bs,
+                       stream);
+    if (st != MX_OK) return st;
+    return gemm_impl(aq, as, bq, bs, out, s.a_lines, s.b_lines, s.k, stream);
+}
+}  // namespace
+
+extern "C" {
+
+size_t mx_codes_bytes(int64_t mn, int64_t k) {
+    if (mn <= 0 || k <= 0) return 0;
+    return static_cast<size_t>(mn) * static_cast<size_t>(k / 2);
+}
+
+size_t mx_scales_bytes(int64_t mn, int64_t k) {
+    if (mn <= 0 || k <= 0) return 0;
+    return static_cast<size_t>(scale_groups(mn)) * 128u * static_cast<size_t>(8 * ((k + 255) / 256));
+}
+
+mx_status mx_quantize(const void *d_src, int64_t rows, int64_t cols, int contract, int rot,
+                      int rot_block, int rnd, uint64_t seed, void *d_codes, void *d_scales,
+                      void *stream) {
+    return quantize_impl(d_src, rows, cols, contract, rot, rot_block, rnd, seed, 1, d_codes,
+                         d_scales, static_cast<cudaStream_t>(stream));
+}
+
+mx_status mx_gemm(const void *d_Aq, const void *d_As, const void *d_Bq, const void *d_Bs,
+                  float *d_C, int64_t M, int64_t N, int64_t K, void *stream) {
+    return gemm_impl(d_Aq, d_As, d_Bq, d_Bs, d_C, M, N, K, static_cast<cudaStream_t>(stream));
+}
+
+size_t mx_linear_workspace_bytes(int op, int64_t T, int64_t N, int64_t K) {
+    OpShape s;
+    if (!op_shape(op, T, N, K, &s)) return 0;
+    return align256(mx_codes_bytes(s.a_lines, s.k)) + align256(mx_scales_bytes(s.a_lines, s.k)) +
+           align256(mx_codes_bytes(s.b_lines, s.k)) + align256(mx_scales_bytes(s.b_lines, s.k));
+}
+
+mx_status mx_linear_wgrad(const void *d_dY, const void *d_X, float *d_dW, int64_t T, int64_t N,
+                          int64_t K, int rot, int rot_block, int rnd, uint64_t seed, void *d_ws,
+                          size_t ws_bytes, void *stream) {
+    // dW[N][K] = dY^T X: both operands encoded down their rows (contraction T).
+    return linear_impl(MX_OP_WGRAD, d_dY, T, N, MX_CONTRACT_ROWS, d_X, T, K, MX_CONTRACT_ROWS,
+                       d_dW, T, N, K, rot, rot_block, rnd, seed, d_ws, ws_bytes,
+                       static_cast<cudaStream_t>(stream));
+}
+
+mx_status mx_linear_fprop(const void *d_X, const void *d_W, float *d_Y, int64_t T, int64_t N,
+                          int64_t K, int rot, int rot_block, int rnd, uint64_t seed, void *d_ws,
+                          size_t ws_bytes, void *stream) {
+    // Y[T][N] = X W^T: X[T][K] and W[N][K] encoded along their rows (contraction K).
+    return linear_impl(MX_OP_FPROP, d_X, T, K, MX_CONTRACT_COLS, d_W, N, K, MX_CONTRACT_COLS, d_Y,
+                       T, N, K, rot, rot_block, rnd, seed, d_ws, ws_bytes,
+                       static_cast<cudaStream_t>(stream));
+}
+
+mx_status mx_linear_dgrad(const void *d_dY, const void *d_W, float *d_dX, int64_t T, int64_t N,
+                          int64_t K, int rot, int rot_block, int rnd, uint64_t seed, void *d_ws,
+                          size_t ws_bytes, void *stream) {
+    // dX[T][K] = dY W: dY[T][N] along its rows, W[N][K] down its rows (contraction N).
+    return linear_impl(MX_OP_DGRAD, d_dY, T, N, MX_CONTRACT_COLS, d_W, N, K, MX_CONTRACT_ROWS,
+                       d_dX, T, N, K, rot, rot_block, rnd, seed, d_ws, ws_bytes,
+                       static_cast<cudaStream_t>(stream));
+}
+
+mx_status mx_check_status(void *stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return MX_ERR_CUDA;
+    const DeviceInfo *dev = nullptr;
+    cudaError_t de = cudaSuccess;
+    if ((dev = current_device(&de)) == nullptr) return MX_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, dev->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MX_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+            return MX_ERR_CUDA;
+        return v == kDevTimeout ? MX_ERR_TIMEOUT : MX_ERR_CUDA;
+    }
+    return MX_OK;
+}
+
+mx_status mx_debug_timeout_probe(int64_t limit_us, void *stream) {
+    if (limit_us <= 0 || limit_us > 10 * 1000 * 1000) return MX_ERR_INVALID_ARG;
+    const DeviceInfo *dev = nullptr;
+    mx_status st = device_or_error(&dev);
+    if (st != MX_OK) return st;
+    timeout_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        dev->status, static_cast<uint64_t>(limit_us) * 1000ull);
+    return from_cuda(cudaGetLastError());
+}
+
+const char *mx_status_string(int status) {
+    switch (status) {
+        case MX_OK: return "MX_OK";
+        case MX_ERR_INVALID_ARG: return "MX_ERR_INVALID_ARG";
+        case MX_ERR_SHAPE: return "MX_ERR_SHAPE";
+        case MX_ERR_ALIGN: return "MX_ERR_ALIGN";
+        case MX_ERR_WORKSPACE: return "MX_ERR_WORKSPACE";
+        case MX_ERR_CUDA: return "MX_ERR_CUDA";
+        case MX_ERR_TIMEOUT: return "MX_ERR_TIMEOUT";
+        case MX_ERR_UNSUPPORTED: return "MX_ERR_UNSUPPORTED";
+        default: return "MX_ERR_UNKNOWN";
+    }
+}
+
+int mx_version(void) { return 100; }
+
+}  // extern "C"

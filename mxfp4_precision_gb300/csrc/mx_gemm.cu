@@ -1,0 +1,295 @@
+// mx_gemm.cu -- block-scaled MXFP4 GEMM on the sm_103a tensor cores.
+//
+// C[M][N] (fp32) = A . B^T with A, B MXFP4-encoded along the contraction
+// dimension K: the Fprop, Dgrad and Wgrad GEMMs of "Neue Studie von AMD
+// durchbricht die bestehende Erkenntnis" (eu.36kr.com), section
+// "Fehlerdiagnoseexperiment", run on native FP4 tensor cores with fp32
+// accumulation.
+//
+// Design (one CTA per SM, persistent over 128 x 256 output tiles):
+//   warp 0       TMA producer: 128B-swizzled A/B code tiles (K-tile of 256
+//                FP4 = 128 bytes per row) and the two matching 1 KB scale
+//                slabs per 128 rows, into a 4-stage shared-memory ring.
+//   warp 1       tensor-memory allocator and single-thread MMA issuer: per
+//                stage, tcgen05.cp moves the scale slabs into tensor memory,
+//                then four tcgen05.mma kind::mxf4 (K = 64 each, two E8M0
+//                scales per row per MMA) accumulate into a 128 x 256 fp32
+//                tile held in tensor memory; tcgen05.commit frees the stage.
+//   warps 2..9   epilogue: tcgen05.ld the accumulator (each warp one 32-lane
+//                quarter x 128 columns) into registers, release tensor
+//                memory to the MMA warp at once, then store fp32 rows while
+//                the next tile's main loop runs.
+// Every wait is bounded (see mx_ptx.cuh); a timeout records an error and the
+// CTA unwinds without faulting.
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "mx_internal.h"
+#include "mx_ptx.cuh"
+
+namespace mx {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBKBytes = 128;                 // 256 FP4 values per row per K-tile
+constexpr int kStages = 4;
+constexpr int kThreads = 320;                 // 10 warps
+constexpr int kEpiWarps = 8;
+constexpr uint32_t kABytes = kBM * kBKBytes;  // 16 KB
+constexpr uint32_t kBBytes = kBN * kBKBytes;  // 32 KB
+constexpr uint32_t kSFABytes = 1024;          // 128 rows x 8 blocks
+constexpr uint32_t kSFBBytes = 2048;          // 256 rows x 8 blocks
+constexpr uint32_t kStageBytes = kABytes + kBBytes + kSFABytes + kSFBBytes;  // 52 KB
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCol = 0;               // accumulator: columns [0, 256)
+constexpr uint32_t kSFCol = 256;              // per-stage scale columns: 32 per stage
+
+struct GemmArgs {
+    const uint8_t *As;
+    const uint8_t *Bs;
+    float *C;
+    int64_t M, N, K;
+    int64_t katoms;      // scale k-atoms per 128-row group
+    int64_t b_groups;    // 128-row scale groups that exist for B
+    int k_tiles;
+    int n_tiles;
+    int num_tiles;
+    int *status;
+};
+
+struct SharedCtl {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t acc_full;
+    uint64_t acc_empty;
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+__device__ __forceinline__ void st_global_v4f(float *p, uint32_t a, uint32_t b, uint32_t c,
+                                              uint32_t d) {
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
+                   const __grid_constant__ CUtensorMap map_b, const GemmArgs g) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    SharedCtl *ctl = reinterpret_cast<SharedCtl *>(smem + kStages * kStageBytes);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&ctl->full[s], 1);
+            mbar_init(&ctl->empty[s], 1);
+        }
+        mbar_init(&ctl->acc_full, 1);
+        mbar_init(&ctl->acc_empty, kEpiWarps);
+        mbar_init(&ctl->drain, 1);
+        ctl->abort_flag = 0;
+        fence_barrier_init();
+        prefetch_tmap(&map_a);
+        prefetch_tmap(&map_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(&ctl->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+    volatile int *abort = &ctl->abort_flag;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < g.num_tiles; tile += gridDim.x) {
+                const int mb = tile / g.n_tiles, nb = tile % g.n_tiles;
+                for (int kt = 0; kt < g.k_tiles; ++kt) {
+                    if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, g.status, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *sa = smem + stage * kStageBytes;
+                    uint8_t *sb = sa + kABytes;
+                    uint8_t *sfa = sb + kBBytes;
+                    uint8_t *sfb = sfa + kSFABytes;
+                    const int64_t g0 = 2 * static_cast<int64_t>(nb);
+                    const uint32_t nsfb = (g0 + 1 < g.b_groups) ? 2u : 1u;
+                    mbar_arrive_expect_tx(&ctl->full[stage],
+                                          kABytes + kBBytes + kSFABytes + nsfb * 1024u);
+                    tma_load_2d(sa, &map_a, &ctl->full[stage], kt * kBKBytes, mb * kBM);
+                    tma_load_2d(sb, &map_b, &ctl->full[stage], kt * kBKBytes, nb * kBN);
+                    bulk_load(sfa, g.As + (static_cast<int64_t>(mb) * g.katoms + 2 * kt) * 512,
+                              1024u, &ctl->full[stage]);
+                    for (uint32_t rb = 0; rb < nsfb; ++rb)
+                        bulk_load(sfb + rb * 1024u,
+                                  g.Bs + ((g0 + rb) * g.katoms + 2 * kt) * 512, 1024u,
+                                  &ctl->full[stage]);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < g.num_tiles; tile += gridDim.x) {
+                if (!mbar_wait(&ctl->acc_empty, acc_phase ^ 1u, g.status, abort)) break;
+                tc_fence_after();
+                for (int kt = 0; kt < g.k_tiles; ++kt) {
+                    if (!mbar_wait(&ctl->full[stage], phase, g.status, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + stage * kStageBytes);
+                    const uint32_t sb = sa + kABytes;
+                    const uint32_t sfa = sb + kBBytes;
+                    const uint32_t sfb = sfa + kSFABytes;
+                    const uint32_t sf_col = tmem + kSFCol + 32u * stage;
+                    // Scale slabs -> tensor memory.  A: 4 columns per k-atom.
+                    // B: per k-atom, 4 columns per 128-row group (rows 128..255
+                    // of the 256-row tile follow rows 0..127).
+#pragma unroll
+                    for (int ka = 0; ka < 2; ++ka) {
+                        tmem_cp_32x128b_x4(sf_col + 4u * ka, sdesc_sf(sfa + 512u * ka));
+#pragma unroll
+                        for (int rb = 0; rb < 2; ++rb)
+                            tmem_cp_32x128b_x4(sf_col + 8u + 8u * ka + 4u * rb,
+                                               sdesc_sf(sfb + 1024u * rb + 512u * ka));
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int ka = j / 2, sf_id = (j % 2) * 2;
+                        mma_mxf4(tmem + kAccCol, sdesc_sw128(sa + 32u * j),
+                                 sdesc_sw128(sb + 32u * j), idesc_mxf4(kBM, kBN, sf_id, sf_id),
+                                 sf_col + 4u * ka, sf_col + 8u + 8u * ka,
+                                 (kt > 0 || j > 0) ? 1u : 0u);
+                    }
+                    tc_commit(&ctl->empty[stage]);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                tc_commit(&ctl->acc_full);
+                acc_phase ^= 1u;
+            }
+            // Make sure every tensor-core operation issued here has finished
+            // before tensor memory is released.
+            tc_commit(&ctl->drain);
+            mbar_wait(&ctl->drain, 0, g.status, nullptr, 100ull * 1000ull * 1000ull);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;           // TMEM lane quarter this warp may access
+        const int half = (warp - 2) / 4;  // column half of the 256-wide tile
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < g.num_tiles; tile += gridDim.x) {
+            const int mb = tile / g.n_tiles, nb = tile % g.n_tiles;
+            // One lane waits; the verdict is broadcast so the warp stays
+            // converged for the .sync.aligned tensor-memory loads.
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(&ctl->acc_full, acc_phase, g.status, abort) ? 1 : 0;
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t v[4][32];
+            const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + kAccCol +
+                                   128u * half;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tbase + 32u * c, v[c]);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->acc_empty);
+            acc_phase ^= 1u;
+
+            const int64_t row = static_cast<int64_t>(mb) * kBM + 32 * q + lane;
+            if (row < g.M) {
+                float *crow = g.C + row * g.N;
+                const int64_t col0 = static_cast<int64_t>(nb) * kBN + 128 * half;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int64_t col = col0 + 32 * c + 4 * j;
+                        if (col + 3 < g.N) {
+                            st_global_v4f(crow + col, v[c][4 * j], v[c][4 * j + 1],
+                                          v[c][4 * j + 2], v[c][4 * j + 3]);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                if (col + e < g.N) crow[col + e] = __uint_as_float(v[c][4 * j + e]);
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+constexpr size_t kGemmSmem = kStages * kStageBytes + sizeof(SharedCtl) + 1024;
+
+}  // namespace
+
+cudaError_t launch_gemm(const void *Aq, const void *As, const void *Bq, const void *Bs, float *C,
+                        int64_t M, int64_t N, int64_t K, const DeviceInfo &dev,
+                        cudaStream_t stream) {
+    CUtensorMap map_a, map_b;
+    if (!encode_tmap_2d(&map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, Aq, K / 2, M, K / 2, kBKBytes, kBM,
+                        CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    if (!encode_tmap_2d(&map_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, Bq, K / 2, N, K / 2, kBKBytes, kBN,
+                        CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    GemmArgs g{};
+    g.As = static_cast<const uint8_t *>(As);
+    g.Bs = static_cast<const uint8_t *>(Bs);
+    g.C = C;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.katoms = scale_katoms(K);
+    g.b_groups = scale_groups(N);
+    g.k_tiles = static_cast<int>((K + 255) / 256);
+    const int64_t m_tiles = (M + kBM - 1) / kBM;
+    const int64_t n_tiles = (N + kBN - 1) / kBN;
+    if (m_tiles * n_tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    g.n_tiles = static_cast<int>(n_tiles);
+    g.num_tiles = static_cast<int>(m_tiles * n_tiles);
+    g.status = dev.status;
+    cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kGemmSmem));
+    if (e != cudaSuccess) return e;
+    const int grid = g.num_tiles < dev.sm_count ? g.num_tiles : dev.sm_count;
+    mx_gemm_kernel<<<grid, kThreads, kGemmSmem, stream>>>(map_a, map_b, g);
+    return cudaGetLastError();
+}
+
+}  // namespace mx

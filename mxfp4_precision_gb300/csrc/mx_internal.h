@@ -1,0 +1,39 @@
+// mx_internal.h -- host-side glue shared by the library's translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace mx {
+
+struct DeviceInfo {
+    int ordinal = -1;
+    int sm_count = 0;
+    int cc_major = 0, cc_minor = 0;
+    int *status = nullptr;  // device address of the per-device status word
+};
+
+// Lazily-filled info for the current device; nullptr (and *err set) on failure.
+const DeviceInfo *current_device(cudaError_t *err);
+
+// Host wrapper of cuTensorMapEncodeTiled for a 2-D row-major tensor.
+bool encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base,
+                    uint64_t inner_elems, uint64_t outer_elems, uint64_t row_bytes,
+                    uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
+
+// Scale-layout geometry (see mx.h): k-atoms (4 blocks of 32) per 128-line group.
+inline int64_t scale_katoms(int64_t k) { return 2 * ((k + 255) / 256); }
+inline int64_t scale_groups(int64_t mn) { return (mn + 127) / 128; }
+
+// Kernel launchers (argument validation happens before these are called).
+cudaError_t launch_quantize(const void *src, int64_t rows, int64_t cols, int contract, int rot,
+                            int rot_block, int rnd, uint64_t seed, uint64_t sr_tag,
+                            void *codes, void *scales, const DeviceInfo &dev,
+                            cudaStream_t stream);
+
+cudaError_t launch_gemm(const void *Aq, const void *As, const void *Bq, const void *Bs, float *C,
+                        int64_t M, int64_t N, int64_t K, const DeviceInfo &dev,
+                        cudaStream_t stream);
+
+}  // namespace mx

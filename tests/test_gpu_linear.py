@@ -1,0 +1,159 @@
+"""GPU parity of the linear-layer entry points (Wgrad / Fprop / Dgrad) against
+the oracle, on small ragged shapes (full outputs) and on the full-size
+Llama-3.1-8B-shaped workloads (every code byte where affordable, otherwise
+sampled lines; sampled output entries computed one by one by the oracle)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import mxfp4_precision_gb300 as mx
+from tests.mx_testutil import assert_gemm_close, untile_scales
+from workloads import bf16_bits, config_inputs
+
+pytestmark = pytest.mark.gpu
+
+OC = {mx.CONTRACT_ROWS: oracle.CONTRACT_ROWS, mx.CONTRACT_COLS: oracle.CONTRACT_COLS}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from mxfp4_precision_gb300 import build
+    build.build()
+    mx.lib()
+
+
+def _dev(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda()
+
+
+def _operands(op, a, b):
+    """(contract, lines) of operands A and B for an op, from the input shapes."""
+    if op == mx.OP_WGRAD:          # dY [T,N] -> lines N; X [T,K] -> lines K
+        return (mx.CONTRACT_ROWS, a.shape[1]), (mx.CONTRACT_ROWS, b.shape[1])
+    if op == mx.OP_FPROP:          # X [T,K] -> lines T; W [N,K] -> lines N
+        return (mx.CONTRACT_COLS, a.shape[0]), (mx.CONTRACT_COLS, b.shape[0])
+    return (mx.CONTRACT_COLS, a.shape[0]), (mx.CONTRACT_ROWS, b.shape[1])  # DGRAD
+
+
+def run_op(op, a, b, rot, nb, rnd, seed):
+    fn = {mx.OP_WGRAD: mx.linear_wgrad, mx.OP_FPROP: mx.linear_fprop,
+          mx.OP_DGRAD: mx.linear_dgrad}[op]
+    out = fn(_dev(a), _dev(b), rot=rot, rot_block=nb, rnd=rnd, seed=seed)
+    mx.check_status()
+    return out
+
+
+def sample_lines(n, count, seed):
+    rng = np.random.default_rng(seed)
+    base = {0, n - 1, min(127, n - 1), min(128, n - 1), n // 2}
+    extra = rng.choice(n, size=min(count, n), replace=False)
+    return np.array(sorted(base | set(int(v) for v in extra)), dtype=np.int64)
+
+
+def check_op(op, a, b, rot, nb, rnd=mx.ROUND_RNE, seed=0, sample=None):
+    out = run_op(op, a, b, rot, nb, rnd, seed).cpu().numpy()
+    (ca, na), (cb, nb_lines) = _operands(op, a, b)
+    ia = None if sample is None else sample_lines(na, sample, 1)
+    jb = None if sample is None else sample_lines(nb_lines, sample, 2)
+    Aq, As = oracle.quantize(a, OC[ca], rot, nb, rnd, seed, 1, lines=ia)
+    Bq, Bs = oracle.quantize(b, OC[cb], rot, nb, rnd, seed, 2, lines=jb)
+    Cref, Cabs = oracle.gemm(Aq, As, Bq, Bs)
+    got = out if sample is None else out[np.ix_(ia, jb)]
+    return assert_gemm_close(got, Cref, Cabs, f"op {op} rot {rot}/{nb} rnd {rnd}")
+
+
+def _bits(shape, seed, scale=1.0):
+    rng = np.random.default_rng(seed)
+    return bf16_bits(rng.standard_normal(shape).astype(np.float32) * np.float32(scale))
+
+
+def test_tiny_wgrad_full():
+    d = config_inputs("tiny", seed=0)
+    worst = check_op(mx.OP_WGRAD, d["dY"], d["X"], mx.ROT_HADAMARD_DET, 32)
+    assert worst < 1e-5
+
+
+@pytest.mark.parametrize("rot,nb,rnd", [(mx.ROT_HADAMARD_DET, 32, mx.ROUND_RNE),
+                                        (mx.ROT_NONE, 32, mx.ROUND_RNE),
+                                        (mx.ROT_HADAMARD_RAND, 64, mx.ROUND_RNE),
+                                        (mx.ROT_NONE, 32, mx.ROUND_SR),
+                                        (mx.ROT_HADAMARD_DET, 256, mx.ROUND_SR)])
+def test_small_ragged_all_ops(rot, nb, rnd):
+    T, N, K = 1280, 200, 328
+    dY, X = _bits((T, N), 1, 1e-3), _bits((T, K), 2)
+    check_op(mx.OP_WGRAD, dY, X, rot, nb, rnd, seed=3)
+    # Fprop: X [T', K'] W [N', K'] with contraction K' = 1280
+    X2, W = _bits((200, 1280), 3), _bits((328, 1280), 4, 0.02)
+    check_op(mx.OP_FPROP, X2, W, rot, nb, rnd, seed=3)
+    # Dgrad: dY [T', N'] W [N', K'] with contraction N' = 1280
+    dY2, W2 = _bits((200, 1280), 5, 1e-3), _bits((1280, 328), 6, 0.02)
+    check_op(mx.OP_DGRAD, dY2, W2, rot, nb, rnd, seed=3)
+
+
+def test_deterministic_bits():
+    d = config_inputs("tiny", seed=0)
+    a = run_op(mx.OP_WGRAD, d["dY"], d["X"], mx.ROT_HADAMARD_DET, 32, mx.ROUND_RNE, 0)
+    b = run_op(mx.OP_WGRAD, d["dY"], d["X"], mx.ROT_HADAMARD_DET, 32, mx.ROUND_RNE, 0)
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def test_timeout_path_reports_without_hanging():
+    # the probe's barrier is never completed; its wait must give up and report
+    assert mx.debug_timeout_probe(20000) == 6
+    mx.check_status()                      # cleared: next status is OK
+    d = config_inputs("tiny", seed=0)      # and the context is still usable
+    check_op(mx.OP_WGRAD, d["dY"], d["X"], mx.ROT_HADAMARD_DET, 32)
+
+
+# ---------------------------------------------------------------- full size
+def _compare_codes(bits, contract, rot, nb, rnd, seed, lines=None):
+    rows, cols = bits.shape
+    L, n = (rows, cols) if contract == mx.CONTRACT_ROWS else (cols, rows)
+    codes, scales = mx.quantize(_dev(bits), contract, rot, nb, rnd, seed)
+    mx.check_status()
+    codes, scales = codes.cpu().numpy(), untile_scales(scales.cpu().numpy(), n, L)
+    oc, os_ = oracle.quantize(bits, OC[contract], rot, nb, rnd, seed, 1, lines=lines)
+    if lines is not None:
+        codes, scales = codes[lines], scales[lines]
+    assert np.array_equal(codes, oc) and np.array_equal(scales, os_)
+
+
+@pytest.mark.slow
+def test_o_proj_full_size():
+    d = config_inputs("o_proj", seed=0)
+    for name in ("dY", "X"):
+        _compare_codes(d[name], mx.CONTRACT_ROWS, mx.ROT_HADAMARD_DET, 32, mx.ROUND_RNE, 0)
+    worst = check_op(mx.OP_WGRAD, d["dY"], d["X"], mx.ROT_HADAMARD_DET, 32, sample=48)
+    assert worst < 1e-5
+
+
+@pytest.mark.slow
+def test_down_proj_rotation_sweep():
+    d = config_inputs("down_proj", seed=0)
+    for nb in (16, 32, 64, 128, 256):
+        lines = sample_lines(14336, 96, nb)
+        _compare_codes(d["X"], mx.CONTRACT_ROWS, mx.ROT_HADAMARD_DET, nb, mx.ROUND_RNE, 0, lines)
+        check_op(mx.OP_WGRAD, d["dY"], d["X"], mx.ROT_HADAMARD_DET, nb, sample=24)
+
+
+@pytest.mark.slow
+def test_ablation_modes_full_size():
+    d = config_inputs("ablation", seed=0)
+    for rot, nb, rnd, seed in [(mx.ROT_NONE, 32, mx.ROUND_RNE, 0),
+                               (mx.ROT_HADAMARD_RAND, 32, mx.ROUND_RNE, 1),
+                               (mx.ROT_NONE, 32, mx.ROUND_SR, 1)]:
+        lines = sample_lines(4096, 64, 7)
+        _compare_codes(d["dY"], mx.CONTRACT_ROWS, rot, nb, rnd, seed, lines)
+        check_op(mx.OP_WGRAD, d["dY"], d["X"], rot, nb, rnd, seed, sample=24)
+
+
+@pytest.mark.slow
+def test_qkv_gateup_all_three_gemms():
+    d = config_inputs("qkv_gateup", seed=0)
+    X = d["X"]
+    for w, dy in (("W_qkv", "dY_qkv"), ("W_gu", "dY_gu")):
+        W, dY = d[w], d[dy]
+        check_op(mx.OP_FPROP, X, W, mx.ROT_NONE, 32, sample=24)
+        check_op(mx.OP_DGRAD, dY, W, mx.ROT_NONE, 32, sample=24)
+        check_op(mx.OP_WGRAD, dY, X, mx.ROT_HADAMARD_DET, 32, sample=24)

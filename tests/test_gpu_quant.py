@@ -1,0 +1,131 @@
+"""GPU parity: mx_quantize codes and scales are bit-exact with the oracle.
+
+Shapes span several tiles with ragged tails (200 lines: not a multiple of the
+64/128-line tiles; contraction 800: not a multiple of the 256 tile) and every
+rotation size, random-sign mode and stochastic rounding."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import mxfp4_precision_gb300 as mx
+from tests.mx_testutil import tile_scales, untile_scales
+from workloads import bf16_bits, config_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from mxfp4_precision_gb300 import build
+    build.build()
+    mx.lib()
+
+
+def gpu_quantize(bits: np.ndarray, contract, rot, nb, rnd, seed):
+    src = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda()
+    codes, scales = mx.quantize(src, contract, rot, nb, rnd, seed)
+    mx.check_status()
+    return codes.cpu().numpy(), scales.cpu().numpy()
+
+
+def check_against_oracle(bits, contract, rot, nb, rnd, seed=0):
+    rows, cols = bits.shape
+    L, lines = (rows, cols) if contract == mx.CONTRACT_ROWS else (cols, rows)
+    codes, scales = gpu_quantize(bits, contract, rot, nb, rnd, seed)
+    oc, os_ = oracle.quantize(bits, contract, rot, nb, rnd, seed, 1)
+    assert codes.shape == oc.shape
+    diff = np.argwhere(codes != oc)
+    assert diff.size == 0, f"{len(diff)} code bytes differ; first {diff[:4].tolist()}"
+    assert np.array_equal(untile_scales(scales, lines, L), os_)
+    assert np.array_equal(scales, tile_scales(os_, lines, L))   # padding bytes are zero
+
+
+def _rand_bits(shape, seed, scale=1.0, outliers=True):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal(shape).astype(np.float32) * np.float32(scale)
+    if outliers:
+        x[:, rng.choice(shape[1], 3, replace=False)] *= 20
+    return bf16_bits(x)
+
+
+ROTS = [(mx.ROT_NONE, 32), (mx.ROT_HADAMARD_DET, 16), (mx.ROT_HADAMARD_DET, 32),
+        (mx.ROT_HADAMARD_DET, 64), (mx.ROT_HADAMARD_DET, 128), (mx.ROT_HADAMARD_DET, 256),
+        (mx.ROT_HADAMARD_RAND, 32), (mx.ROT_HADAMARD_RAND, 256)]
+
+
+@pytest.mark.parametrize("rot,nb", ROTS)
+@pytest.mark.parametrize("rnd", [mx.ROUND_RNE, mx.ROUND_SR])
+def test_colwise_parity(rot, nb, rnd):
+    check_against_oracle(_rand_bits((1280, 200), 1), mx.CONTRACT_ROWS, rot, nb, rnd, seed=5)
+
+
+@pytest.mark.parametrize("rot,nb", ROTS)
+@pytest.mark.parametrize("rnd", [mx.ROUND_RNE, mx.ROUND_SR])
+def test_rowwise_parity(rot, nb, rnd):
+    check_against_oracle(_rand_bits((200, 1280), 2), mx.CONTRACT_COLS, rot, nb, rnd, seed=5)
+
+
+@pytest.mark.parametrize("contract", [mx.CONTRACT_ROWS, mx.CONTRACT_COLS])
+@pytest.mark.parametrize("rot,nb", [(mx.ROT_NONE, 32), (mx.ROT_HADAMARD_DET, 16),
+                                    (mx.ROT_HADAMARD_DET, 32)])
+def test_ragged_contraction_tail(contract, rot, nb):
+    shape = (800, 136) if contract == mx.CONTRACT_ROWS else (136, 800)
+    check_against_oracle(_rand_bits(shape, 3), contract, rot, nb, mx.ROUND_RNE)
+
+
+def _edge_matrix():
+    """256 x 64 bf16 (T x C) where each column exercises one edge case."""
+    x = np.zeros((256, 64), dtype=np.float32)
+    x[7, 1] = 3.0                                          # single non-zero
+    x[:, 2] = np.exp2(np.arange(256) % 40 - 20)            # exact powers of two
+    x[:, 3] = 1.75 * np.exp2(np.arange(256) % 7)           # amax mantissa > 1.5: saturation
+    x[:, 4] = np.exp2(-133.0) * (np.arange(256) % 100 + 1)  # bf16 subnormals
+    x[:, 5] = -0.0                                         # negative zeros
+    ties = np.array([4, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5, -0.25, -0.75, -1.25, -1.75,
+                     -2.5, -3.5, -5, 6, 0.5, 1, 1.5, 2, 3, -4, -6, 0.1, -0.1, 7, -7.5,
+                     0.3, 1.1, 2.9, 4.4, -5.5], dtype=np.float32)
+    x[:, 6] = np.tile(ties, 8) * np.float32(2.0 ** 3)      # exact ties at scale 2^3
+    x[:, 7] = np.tile(ties, 8) * np.float32(2.0 ** -120)
+    x[100, 8] = np.inf
+    x[40, 9] = np.nan
+    x[:, 10] = 3.0e38 * np.sign(np.arange(256) - 127.5)    # near the bf16 maximum
+    x[:, 11] = 1.2e-38 * (np.arange(256) % 5 - 2)          # smallest normals
+    x[5, 12] = -np.inf
+    rng = np.random.default_rng(9)
+    x[:, 13:] = rng.standard_normal((256, 51)) * np.exp2(rng.integers(-30, 30, (1, 51)))
+    return bf16_bits(x)
+
+
+@pytest.mark.parametrize("rot,nb", [(mx.ROT_NONE, 32), (mx.ROT_HADAMARD_DET, 32),
+                                    (mx.ROT_HADAMARD_DET, 256), (mx.ROT_HADAMARD_RAND, 64)])
+@pytest.mark.parametrize("rnd", [mx.ROUND_RNE, mx.ROUND_SR])
+def test_edge_cases(rot, nb, rnd):
+    x = _edge_matrix()
+    check_against_oracle(x, mx.CONTRACT_ROWS, rot, nb, rnd, seed=3)
+    check_against_oracle(np.ascontiguousarray(x.T), mx.CONTRACT_COLS, rot, nb, rnd, seed=3)
+
+
+def test_deterministic_and_seeded():
+    x = _rand_bits((512, 128), 4)
+    a = gpu_quantize(x, mx.CONTRACT_ROWS, mx.ROT_HADAMARD_DET, 32, mx.ROUND_RNE, 0)
+    b = gpu_quantize(x, mx.CONTRACT_ROWS, mx.ROT_HADAMARD_DET, 32, mx.ROUND_RNE, 77)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    r1 = gpu_quantize(x, mx.CONTRACT_ROWS, mx.ROT_HADAMARD_RAND, 32, mx.ROUND_SR, 1)
+    r2 = gpu_quantize(x, mx.CONTRACT_ROWS, mx.ROT_HADAMARD_RAND, 32, mx.ROUND_SR, 1)
+    r3 = gpu_quantize(x, mx.CONTRACT_ROWS, mx.ROT_HADAMARD_RAND, 32, mx.ROUND_SR, 2)
+    assert np.array_equal(r1[0], r2[0]) and not np.array_equal(r1[0], r3[0])
+
+
+def test_empty_inputs_are_noops():
+    src = torch.zeros((0, 64), dtype=torch.int16, device="cuda")
+    codes = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    mx.quantize_into(src, codes, codes, mx.CONTRACT_ROWS)
+    mx.check_status()
+    assert int(codes.sum()) == 0
+
+
+def test_tiny_config_both_operands():
+    d = config_inputs("tiny", seed=0)
+    for name in ("dY", "X"):
+        check_against_oracle(d[name], mx.CONTRACT_ROWS, mx.ROT_HADAMARD_DET, 32, mx.ROUND_RNE)
