@@ -1,0 +1,435 @@
+#!/usr/bin/env python3
+"""Benchmark of the MXFP4 Wgrad hot path on one GB300.
+
+Metric: MXFP4 Wgrad TFLOP/s including the Hadamard rotation and quantisation,
+2*N*K*T / step time, on the Llama-3.1-8B attention o_proj shape (T = 8192
+tokens, dY [8192, 4096], X [8192, 4096] -> dW [4096, 4096] fp32), deterministic
+block Hadamard of 32 along T, round-to-nearest-even.  Inputs are synthetic
+(seeded; Student-t(3) gradients with std 1e-3, N(0,1) activations with 1% x20
+outlier channels) and resident in HBM when the timed region starts.
+
+One step = the three launches of the hot path through the C ABI:
+mx_quantize(dY), mx_quantize(X), mx_gemm.  L2 is flushed (512 MB write)
+before every timed step, outside the events.  `e2e` repeats the step through
+mx_linear_wgrad with pinned HOST buffers, the H2D/D2H copies inside the
+timed region.  The reference arm (--impl reference) times the CPU oracle on
+a bounded sample of the same workload.
+
+Multi-GPU: the path runs as independent replicas (weak scaling); under
+torchrun every rank times its own replica and rank 0 reports
+sum(units) / max(time).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MXFP4 Wgrad TFLOPS incl. Hadamard+quant, Llama-3.1-8B shapes; % FP4 peak"
+WORKLOADS = {
+    # name: (config key, T, N, K)
+    "o_proj": ("o_proj", 8192, 4096, 4096),
+    "down_proj": ("down_proj", 8192, 4096, 14336),
+}
+NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25      # nominal dense ratio (recipe table)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------------------
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash(name: str) -> str:
+    with open(os.path.join(ROOT, "mxfp4_precision_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def load_traffic():
+    """DRAM bytes per launch from committed ncu summaries (profiles/traffic.txt):
+    lines `kernel source_hash workload bytes`.  Ignored when the kernel source
+    changed since the capture."""
+    out = {}
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return out
+    with open(path) as f:
+        for line in f:
+            line = line.split("#", 1)[0].split()
+            if len(line) == 4:
+                out[(line[0], line[2])] = (line[1], float(line[3]))
+    return out
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.05)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx_, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx_.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx_),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int, device) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def oracle_sample(d, T, N, K, s_lines, seed=0):
+    """One bounded oracle sample: encode s_lines lines of each operand over the
+    full T and contract them (s_lines^2 outputs).  Returns (seconds, flops)."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(seed)
+    la = np.sort(rng.choice(N, s_lines, replace=False))
+    lb = np.sort(rng.choice(K, s_lines, replace=False))
+    t0 = time.perf_counter()
+    Aq, As = oracle.quantize(d["dY"], oracle.CONTRACT_ROWS, oracle.ROT_HADAMARD_DET, 32,
+                             oracle.ROUND_RNE, 0, 1, lines=la)
+    Bq, Bs = oracle.quantize(d["X"], oracle.CONTRACT_ROWS, oracle.ROT_HADAMARD_DET, 32,
+                             oracle.ROUND_RNE, 0, 2, lines=lb)
+    oracle.gemm(Aq, As, Bq, Bs)
+    return time.perf_counter() - t0, 2.0 * s_lines * s_lines * T
+
+
+def calibrate_sample(d, T, N, K, budget_s):
+    """Lines per operand so that one oracle sample takes about budget_s
+    (the contraction, quadratic in the lines, dominates the cost)."""
+    dt, _ = oracle_sample(d, T, N, K, 64)
+    s = int(64 * (budget_s / max(dt, 1e-6)) ** 0.5) // 16 * 16
+    return max(16, min(s, N, K))
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    from workloads import config_inputs
+    cfg, T, N, K = WORKLOADS[args.workload]
+    d = config_inputs(cfg, seed=0, only=("dY", "X"))
+    total_budget = args.ref_budget_s
+    per_step = max(0.01, total_budget / max(1, args.steps + args.warmup))
+    s = calibrate_sample(d, T, N, K, per_step)
+    for i in range(args.warmup):
+        oracle_sample(d, T, N, K, s, seed=100 + i)
+    times, flops = [], 0.0
+    for i in range(args.steps):
+        dt, f = oracle_sample(d, T, N, K, s, seed=i)
+        times.append(dt)
+        flops += f
+    tot = sum(times)
+    value = flops / tot / 1e12
+    sample = (f"per step: {s} lines of dY and {s} lines of X (full T={T}) encoded with "
+              f"det-Hadamard-32 + RNE, then their {s}x{s} block of dW contracted in double")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+            "data": "synthetic",
+            "config": workload_config(args, T, N, K),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(args, T, N, K):
+    return {"workload": f"{args.workload} Wgrad: dY [{T},{N}] x X [{T},{K}] -> dW [{N},{K}] fp32, "
+                        f"deterministic Hadamard 32 along T, MXFP4 block 32, RNE",
+            "T": T, "N": N, "K": K, "rot": "hadamard_det", "rot_block": 32, "round": "rne",
+            "l2": "flushed before every timed step (512 MB write, outside the events)",
+            "parallelism": "replicas" if args.gpus > 1 else "single-gpu"}
+
+
+def run_mine(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    import mxfp4_precision_gb300 as mx
+    from workloads import config_inputs
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    cfg, T, N, K = WORKLOADS[args.workload]
+    d = config_inputs(cfg, seed=0, only=("dY", "X"))
+    dY_h = torch.from_numpy(d["dY"].view(np.int16)).pin_memory()
+    X_h = torch.from_numpy(d["X"].view(np.int16)).pin_memory()
+    dY = dY_h.to(dev)
+    X = X_h.to(dev)
+    stream = torch.cuda.current_stream(dev)
+    L = mx.lib()
+    sp = stream.cuda_stream
+    rot, nb, rnd, seed = mx.ROT_HADAMARD_DET, 32, mx.ROUND_RNE, 0
+
+    aq = torch.empty(mx.codes_bytes(N, T), dtype=torch.uint8, device=dev)
+    as_ = torch.empty(mx.scales_bytes(N, T), dtype=torch.uint8, device=dev)
+    bq = torch.empty(mx.codes_bytes(K, T), dtype=torch.uint8, device=dev)
+    bs = torch.empty(mx.scales_bytes(K, T), dtype=torch.uint8, device=dev)
+    dW = torch.empty((N, K), dtype=torch.float32, device=dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    ptr = lambda t: t.data_ptr()
+
+    def step_parts():
+        s1 = L.mx_quantize(ptr(dY), T, N, mx.CONTRACT_ROWS, rot, nb, rnd, seed, ptr(aq), ptr(as_), sp)
+        yield s1
+        s2 = L.mx_quantize(ptr(X), T, K, mx.CONTRACT_ROWS, rot, nb, rnd, seed, ptr(bq), ptr(bs), sp)
+        yield s2
+        s3 = L.mx_gemm(ptr(aq), ptr(as_), ptr(bq), ptr(bs), ptr(dW), N, K, T, sp)
+        yield s3
+
+    def check(st, what):
+        if st != 0:
+            raise RuntimeError(f"{what} failed: {mx.status_string(st)}")
+
+    # warm-up
+    for _ in range(args.warmup):
+        flush.zero_()
+        for st in step_parts():
+            check(st, "warm-up")
+    torch.cuda.synchronize(dev)
+    mx.check_status()
+
+    n = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        for i in range(n):
+            flush.zero_()
+            ev[i][0].record(stream)
+            for j, st in enumerate(step_parts()):
+                check(st, "step")
+                ev[i][j + 1].record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    mx.check_status()
+    q1 = [ev[i][0].elapsed_time(ev[i][1]) for i in range(n)]
+    q2 = [ev[i][1].elapsed_time(ev[i][2]) for i in range(n)]
+    gm = [ev[i][2].elapsed_time(ev[i][3]) for i in range(n)]
+    step_ms = [a + b + c for a, b, c in zip(q1, q2, gm)]
+    total_ms = reduce_max(sum(step_ms), world, dev)
+    flops_step = 2.0 * N * K * T
+    value = world * n * flops_step / (total_ms * 1e-3) / 1e12
+
+    # ---- e2e: public call with host buffers, copies inside the timed region
+    ws = torch.empty(mx.linear_workspace_bytes(mx.OP_WGRAD, T, N, K), dtype=torch.uint8, device=dev)
+    dW_h = torch.empty((N, K), dtype=torch.float32).pin_memory()
+    dY_d = torch.empty_like(dY)
+    X_d = torch.empty_like(X)
+    n_e2e = max(3, min(n, args.e2e_steps))
+    e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_e2e + 2)]
+    for i in range(n_e2e + 2):       # first two are warm-up
+        flush.zero_()
+        e_ev[i][0].record(stream)
+        dY_d.copy_(dY_h, non_blocking=True)
+        X_d.copy_(X_h, non_blocking=True)
+        check(L.mx_linear_wgrad(ptr(dY_d), ptr(X_d), ptr(dW), T, N, K, rot, nb, rnd, seed,
+                                ptr(ws), ws.numel(), sp), "e2e")
+        dW_h.copy_(dW, non_blocking=True)
+        e_ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    mx.check_status()
+    e2e_ms = reduce_max(sum(e_ev[i][0].elapsed_time(e_ev[i][1]) for i in range(2, n_e2e + 2)),
+                        world, dev)
+    e2e_value = world * n_e2e * flops_step / (e2e_ms * 1e-3) / 1e12
+
+    # parity spot check of the timed output (oracle entries, rank 0 only)
+    parity = None
+    if rank == 0 and not args.no_parity_check:
+        parity = spot_check(d, dW, T, N, K)
+
+    if rank != 0:
+        return 0
+    peaks, peak_src = load_peaks()
+    fp4_peak = peaks["bf16_tflops"] * NOMINAL_FP4_OVER_BF16
+    hbm = peaks["hbm_gbs"]
+    q_bytes_n = N * T * (2 + 0.5 + 1 / 32)      # bf16 in, codes + scales out
+    q_bytes_k = K * T * (2 + 0.5 + 1 / 32)
+    mean = lambda v: sum(v) / len(v)
+    t_q1, t_q2, t_g = mean(q1), mean(q2), mean(gm)
+    traffic = load_traffic()
+    wl = args.workload
+
+    def tr(kernel, file):
+        hit = traffic.get((kernel, wl))
+        if hit and hit[0] == kernel_source_hash(file):
+            return hit[1]
+        return None
+
+    gemm_rf = {"kernel": "mx_gemm_kernel", "bound": "tensor",
+               "achieved": flops_step / (t_g * 1e-3) / 1e12,
+               "peak": fp4_peak, "unit": "TFLOP/s",
+               "frac": flops_step / (t_g * 1e-3) / 1e12 / fp4_peak,
+               "traffic": tr("mx_gemm_kernel", "mx_gemm.cu"),
+               "peak_basis": f"{peak_src} bf16 burst {peaks['bf16_tflops']} TFLOP/s x nominal "
+                             f"fp4/bf16 ratio {NOMINAL_FP4_OVER_BF16:g}",
+               "ms_per_launch": t_g}
+    quant_rf = {"kernel": "mxq_colwise_kernel", "bound": "hbm",
+                "achieved": (q_bytes_n + q_bytes_k) / ((t_q1 + t_q2) * 1e-3) / 1e9,
+                "peak": hbm, "unit": "GB/s",
+                "frac": (q_bytes_n + q_bytes_k) / ((t_q1 + t_q2) * 1e-3) / 1e9 / hbm,
+                "traffic": tr("mxq_colwise_kernel", "mx_quant.cu"),
+                "peak_basis": f"{peak_src} HBM copy bandwidth",
+                "ms_per_launch": (t_q1 + t_q2) / 2}
+    dominant = gemm_rf if t_g >= (t_q1 + t_q2) else quant_rf
+    clk = clocks.summary()
+    cpu = None
+    if not args.no_cpu_baseline:
+        s = calibrate_sample(d, T, N, K, args.cpu_budget_s)
+        dt, f = oracle_sample(d, T, N, K, s)
+        cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+               "sample": f"{s} lines of dY and {s} lines of X (full T={T}) encoded "
+                         f"(det-Hadamard-32, RNE), then their {s}x{s} block of dW contracted "
+                         f"in double; {dt:.1f} s single-threaded"}
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": n, "warmup": args.warmup, "ms_per_step": total_ms / n,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "mxfp4 (e2m1 x e8m0, fp32 accumulate)", "data": "synthetic",
+            "config": workload_config(args, T, N, K),
+            "roofline": {k: dominant[k] for k in ("bound", "achieved", "peak", "unit", "frac",
+                                                   "traffic")},
+            "roofline_kernels": [gemm_rf, quant_rf],
+            "fp4_peak_fraction": value / fp4_peak,
+            "breakdown_ms": {"quantize_dY": t_q1, "quantize_X": t_q2, "gemm": t_g},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": dY_h.numel() * 2 + X_h.numel() * 2,
+                    "d2h_bytes_per_step": dW_h.numel() * 4,
+                    "ms_per_step": e2e_ms / n_e2e, "call": "mx_linear_wgrad"},
+            "gpu_launches": 3 * n,
+            "clocks": clk,
+            "parity_spot_check": parity}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def spot_check(d, dW, T, N, K):
+    """Oracle check of 32 x 32 sampled entries of the timed dW."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(123)
+    ia = np.sort(rng.choice(N, 32, replace=False))
+    jb = np.sort(rng.choice(K, 32, replace=False))
+    Aq, As = oracle.quantize(d["dY"], oracle.CONTRACT_ROWS, oracle.ROT_HADAMARD_DET, 32,
+                             oracle.ROUND_RNE, 0, 1, lines=ia)
+    Bq, Bs = oracle.quantize(d["X"], oracle.CONTRACT_ROWS, oracle.ROT_HADAMARD_DET, 32,
+                             oracle.ROUND_RNE, 0, 2, lines=jb)
+    C, Ca = oracle.gemm(Aq, As, Bq, Bs)
+    got = dW.cpu().numpy()[np.ix_(ia, jb)].astype(np.float64)
+    ratio = float((np.abs(got - C) / np.maximum(Ca, 1e-300)).max())
+    return {"entries": 1024, "max_err_over_sum_abs": ratio, "pass": ratio <= 1e-5}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="o_proj")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--ref-budget-s", type=float, default=120.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-parity-check", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_mine(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
