@@ -161,6 +161,39 @@ mx_status mx_linear_dgrad(const void *d_dY, const void *d_W, float *d_dX, int64_
                           int64_t K, int rot, int rot_block, int rnd, uint64_t seed,
                           void *d_ws, size_t ws_bytes, void *stream);
 
+/*
+ * mx_linear_wgrad_noalloc -- mx_linear_wgrad without a caller workspace.
+ * No counterpart in the paper: this is a deployment convenience.
+ *
+ * For callers that cannot allocate device memory themselves: plugins and
+ * custom ops running inside a framework that owns all device memory through
+ * its own pool (an allocation behind the pool's back breaks its accounting or
+ * fails under a hard memory cap), bare C/Fortran hosts without a device
+ * allocator, and hot loops that cannot afford the implicit device-wide
+ * synchronisation of cudaMalloc/cudaFree.  The encoded operands go to a fixed
+ * scratch area of MX_NOALLOC_SCRATCH_BYTES held by the library's module on
+ * every GPU that loads it, until process exit.  The call itself allocates
+ * nothing and calls no allocating routine.
+ *
+ * Limits and behaviour:
+ *   - mx_linear_workspace_bytes(MX_OP_WGRAD, T, N, K) must not exceed
+ *     MX_NOALLOC_SCRATCH_BYTES (64 MiB; e.g. T = 8192 with N = K = 4096 needs
+ *     35.7 MB), else MX_ERR_WORKSPACE is returned and nothing is launched.
+ *   - The first call on a device looks up the scratch area's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - Every call on a device shares the one scratch area and leaves its
+ *     contents behind (they are fully rewritten by the next call).  Calls that
+ *     overlap on the GPU (different streams, no ordering between them) race
+ *     on it and give undefined results; serialise them.
+ *   - Arguments, layouts and the other status codes are those of
+ *     mx_linear_wgrad.
+ */
+#define MX_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+mx_status mx_linear_wgrad_noalloc(const void *d_dY, const void *d_X, float *d_dW, int64_t T,
+                                  int64_t N, int64_t K, int rot, int rot_block, int rnd,
+                                  uint64_t seed, void *stream);
+
 /* ------------------------------------------------------------------------ */
 /* Status and diagnostics                                                    */
 /* ------------------------------------------------------------------------ */

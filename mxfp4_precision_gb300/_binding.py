@@ -22,7 +22,8 @@ OP_FPROP, OP_DGRAD, OP_WGRAD = 0, 1, 2
 
 EXPORTED = [
     "mx_codes_bytes", "mx_scales_bytes", "mx_quantize", "mx_gemm", "mx_linear_workspace_bytes",
-    "mx_linear_wgrad", "mx_linear_fprop", "mx_linear_dgrad", "mx_check_status",
+    "mx_linear_wgrad", "mx_linear_fprop", "mx_linear_dgrad", "mx_linear_wgrad_noalloc",
+    "mx_check_status",
     "mx_debug_timeout_probe", "mx_status_string", "mx_version",
 ]
 
@@ -66,6 +67,8 @@ def lib() -> ctypes.CDLL:
                 fn = getattr(L, name)
                 fn.argtypes = [P, P, P, i64, i64, i64, i32, i32, i32, u64, P, sz, P]
                 fn.restype = i32
+            L.mx_linear_wgrad_noalloc.argtypes = [P, P, P, i64, i64, i64, i32, i32, i32, u64, P]
+            L.mx_linear_wgrad_noalloc.restype = i32
             L.mx_check_status.argtypes = [P]
             L.mx_check_status.restype = i32
             L.mx_debug_timeout_probe.argtypes = [i64, P]
@@ -176,6 +179,24 @@ def linear_wgrad(dY, X, rot=ROT_HADAMARD_DET, rot_block=32, rnd=ROUND_RNE, seed=
     K = X.shape[1]
     return _linear("mx_linear_wgrad", OP_WGRAD, dY, X, (N, K), T, N, K, rot, rot_block, rnd,
                    seed, ws, out, stream)
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def linear_wgrad_noalloc(dY, X, rot=ROT_HADAMARD_DET, rot_block=32, rnd=ROUND_RNE, seed=0,
+                         out=None, stream=None) -> torch.Tensor:
+    """dW = dY^T X through mx_linear_wgrad_noalloc: the library's fixed scratch
+    area instead of a workspace (for callers that cannot allocate; see mx.h)."""
+    dY, X = _as_bf16_bits(dY), _as_bf16_bits(X)
+    T, N = dY.shape
+    K = X.shape[1]
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.float32, device=dY.device)
+    st = lib().mx_linear_wgrad_noalloc(_dev_ptr(dY, "dY"), _dev_ptr(X, "X"), _dev_ptr(out, "out"),
+                                       T, N, K, rot, rot_block, rnd, seed, _stream(stream))
+    _check(st, "mx_linear_wgrad_noalloc")
+    return out
 
 
 def linear_fprop(X, W, rot=ROT_NONE, rot_block=32, rnd=ROUND_RNE, seed=0, ws=None, out=None,
