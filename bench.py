@@ -8,8 +8,9 @@ block Hadamard of 32 along T, round-to-nearest-even.  Inputs are synthetic
 (seeded; Student-t(3) gradients with std 1e-3, N(0,1) activations with 1% x20
 outlier channels) and resident in HBM when the timed region starts.
 
-One step = the three launches of the hot path through the C ABI:
-mx_quantize(dY), mx_quantize(X), mx_gemm.  L2 is flushed (512 MB write)
+One step = the two launches of the hot path through the C ABI:
+mx_quantize_pair(dY, X) (both operands rotated and encoded in one launch) and
+mx_gemm.  L2 is flushed (512 MB write)
 before every timed step, outside the events.  `e2e` repeats the step through
 mx_linear_wgrad with pinned HOST buffers, the H2D/D2H copies inside the
 timed region.  The reference arm (--impl reference) times the CPU oracle on
@@ -257,12 +258,11 @@ def run_mine(args, world, rank, local):
     ptr = lambda t: t.data_ptr()
 
     def step_parts():
-        s1 = L.mx_quantize(ptr(dY), T, N, mx.CONTRACT_ROWS, rot, nb, rnd, seed, ptr(aq), ptr(as_), sp)
+        s1 = L.mx_quantize_pair(ptr(dY), T, N, ptr(X), T, K, rot, nb, rnd, seed, ptr(aq), ptr(as_),
+                                ptr(bq), ptr(bs), sp)
         yield s1
-        s2 = L.mx_quantize(ptr(X), T, K, mx.CONTRACT_ROWS, rot, nb, rnd, seed, ptr(bq), ptr(bs), sp)
+        s2 = L.mx_gemm(ptr(aq), ptr(as_), ptr(bq), ptr(bs), ptr(dW), N, K, T, sp)
         yield s2
-        s3 = L.mx_gemm(ptr(aq), ptr(as_), ptr(bq), ptr(bs), ptr(dW), N, K, T, sp)
-        yield s3
 
     def check(st, what):
         if st != 0:
@@ -277,7 +277,7 @@ def run_mine(args, world, rank, local):
     mx.check_status()
 
     n = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
     barrier(world)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clocks:
@@ -290,10 +290,9 @@ def run_mine(args, world, rank, local):
         torch.cuda.synchronize(dev)
     barrier(world)
     mx.check_status()
-    q1 = [ev[i][0].elapsed_time(ev[i][1]) for i in range(n)]
-    q2 = [ev[i][1].elapsed_time(ev[i][2]) for i in range(n)]
-    gm = [ev[i][2].elapsed_time(ev[i][3]) for i in range(n)]
-    step_ms = [a + b + c for a, b, c in zip(q1, q2, gm)]
+    qp = [ev[i][0].elapsed_time(ev[i][1]) for i in range(n)]
+    gm = [ev[i][1].elapsed_time(ev[i][2]) for i in range(n)]
+    step_ms = [a + b for a, b in zip(qp, gm)]
     total_ms = reduce_max(sum(step_ms), world, dev)
     flops_step = 2.0 * N * K * T
     value = world * n * flops_step / (total_ms * 1e-3) / 1e12
@@ -333,7 +332,7 @@ def run_mine(args, world, rank, local):
     q_bytes_n = N * T * (2 + 0.5 + 1 / 32)      # bf16 in, codes + scales out
     q_bytes_k = K * T * (2 + 0.5 + 1 / 32)
     mean = lambda v: sum(v) / len(v)
-    t_q1, t_q2, t_g = mean(q1), mean(q2), mean(gm)
+    t_q, t_g = mean(qp), mean(gm)
     traffic = load_traffic()
     wl = args.workload
 
@@ -352,13 +351,13 @@ def run_mine(args, world, rank, local):
                              f"fp4/bf16 ratio {NOMINAL_FP4_OVER_BF16:g}",
                "ms_per_launch": t_g}
     quant_rf = {"kernel": "mxq_colwise_kernel", "bound": "hbm",
-                "achieved": (q_bytes_n + q_bytes_k) / ((t_q1 + t_q2) * 1e-3) / 1e9,
+                "achieved": (q_bytes_n + q_bytes_k) / (t_q * 1e-3) / 1e9,
                 "peak": hbm, "unit": "GB/s",
-                "frac": (q_bytes_n + q_bytes_k) / ((t_q1 + t_q2) * 1e-3) / 1e9 / hbm,
+                "frac": (q_bytes_n + q_bytes_k) / (t_q * 1e-3) / 1e9 / hbm,
                 "traffic": tr("mxq_colwise_kernel", "mx_quant.cu"),
                 "peak_basis": f"{peak_src} HBM copy bandwidth",
-                "ms_per_launch": (t_q1 + t_q2) / 2}
-    dominant = gemm_rf if t_g >= (t_q1 + t_q2) else quant_rf
+                "ms_per_launch": t_q}
+    dominant = gemm_rf if t_g >= t_q else quant_rf
     clk = clocks.summary()
     cpu = None
     if not args.no_cpu_baseline:
@@ -377,13 +376,13 @@ def run_mine(args, world, rank, local):
                                                    "traffic")},
             "roofline_kernels": [gemm_rf, quant_rf],
             "fp4_peak_fraction": value / fp4_peak,
-            "breakdown_ms": {"quantize_dY": t_q1, "quantize_X": t_q2, "gemm": t_g},
+            "breakdown_ms": {"quantize_pair": t_q, "gemm": t_g},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": dY_h.numel() * 2 + X_h.numel() * 2,
                     "d2h_bytes_per_step": dW_h.numel() * 4,
                     "ms_per_step": e2e_ms / n_e2e, "call": "mx_linear_wgrad"},
-            "gpu_launches": 3 * n,
+            "gpu_launches": 2 * n,
             "clocks": clk,
             "parity_spot_check": parity}
     print(json.dumps(line), flush=True)

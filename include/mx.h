@@ -120,6 +120,20 @@ mx_status mx_quantize(const void *d_src, int64_t rows, int64_t cols, int contrac
                       void *stream);
 
 /*
+ * mx_quantize_pair -- encode the two operands of a Wgrad in ONE launch: both
+ * d_src0[rows0][cols0] and d_src1[rows1][cols1] are encoded down their rows
+ * (MX_CONTRACT_ROWS: contraction length rows0 == rows1) with the same rotation,
+ * rounding and seed; SR draws use key (seed, 1) for operand 0 and (seed, 2)
+ * for operand 1 (as mx_linear_wgrad does).  Outputs, layouts and argument rules
+ * are those of mx_quantize for each operand.  One launch instead of two lets
+ * the two HBM-bound encodes share one pipeline ramp-up and tail.
+ */
+mx_status mx_quantize_pair(const void *d_src0, int64_t rows0, int64_t cols0, const void *d_src1,
+                           int64_t rows1, int64_t cols1, int rot, int rot_block, int rnd,
+                           uint64_t seed, void *d_codes0, void *d_scales0, void *d_codes1,
+                           void *d_scales1, void *stream);
+
+/*
  * mx_gemm -- C[M][N] (fp32, row-major, overwritten) = A . B^T, where A is an
  * encoded operand with M lines and B one with N lines, both of contraction
  * length K (K % 32 == 0).  Block-scaled FP4 tensor-core contraction with fp32

@@ -10,7 +10,7 @@ from ._binding import (CONTRACT_COLS, CONTRACT_ROWS, OP_DGRAD, OP_FPROP, OP_WGRA
                        ROT_HADAMARD_RAND, ROT_NONE, ROUND_RNE, ROUND_SR, MXError, check_status,
                        codes_bytes, debug_timeout_probe, gemm, gemm_into, lib, library_path,
                        linear_dgrad, linear_fprop, linear_wgrad, linear_wgrad_noalloc,
-                       linear_workspace_bytes, NOALLOC_SCRATCH_BYTES, quantize,
+                       linear_workspace_bytes, NOALLOC_SCRATCH_BYTES, quantize, quantize_pair,
                        quantize_into, scales_bytes, status_string)
 
 __all__ = [
@@ -18,6 +18,6 @@ __all__ = [
     "ROT_HADAMARD_RAND", "ROT_NONE", "ROUND_RNE", "ROUND_SR", "MXError", "check_status",
     "codes_bytes", "debug_timeout_probe", "gemm", "gemm_into", "lib", "library_path",
     "linear_dgrad", "linear_fprop", "linear_wgrad", "linear_wgrad_noalloc", "linear_workspace_bytes",
-    "NOALLOC_SCRATCH_BYTES", "quantize",
+    "NOALLOC_SCRATCH_BYTES", "quantize", "quantize_pair",
     "quantize_into", "scales_bytes", "status_string",
 ]

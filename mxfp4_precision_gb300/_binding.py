@@ -21,7 +21,7 @@ CONTRACT_ROWS, CONTRACT_COLS = 0, 1
 OP_FPROP, OP_DGRAD, OP_WGRAD = 0, 1, 2
 
 EXPORTED = [
-    "mx_codes_bytes", "mx_scales_bytes", "mx_quantize", "mx_gemm", "mx_linear_workspace_bytes",
+    "mx_codes_bytes", "mx_scales_bytes", "mx_quantize", "mx_quantize_pair", "mx_gemm", "mx_linear_workspace_bytes",
     "mx_linear_wgrad", "mx_linear_fprop", "mx_linear_dgrad", "mx_linear_wgrad_noalloc",
     "mx_check_status",
     "mx_debug_timeout_probe", "mx_status_string", "mx_version",
@@ -59,6 +59,9 @@ def lib() -> ctypes.CDLL:
             L.mx_scales_bytes.restype = sz
             L.mx_quantize.argtypes = [P, i64, i64, i32, i32, i32, i32, u64, P, P, P]
             L.mx_quantize.restype = i32
+            L.mx_quantize_pair.argtypes = [P, i64, i64, P, i64, i64, i32, i32, i32, u64, P, P, P,
+                                           P, P]
+            L.mx_quantize_pair.restype = i32
             L.mx_gemm.argtypes = [P, P, P, P, P, i64, i64, i64, P]
             L.mx_gemm.restype = i32
             L.mx_linear_workspace_bytes.argtypes = [i32, i64, i64, i64]
@@ -144,6 +147,24 @@ def quantize(src: torch.Tensor, contract: int, rot: int = ROT_NONE, rot_block: i
     scales = torch.empty((max(1, scales_bytes(lines, L)),), dtype=torch.uint8, device=src.device)
     quantize_into(src, codes, scales, contract, rot, rot_block, rnd, seed, stream)
     return codes, scales
+
+
+def quantize_pair(src0: torch.Tensor, src1: torch.Tensor, rot: int = ROT_HADAMARD_DET,
+                  rot_block: int = 32, rnd: int = ROUND_RNE, seed: int = 0, stream=None):
+    """Both Wgrad operands (encoded down their rows) in one launch; returns
+    ((codes0, scales0), (codes1, scales1))."""
+    src0, src1 = _as_bf16_bits(src0), _as_bf16_bits(src1)
+    (r0, c0), (r1, c1) = src0.shape, src1.shape
+    out = []
+    for r, c, d in ((r0, c0, src0.device), (r1, c1, src1.device)):
+        out.append((torch.empty((c, r // 2), dtype=torch.uint8, device=d),
+                    torch.empty((max(1, scales_bytes(c, r)),), dtype=torch.uint8, device=d)))
+    st = lib().mx_quantize_pair(_dev_ptr(src0, "src0"), r0, c0, _dev_ptr(src1, "src1"), r1, c1, rot,
+                                rot_block, rnd, seed, _dev_ptr(out[0][0], "codes0"),
+                                _dev_ptr(out[0][1], "scales0"), _dev_ptr(out[1][0], "codes1"),
+                                _dev_ptr(out[1][1], "scales1"), _stream(stream))
+    _check(st, "mx_quantize_pair")
+    return out[0], out[1]
 
 
 def gemm_into(Aq, As, Bq, Bs, C: torch.Tensor, M: int, N: int, K: int, stream=None) -> None:

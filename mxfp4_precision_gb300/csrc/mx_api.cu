@@ -177,6 +177,30 @@ mx_status quantize_impl(const void *src, int64_t rows, int64_t cols, int contrac
                                      codes, scales, *dev, stream));
 }
 
+mx_status quantize_pair_impl(const void *src0, int64_t rows0, int64_t cols0, const void *src1,
+                             int64_t rows1, int64_t cols1, int rot, int rot_block, int rnd,
+                             uint64_t seed, void *codes0, void *scales0, void *codes1,
+                             void *scales1, cudaStream_t stream) {
+    if (rows0 != rows1) return MX_ERR_SHAPE;
+    mx_status st = check_encode(src0, rows0, cols0, MX_CONTRACT_ROWS, rot, rot_block, rnd, codes0,
+                                scales0);
+    if (st != MX_OK) return st;
+    st = check_encode(src1, rows1, cols1, MX_CONTRACT_ROWS, rot, rot_block, rnd, codes1, scales1);
+    if (st != MX_OK) return st;
+    const bool e0 = rows0 == 0 || cols0 == 0, e1 = rows1 == 0 || cols1 == 0;
+    if (e0 && e1) return MX_OK;
+    if (e0 || e1)  // one side empty: plain single-operand encode of the other
+        return e0 ? quantize_impl(src1, rows1, cols1, MX_CONTRACT_ROWS, rot, rot_block, rnd, seed,
+                                  2, codes1, scales1, stream)
+                  : quantize_impl(src0, rows0, cols0, MX_CONTRACT_ROWS, rot, rot_block, rnd, seed,
+                                  1, codes0, scales0, stream);
+    const DeviceInfo *dev = nullptr;
+    if ((st = device_or_error(&dev)) != MX_OK) return st;
+    return from_cuda(launch_quantize_pair_colwise(src0, rows0, cols0, src1, rows1, cols1, rot,
+                                                  rot_block, rnd, seed, codes0, scales0, codes1,
+                                                  scales1, *dev, stream));
+}
+
 mx_status gemm_impl(const void *Aq, const void *As, const void *Bq, const void *Bs, float *C,
                     int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
     mx_status st = check_gemm(Aq, As, Bq, Bs, C, M, N, K);
@@ -217,11 +241,17 @@ mx_status linear_impl(int op, const void *a_src, int64_t a_rows, int64_t a_cols,
     uint8_t *bq = p;
     p += align256(mx_codes_bytes(s.b_lines, s.k));
     uint8_t *bs = p;
-    st = quantize_impl(a_src, a_rows, a_cols, a_contract, rot, rot_block, rnd, seed, 1, aq, as,
-                       stream);
-    if (st != MX_OK) return st;
-    st = quantize_impl(b_src, b_rows, b_cols, b_contract, rot, rot_block, rnd, seed, 2, bq, bs,
-                       stream);
+    if (a_contract == MX_CONTRACT_ROWS && b_contract == MX_CONTRACT_ROWS) {
+        // Wgrad: both operands encoded down their rows in a single launch.
+        st = quantize_pair_impl(a_src, a_rows, a_cols, b_src, b_rows, b_cols, rot, rot_block, rnd,
+                                seed, aq, as, bq, bs, stream);
+    } else {
+        st = quantize_impl(a_src, a_rows, a_cols, a_contract, rot, rot_block, rnd, seed, 1, aq, as,
+                           stream);
+        if (st == MX_OK)
+            st = quantize_impl(b_src, b_rows, b_cols, b_contract, rot, rot_block, rnd, seed, 2,
+                               bq, bs, stream);
+    }
     if (st != MX_OK) return st;
     return gemm_impl(aq, as, bq, bs, out, s.a_lines, s.b_lines, s.k, stream);
 }
@@ -244,6 +274,15 @@ mx_status mx_quantize(const void *d_src, int64_t rows, int64_t cols, int contrac
                       void *stream) {
     return quantize_impl(d_src, rows, cols, contract, rot, rot_block, rnd, seed, 1, d_codes,
                          d_scales, static_cast<cudaStream_t>(stream));
+}
+
+mx_status mx_quantize_pair(const void *d_src0, int64_t rows0, int64_t cols0, const void *d_src1,
+                           int64_t rows1, int64_t cols1, int rot, int rot_block, int rnd,
+                           uint64_t seed, void *d_codes0, void *d_scales0, void *d_codes1,
+                           void *d_scales1, void *stream) {
+    return quantize_pair_impl(d_src0, rows0, cols0, d_src1, rows1, cols1, rot, rot_block, rnd, seed,
+                              d_codes0, d_scales0, d_codes1, d_scales1,
+                              static_cast<cudaStream_t>(stream));
 }
 
 mx_status mx_gemm(const void *d_Aq, const void *d_As, const void *d_Bq, const void *d_Bs,

@@ -32,6 +32,14 @@ cudaError_t launch_quantize(const void *src, int64_t rows, int64_t cols, int con
                             void *codes, void *scales, const DeviceInfo &dev,
                             cudaStream_t stream);
 
+// Both operands encoded down their rows (contraction = rows) in one launch;
+// SR tags 1 and 2.
+cudaError_t launch_quantize_pair_colwise(const void *src0, int64_t rows0, int64_t cols0,
+                                         const void *src1, int64_t rows1, int64_t cols1, int rot,
+                                         int rot_block, int rnd, uint64_t seed, void *codes0,
+                                         void *scales0, void *codes1, void *scales1,
+                                         const DeviceInfo &dev, cudaStream_t stream);
+
 cudaError_t launch_gemm(const void *Aq, const void *As, const void *Bq, const void *Bs, float *C,
                         int64_t M, int64_t N, int64_t K, const DeviceInfo &dev,
                         cudaStream_t stream);

@@ -33,7 +33,10 @@
 namespace mx {
 namespace {
 
-constexpr int kStages = 3;
+#ifndef MXQ_STAGES
+#define MXQ_STAGES 2
+#endif
+constexpr int kStages = MXQ_STAGES;  // TMA ring depth per CTA (2 stages: 3 CTAs per SM)
 constexpr int kThreads = 256;
 constexpr uint32_t kTileBytes = 32768;  // 256 x 64 bf16 (colwise) / 64 x 256 bf16 (rowwise)
 constexpr uint32_t kScaleStage = 512;   // two half-atoms of scales per tile
@@ -172,6 +175,96 @@ __device__ __forceinline__ uint32_t cvt_e2m1x8(float v0, float v1, float v2, flo
     return out;
 }
 
+// ---------------------------------------------------------------- paired lanes
+// Two channels processed in lockstep travel as one 64-bit register pair
+// {channel 2l (low), channel 2l+1 (high)}; the f32x2 instructions round each
+// half exactly like the scalar fp32 instruction would.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t r, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// max(|a|, m), NaN-propagating: a NaN anywhere in the block survives.
+__device__ __forceinline__ float absmax_nan(float m, float a) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(fabsf(a)), "f"(m));
+    return r;
+}
+
+// Butterfly stages of stride 1 .. min(N,32)/2 on 32 channel pairs.
+template <int N>
+__device__ __forceinline__ void fwht_pairs(uint64_t (&x)[32]) {
+    constexpr int H = N < 32 ? N : 32;
+#pragma unroll
+    for (int h = 1; h < H; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            if ((i & h) == 0) {
+                const uint64_t a = x[i], b = x[i + h];
+                x[i] = add2(a, b);
+                x[i + h] = sub2(a, b);
+            }
+        }
+    }
+}
+
+// Shared-exponent byte and its exact inverse power of two for a block amax.
+__device__ __forceinline__ uint32_t scale_of(float amax, float &inv) {
+    const uint32_t m = __float_as_uint(amax);
+    const uint32_t e = m >> 23;                 // biased exponent (0: zero/subnormal)
+    const uint32_t sb = e >= 2u ? e - 2u : 0u;  // floor(log2 amax) - 2 + 127, clamped at 0
+    inv = __uint_as_float((254u - (sb > 253u ? 253u : sb)) << 23);  // 2^(127 - sb)
+    return m >= 0x7F800000u ? 0xFFu : sb;       // Inf/NaN in the block: NaN scale
+}
+
+// Round-to-nearest encode of two channels' blocks held as pairs.
+__device__ __forceinline__ void encode_pair_rne(const uint64_t (&x)[32], uint4 &q0, uint4 &q1,
+                                                uint32_t &s0, uint32_t &s1) {
+    float m0 = 0.0f, m1 = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        float lo, hi;
+        unpack2(x[i], lo, hi);
+        m0 = absmax_nan(m0, lo);
+        m1 = absmax_nan(m1, hi);
+    }
+    float inv0, inv1;
+    s0 = scale_of(m0, inv0);
+    s1 = scale_of(m1, inv1);
+    const uint64_t inv = pack2(inv0, inv1);
+    float v0[32], v1[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) unpack2(mul2(x[i], inv), v0[i], v1[i]);
+    uint32_t w0[4], w1[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        w0[j] = cvt_e2m1x8(v0[8 * j], v0[8 * j + 1], v0[8 * j + 2], v0[8 * j + 3], v0[8 * j + 4],
+                           v0[8 * j + 5], v0[8 * j + 6], v0[8 * j + 7]);
+        w1[j] = cvt_e2m1x8(v1[8 * j], v1[8 * j + 1], v1[8 * j + 2], v1[8 * j + 3], v1[8 * j + 4],
+                           v1[8 * j + 5], v1[8 * j + 6], v1[8 * j + 7]);
+    }
+    q0 = s0 == 0xFFu ? make_uint4(0, 0, 0, 0) : make_uint4(w0[0], w0[1], w0[2], w0[3]);
+    q1 = s1 == 0xFFu ? make_uint4(0, 0, 0, 0) : make_uint4(w1[0], w1[1], w1[2], w1[3]);
+}
+
 // Encode one block of 32 rotated values.  Returns the E8M0 byte; codes in q.
 template <bool SR>
 __device__ __forceinline__ uint32_t encode_block32(const float (&r)[32], uint4 &q,
@@ -236,113 +329,168 @@ __device__ __forceinline__ void flush_scales(const uint8_t *stage, const QuantAr
 }
 
 // ---------------------------------------------------------------- colwise
+// Byte offset of the scale of (line, block) in the tiled layout.
+__device__ __forceinline__ int64_t scale_offset(int64_t line, int64_t block, int64_t katoms) {
+    return ((line / 128) * katoms + block / 4) * 512 + (line % 32) * 16 + ((line % 128) / 32) * 4 +
+           (block % 4);
+}
+
+// One launch encodes up to two operands (the two Wgrad operands): tiles
+// [0, a0.num_tiles) belong to operand 0, the rest to operand 1.  For Hadamard
+// sizes up to 32 every warp works on its own 32-token slice of the tile and
+// no CTA-wide barrier is taken inside the loop: each warp marks the stage
+// consumed on an mbarrier and thread 0 refills it once all eight have.
 template <int ROTN, bool RAND, bool SR>
-__global__ void __launch_bounds__(kThreads) mxq_colwise_kernel(const __grid_constant__ CUtensorMap src_map,
-                                                               const QuantArgs p) {
+__global__ void __launch_bounds__(kThreads) mxq_colwise_kernel(
+    const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
+    const QuantArgs a0, const QuantArgs a1) {
+    constexpr bool kCtaSync = ROTN >= 64;  // cross-warp Hadamard stages need CTA barriers
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~uintptr_t(1023));
+    // 1024-byte aligned base, kept as a shared-space pointer (offset arithmetic
+    // only) so that the compiler emits shared-memory loads.
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *tiles = smem;                                   // kStages x 32 KB
-    uint8_t *sstage = smem + kStages * kTileBytes;           // 512 B
-    uint64_t *full = reinterpret_cast<uint64_t *>(sstage + kScaleStage);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kTileBytes);
+    uint64_t *empty = full + kStages;
     float2 *xchg = reinterpret_cast<float2 *>(smem + kStages * kTileBytes + 1024);  // 64 KB
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int total = a0.num_tiles + a1.num_tiles;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kThreads / 32);
+        }
         abort_flag = 0;
         fence_barrier_init();
-        prefetch_tmap(&src_map);
+        prefetch_tmap(&map0);
+        if (a1.num_tiles > 0) prefetch_tmap(&map1);
     }
     __syncthreads();
 
     auto issue = [&](int tile, int s) {
-        const int tt = tile / p.tiles_inner, ct = tile % p.tiles_inner;
+        const bool second = tile >= a0.num_tiles;
+        const int lt = second ? tile - a0.num_tiles : tile;
+        const int inner = second ? a1.tiles_inner : a0.tiles_inner;
         mbar_arrive_expect_tx(&full[s], kTileBytes);
-        tma_load_2d(tiles + s * kTileBytes, &src_map, &full[s], ct * 64, tt * 256);
+        tma_load_2d(tiles + s * kTileBytes, second ? &map1 : &map0, &full[s], (lt % inner) * 64,
+                    (lt / inner) * 256);
     };
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             const int tile = blockIdx.x + s * gridDim.x;
-            if (tile < p.num_tiles) issue(tile, s);
+            if (tile < total) issue(tile, s);
         }
     }
 
     for (int it = 0;; ++it) {
         const int tile = blockIdx.x + it * gridDim.x;
-        if (tile >= p.num_tiles) break;
+        if (tile >= total) break;
         const int s = it % kStages;
         const uint32_t parity = (it / kStages) & 1u;
-        const int64_t t0 = static_cast<int64_t>(tile / p.tiles_inner) * 256;
-        const int64_t c0 = static_cast<int64_t>(tile % p.tiles_inner) * 64;
+        const bool second = tile >= a0.num_tiles;
+        const int lt = second ? tile - a0.num_tiles : tile;
+        const int inner = second ? a1.tiles_inner : a0.tiles_inner;
+        const int64_t L = second ? a1.L : a0.L;
+        const int64_t lines = second ? a1.lines : a0.lines;
+        const int64_t katoms = second ? a1.katoms : a0.katoms;
+        uint8_t *const codes = second ? a1.codes : a0.codes;
+        uint8_t *const scales = second ? a1.scales : a0.scales;
+        const int64_t t0 = static_cast<int64_t>(lt / inner) * 256;
+        const int64_t c0 = static_cast<int64_t>(lt % inner) * 64;
 
-        const bool ok = mbar_wait(&full[s], parity, p.status, &abort_flag);
-        if (__syncthreads_or(!ok)) break;
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait(&full[s], parity, a0.status, &abort_flag) ? 1 : 0;
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (kCtaSync) {
+            if (__syncthreads_or(!ok)) break;
+        } else if (!ok) {
+            break;
+        }
 
-        // Column pair (2*lane, 2*lane+1), tokens 32*warp .. 32*warp+31.
-        float x0[32], x1[32];
+        // Column pair (2*lane, 2*lane+1), tokens 32*warp .. 32*warp+31, as
+        // 32 register pairs {channel 2*lane, channel 2*lane+1}.
+        uint64_t x[32];
         const uint32_t *tw = reinterpret_cast<const uint32_t *>(tiles + s * kTileBytes);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             const uint32_t v = tw[(warp * 32 + i) * 32 + lane];
-            x0[i] = __uint_as_float(v << 16);
-            x1[i] = __uint_as_float(v & 0xFFFF0000u);
+            x[i] = pack2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
         }
-        __syncthreads();  // stage s fully consumed
-        if (threadIdx.x == 0) {
-            const int nt = tile + kStages * gridDim.x;
-            if (nt < p.num_tiles) issue(nt, s);
+        if (kCtaSync) {
+            __syncthreads();  // stage s fully consumed
+            if (threadIdx.x == 0) {
+                const int nt = tile + kStages * gridDim.x;
+                if (nt < total) issue(nt, s);
+            }
+        } else {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            if (threadIdx.x == 0) {
+                const int nt = tile + kStages * gridDim.x;
+                if (nt < total && mbar_wait(&empty[s], parity, a0.status, &abort_flag)) issue(nt, s);
+            }
         }
 
         if (ROTN > 0) {
             if (RAND) {
-                const uint32_t bits = sign_bits32(p.seed, static_cast<uint64_t>(t0 / 256), warp);
-                apply_signs(x0, bits);
-                apply_signs(x1, bits);
+                const uint32_t bits = sign_bits32(a0.seed, static_cast<uint64_t>(t0 / 256), warp);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    x[i] ^= ((bits >> i) & 1u) ? 0x8000000080000000ull : 0ull;
             }
-            fwht_in_thread<ROTN>(x0);
-            fwht_in_thread<ROTN>(x1);
+            fwht_pairs<ROTN>(x);
             if (ROTN >= 64) {
+                uint64_t *xw = reinterpret_cast<uint64_t *>(xchg);
 #pragma unroll
                 for (int h = 32; h < ROTN; h <<= 1) {
                     const int m = h / 32;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        xchg[(warp * 32 + i) * 32 + lane] = make_float2(x0[i], x1[i]);
+                    for (int i = 0; i < 32; ++i) xw[(warp * 32 + i) * 32 + lane] = x[i];
                     __syncthreads();
                     const int pw = warp ^ m;
                     const bool lower = (warp & m) == 0;
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const float2 o = xchg[(pw * 32 + i) * 32 + lane];
-                        x0[i] = lower ? __fadd_rn(x0[i], o.x) : __fsub_rn(o.x, x0[i]);
-                        x1[i] = lower ? __fadd_rn(x1[i], o.y) : __fsub_rn(o.y, x1[i]);
+                        const uint64_t o = xw[(pw * 32 + i) * 32 + lane];
+                        x[i] = lower ? add2(x[i], o) : sub2(o, x[i]);
                     }
                     __syncthreads();
                 }
             }
-            scale_by_norm<ROTN>(x0);
-            scale_by_norm<ROTN>(x1);
+            const float cn = hadamard_norm<ROTN>();
+            const uint64_t cc = pack2(cn, cn);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] = mul2(x[i], cc);
         }
 
         const int64_t tb = t0 + 32 * warp;   // first token of this thread's block
         const int64_t c = c0 + 2 * lane;     // first of the thread's two channels
-        uint32_t u[32];
         uint4 q0, q1;
-        if (SR) sr_draws32(p.seed, p.sr_tag, static_cast<uint64_t>(c * p.L + tb), u);
-        const uint32_t s0 = encode_block32<SR>(x0, q0, u);
-        if (SR) sr_draws32(p.seed, p.sr_tag, static_cast<uint64_t>((c + 1) * p.L + tb), u);
-        const uint32_t s1 = encode_block32<SR>(x1, q1, u);
-
-        if (tb < p.L) {
-            if (c < p.lines) st_global_16(p.codes + c * (p.L / 2) + tb / 2, q0);
-            if (c + 1 < p.lines) st_global_16(p.codes + (c + 1) * (p.L / 2) + tb / 2, q1);
+        uint32_t s0, s1;
+        if (SR) {
+            const uint64_t tag = second ? a1.sr_tag : a0.sr_tag;
+            float x0[32], x1[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) unpack2(x[i], x0[i], x1[i]);
+            uint32_t u[32];
+            sr_draws32(a0.seed, tag, static_cast<uint64_t>(c * L + tb), u);
+            s0 = encode_block32<true>(x0, q0, u);
+            sr_draws32(a0.seed, tag, static_cast<uint64_t>((c + 1) * L + tb), u);
+            s1 = encode_block32<true>(x1, q1, u);
+        } else {
+            encode_pair_rne(x, q0, q1, s0, s1);
         }
-        sstage[stage_offset(2 * lane, warp)] = static_cast<uint8_t>(s0);
-        sstage[stage_offset(2 * lane + 1, warp)] = static_cast<uint8_t>(s1);
-        __syncthreads();
-        flush_scales(sstage, p, c0, t0);
+
+        if (tb < L) {
+            if (c < lines) st_global_16(codes + c * (L / 2) + tb / 2, q0);
+            if (c + 1 < lines) st_global_16(codes + (c + 1) * (L / 2) + tb / 2, q1);
+        }
+        // Scale bytes (padding lines / blocks included: their input is zero).
+        const int64_t kb = tb / 32;
+        scales[scale_offset(c, kb, katoms)] = static_cast<uint8_t>(s0);
+        scales[scale_offset(c + 1, kb, katoms)] = static_cast<uint8_t>(s1);
     }
 }
 
@@ -351,8 +499,9 @@ template <int ROTN, bool RAND, bool SR>
 __global__ void __launch_bounds__(kThreads) mxq_rowwise_kernel(const __grid_constant__ CUtensorMap src_map,
                                                                const QuantArgs p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~uintptr_t(1023));
+    // 1024-byte aligned base, kept as a shared-space pointer (offset arithmetic
+    // only) so that the compiler emits shared-memory loads.
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *tiles = smem;
     uint8_t *sstage = smem + kStages * kTileBytes;
     uint64_t *full = reinterpret_cast<uint64_t *>(sstage + kScaleStage);
@@ -488,9 +637,9 @@ __global__ void __launch_bounds__(kThreads) mxq_rowwise_kernel(const __grid_cons
 }
 
 // ---------------------------------------------------------------- dispatch
-template <typename Kern>
-cudaError_t launch_persistent(Kern kernel, const CUtensorMap &map, const QuantArgs &a,
-                              size_t smem, const DeviceInfo &dev, cudaStream_t stream) {
+template <typename Kern, typename... Args>
+cudaError_t launch_persistent(Kern kernel, int num_tiles, size_t smem, const DeviceInfo &dev,
+                              cudaStream_t stream, Args... args) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -498,32 +647,42 @@ cudaError_t launch_persistent(Kern kernel, const CUtensorMap &map, const QuantAr
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
-    const int grid = a.num_tiles < dev.sm_count * per_sm ? a.num_tiles : dev.sm_count * per_sm;
-    kernel<<<grid, kThreads, smem, stream>>>(map, a);
+    const int grid = num_tiles < dev.sm_count * per_sm ? num_tiles : dev.sm_count * per_sm;
+    kernel<<<grid, kThreads, smem, stream>>>(args...);
     return cudaGetLastError();
 }
 
+struct Operands {
+    CUtensorMap map0, map1;
+    QuantArgs a0, a1;
+};
+
 template <bool COLWISE, int ROTN, bool RAND>
-cudaError_t launch_rot(bool sr, const CUtensorMap &map, const QuantArgs &a,
-                       const DeviceInfo &dev, cudaStream_t stream) {
-    const size_t smem = kStages * kTileBytes + 1024 + (COLWISE && ROTN >= 64 ? 65536 : 0) + 1024;
+cudaError_t launch_rot(bool sr, const Operands &o, const DeviceInfo &dev, cudaStream_t stream) {
     if (COLWISE) {
-        return sr ? launch_persistent(mxq_colwise_kernel<ROTN, RAND, true>, map, a, smem, dev, stream)
-                  : launch_persistent(mxq_colwise_kernel<ROTN, RAND, false>, map, a, smem, dev, stream);
+        const size_t smem = kStages * kTileBytes + 1024 + (ROTN >= 64 ? 65536 : 0) + 1024;
+        const int n = o.a0.num_tiles + o.a1.num_tiles;
+        return sr ? launch_persistent(mxq_colwise_kernel<ROTN, RAND, true>, n, smem, dev, stream,
+                                      o.map0, o.map1, o.a0, o.a1)
+                  : launch_persistent(mxq_colwise_kernel<ROTN, RAND, false>, n, smem, dev, stream,
+                                      o.map0, o.map1, o.a0, o.a1);
     }
-    return sr ? launch_persistent(mxq_rowwise_kernel<ROTN, RAND, true>, map, a, smem, dev, stream)
-              : launch_persistent(mxq_rowwise_kernel<ROTN, RAND, false>, map, a, smem, dev, stream);
+    const size_t smem = kStages * kTileBytes + 1024 + 1024;
+    return sr ? launch_persistent(mxq_rowwise_kernel<ROTN, RAND, true>, o.a0.num_tiles, smem, dev,
+                                  stream, o.map0, o.a0)
+              : launch_persistent(mxq_rowwise_kernel<ROTN, RAND, false>, o.a0.num_tiles, smem,
+                                  dev, stream, o.map0, o.a0);
 }
 
 template <bool COLWISE>
-cudaError_t launch_dir(int rot, int rot_block, bool sr, const CUtensorMap &map,
-                       const QuantArgs &a, const DeviceInfo &dev, cudaStream_t stream) {
-    if (rot == 0) return launch_rot<COLWISE, 0, false>(sr, map, a, dev, stream);
+cudaError_t launch_dir(int rot, int rot_block, bool sr, const Operands &o, const DeviceInfo &dev,
+                       cudaStream_t stream) {
+    if (rot == 0) return launch_rot<COLWISE, 0, false>(sr, o, dev, stream);
     const bool rnd = rot == 2;
 #define MX_ROT_CASE(N)                                                                      \
     case N:                                                                                 \
-        return rnd ? launch_rot<COLWISE, N, true>(sr, map, a, dev, stream)                  \
-                   : launch_rot<COLWISE, N, false>(sr, map, a, dev, stream);
+        return rnd ? launch_rot<COLWISE, N, true>(sr, o, dev, stream)                       \
+                   : launch_rot<COLWISE, N, false>(sr, o, dev, stream);
     switch (rot_block) {
         MX_ROT_CASE(16)
         MX_ROT_CASE(32)
@@ -536,6 +695,35 @@ cudaError_t launch_dir(int rot, int rot_block, bool sr, const CUtensorMap &map,
 #undef MX_ROT_CASE
 }
 
+// Fills the per-operand arguments (and tensor map) of one encode.
+bool prepare_operand(const void *src, int64_t rows, int64_t cols, bool colwise, uint64_t seed,
+                     uint64_t sr_tag, void *codes, void *scales, const DeviceInfo &dev,
+                     CUtensorMap *map, QuantArgs *a) {
+    *a = QuantArgs{};
+    a->L = colwise ? rows : cols;
+    a->lines = colwise ? cols : rows;
+    a->katoms = scale_katoms(a->L);
+    a->codes = static_cast<uint8_t *>(codes);
+    a->scales = static_cast<uint8_t *>(scales);
+    a->seed = seed;
+    a->sr_tag = sr_tag;
+    a->status = dev.status;
+    // Tiles cover the padded scale layout: lines to a multiple of 128 and the
+    // contraction dim to a multiple of 256, so padding scale bytes get zeros.
+    const int64_t line_tiles = scale_groups(a->lines) * 2;  // 64 lines per tile
+    const int64_t k_tiles = (a->L + 255) / 256;
+    if (line_tiles * k_tiles > 0x3FFFFFFF) return false;
+    a->num_tiles = static_cast<int>(line_tiles * k_tiles);
+    if (colwise) {
+        a->tiles_inner = static_cast<int>(line_tiles);
+        return encode_tmap_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, src, cols, rows, cols * 2, 64,
+                              256, CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    a->tiles_inner = static_cast<int>(k_tiles);
+    return encode_tmap_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, src, cols, rows, cols * 2, 64, 64,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 }  // namespace
 
 cudaError_t launch_quantize(const void *src, int64_t rows, int64_t cols, int contract, int rot,
@@ -543,35 +731,25 @@ cudaError_t launch_quantize(const void *src, int64_t rows, int64_t cols, int con
                             void *codes, void *scales, const DeviceInfo &dev,
                             cudaStream_t stream) {
     const bool colwise = contract == 0;
-    QuantArgs a{};
-    a.L = colwise ? rows : cols;
-    a.lines = colwise ? cols : rows;
-    a.katoms = scale_katoms(a.L);
-    a.codes = static_cast<uint8_t *>(codes);
-    a.scales = static_cast<uint8_t *>(scales);
-    a.seed = seed;
-    a.sr_tag = sr_tag;
-    a.status = dev.status;
-    // Tiles cover the padded scale layout: lines to a multiple of 128 and the
-    // contraction dim to a multiple of 256, so padding scale bytes get zeros.
-    const int64_t line_tiles = scale_groups(a.lines) * 2;  // 64 lines per tile
-    const int64_t k_tiles = (a.L + 255) / 256;
-    if (line_tiles * k_tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    CUtensorMap map;
-    if (colwise) {
-        a.tiles_inner = static_cast<int>(line_tiles);
-        a.num_tiles = static_cast<int>(line_tiles * k_tiles);
-        if (!encode_tmap_2d(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, src, cols, rows, cols * 2, 64,
-                            256, CU_TENSOR_MAP_SWIZZLE_NONE))
-            return cudaErrorInvalidValue;
-        return launch_dir<true>(rot, rot_block, rnd == 1, map, a, dev, stream);
-    }
-    a.tiles_inner = static_cast<int>(k_tiles);
-    a.num_tiles = static_cast<int>(line_tiles * k_tiles);
-    if (!encode_tmap_2d(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, src, cols, rows, cols * 2, 64, 64,
-                        CU_TENSOR_MAP_SWIZZLE_128B))
+    Operands o;
+    if (!prepare_operand(src, rows, cols, colwise, seed, sr_tag, codes, scales, dev, &o.map0, &o.a0))
         return cudaErrorInvalidValue;
-    return launch_dir<false>(rot, rot_block, rnd == 1, map, a, dev, stream);
+    o.map1 = o.map0;
+    o.a1 = QuantArgs{};
+    if (colwise) return launch_dir<true>(rot, rot_block, rnd == 1, o, dev, stream);
+    return launch_dir<false>(rot, rot_block, rnd == 1, o, dev, stream);
+}
+
+cudaError_t launch_quantize_pair_colwise(const void *src0, int64_t rows0, int64_t cols0,
+                                         const void *src1, int64_t rows1, int64_t cols1, int rot,
+                                         int rot_block, int rnd, uint64_t seed, void *codes0,
+                                         void *scales0, void *codes1, void *scales1,
+                                         const DeviceInfo &dev, cudaStream_t stream) {
+    Operands o;
+    if (!prepare_operand(src0, rows0, cols0, true, seed, 1, codes0, scales0, dev, &o.map0, &o.a0) ||
+        !prepare_operand(src1, rows1, cols1, true, seed, 2, codes1, scales1, dev, &o.map1, &o.a1))
+        return cudaErrorInvalidValue;
+    return launch_dir<true>(rot, rot_block, rnd == 1, o, dev, stream);
 }
 
 }  // namespace mx

@@ -129,3 +129,30 @@ def test_tiny_config_both_operands():
     d = config_inputs("tiny", seed=0)
     for name in ("dY", "X"):
         check_against_oracle(d[name], mx.CONTRACT_ROWS, mx.ROT_HADAMARD_DET, 32, mx.ROUND_RNE)
+
+
+def _pair_check(dy_bits, x_bits, rot, nb, rnd, seed):
+    (c0, s0), (c1, s1) = mx.quantize_pair(
+        torch.from_numpy(np.ascontiguousarray(dy_bits).view(np.int16)).cuda(),
+        torch.from_numpy(np.ascontiguousarray(x_bits).view(np.int16)).cuda(), rot, nb, rnd, seed)
+    mx.check_status()
+    T = dy_bits.shape[0]
+    for bits, (c, sc), tag in ((dy_bits, (c0, s0), 1), (x_bits, (c1, s1), 2)):
+        oc, os_ = oracle.quantize(bits, oracle.CONTRACT_ROWS, rot, nb, rnd, seed, tag)
+        assert np.array_equal(c.cpu().numpy(), oc)
+        assert np.array_equal(sc.cpu().numpy(), tile_scales(os_, bits.shape[1], T))
+
+
+@pytest.mark.parametrize("rot,nb,rnd", [(mx.ROT_HADAMARD_DET, 32, mx.ROUND_RNE),
+                                        (mx.ROT_NONE, 32, mx.ROUND_SR),
+                                        (mx.ROT_HADAMARD_DET, 16, mx.ROUND_RNE),
+                                        (mx.ROT_HADAMARD_RAND, 32, mx.ROUND_RNE),
+                                        (mx.ROT_HADAMARD_DET, 128, mx.ROUND_SR)])
+def test_pair_launch_matches_oracle(rot, nb, rnd):
+    # two operands of different widths (ragged vs the 64/128-line tiles), one launch
+    _pair_check(_rand_bits((1280, 200), 7, 1e-3), _rand_bits((1280, 328), 8), rot, nb, rnd, 11)
+
+
+def test_pair_launch_tiny_config():
+    d = config_inputs("tiny", seed=0)
+    _pair_check(d["dY"], d["X"], mx.ROT_HADAMARD_DET, 32, mx.ROUND_RNE, 0)
