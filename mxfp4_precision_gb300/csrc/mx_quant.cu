@@ -36,7 +36,11 @@ namespace {
 #ifndef MXQ_STAGES
 #define MXQ_STAGES 2
 #endif
-constexpr int kStages = MXQ_STAGES;  // TMA ring depth per CTA (2 stages: 3 CTAs per SM)
+constexpr int kStages = MXQ_STAGES;  // TMA ring depth per CTA
+// Two resident CTAs per SM (shared memory allows no more with two stages):
+// the round-to-nearest colwise kernels are held to 128 registers so that the
+// random-sign variants do not fall to one CTA per SM.
+constexpr int kColMinBlocks = 2;
 constexpr int kThreads = 256;
 constexpr uint32_t kTileBytes = 32768;  // 256 x 64 bf16 (colwise) / 64 x 256 bf16 (rowwise)
 constexpr uint32_t kScaleStage = 512;   // two half-atoms of scales per tile
@@ -202,11 +206,30 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
-// max(|a|, m), NaN-propagating: a NaN anywhere in the block survives.
-__device__ __forceinline__ float absmax_nan(float m, float a) {
+// NaN-propagating maxima of magnitudes: a NaN anywhere in a block survives
+// (max.NaN returns the canonical NaN, whose bits exceed every other magnitude).
+__device__ __forceinline__ float absmax2_nan(float a, float b) {
     float r;
-    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(fabsf(a)), "f"(m));
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(fabsf(a)), "f"(fabsf(b)));
     return r;
+}
+__device__ __forceinline__ float absmax3_nan(float a, float b, float c) {
+    float r;
+    asm("max.NaN.abs.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// max |v_i| over 32 values as a tree of three-input maxima (17 instructions).
+__device__ __forceinline__ float block_amax32(const float (&v)[32]) {
+    float t[11];
+#pragma unroll
+    for (int j = 0; j < 10; ++j) t[j] = absmax3_nan(v[3 * j], v[3 * j + 1], v[3 * j + 2]);
+    t[10] = absmax2_nan(v[30], v[31]);
+    float u[4];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) u[j] = absmax3_nan(t[3 * j], t[3 * j + 1], t[3 * j + 2]);
+    u[3] = absmax2_nan(t[9], t[10]);
+    return absmax2_nan(absmax3_nan(u[0], u[1], u[2]), u[3]);
 }
 
 // Butterfly stages of stride 1 .. min(N,32)/2 on 32 channel pairs.
@@ -235,24 +258,45 @@ __device__ __forceinline__ uint32_t scale_of(float amax, float &inv) {
     return m >= 0x7F800000u ? 0xFFu : sb;       // Inf/NaN in the block: NaN scale
 }
 
-// Round-to-nearest encode of two channels' blocks held as pairs.
-__device__ __forceinline__ void encode_pair_rne(const uint64_t (&x)[32], uint4 &q0, uint4 &q1,
+// Round-to-nearest encode of two channels' blocks held as pairs.  x holds the
+// rotation's butterfly sums before the 1/sqrt(n) factor cn (cn = 1: none).
+// Rounding is monotone, so the block amax of fl(x*cn) is fl(amax(x)*cn), and
+// the scale comes out exactly as if every value had been normalised first.
+// The normalised value is then divided by the scale's power of two; when the
+// scale exponent keeps both fl(x*cn) and cn*2^-e away from the subnormal
+// range, fl(fl(x*cn)*2^-e) == fl(x*(cn*2^-e)) (scaling by a power of two
+// commutes with rounding in the normal range, and any value that lands below
+// it encodes to a signed zero either way), so one multiply does both.
+// Outside that range the two multiplies are done one after the other.
+template <bool NORM>
+__device__ __forceinline__ void encode_pair_rne(uint64_t (&x)[32], float cn, uint4 &q0, uint4 &q1,
                                                 uint32_t &s0, uint32_t &s1) {
-    float m0 = 0.0f, m1 = 0.0f;
+    float l[32], h[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        float lo, hi;
-        unpack2(x[i], lo, hi);
-        m0 = absmax_nan(m0, lo);
-        m1 = absmax_nan(m1, hi);
+    for (int i = 0; i < 32; ++i) unpack2(x[i], l[i], h[i]);
+    float m0 = block_amax32(l), m1 = block_amax32(h);
+    if (NORM) {
+        m0 = __fmul_rn(m0, cn);
+        m1 = __fmul_rn(m1, cn);
     }
     float inv0, inv1;
     s0 = scale_of(m0, inv0);
     s1 = scale_of(m1, inv1);
-    const uint64_t inv = pack2(inv0, inv1);
+    uint64_t mult = pack2(inv0, inv1);
+    if (NORM) {
+        // Scale bytes 4 .. 249 (or a NaN scale, whose codes are discarded).
+        const bool fused = (s0 - 4u <= 245u || s0 == 0xFFu) && (s1 - 4u <= 245u || s1 == 0xFFu);
+        if (fused) {
+            mult = pack2(__fmul_rn(inv0, cn), __fmul_rn(inv1, cn));
+        } else {
+            const uint64_t cc = pack2(cn, cn);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] = mul2(x[i], cc);
+        }
+    }
     float v0[32], v1[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) unpack2(mul2(x[i], inv), v0[i], v1[i]);
+    for (int i = 0; i < 32; ++i) unpack2(mul2(x[i], mult), v0[i], v1[i]);
     uint32_t w0[4], w1[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -340,8 +384,17 @@ __device__ __forceinline__ int64_t scale_offset(int64_t line, int64_t block, int
 // sizes up to 32 every warp works on its own 32-token slice of the tile and
 // no CTA-wide barrier is taken inside the loop: each warp marks the stage
 // consumed on an mbarrier and thread 0 refills it once all eight have.
+// Column-wise tile: TT tokens x TC channels of bf16 (32 KB).  128 x 128 gives
+// 256-byte contiguous row segments; a 256-token Hadamard needs 256 x 64.
+template <int ROTN>
+struct ColTile {
+    static constexpr int TT = ROTN == 256 ? 256 : 128;
+    static constexpr int TC = 32768 / (2 * TT);
+    static constexpr int TOKEN_BLOCKS = TT / 32;  // warps along tokens
+};
+
 template <int ROTN, bool RAND, bool SR>
-__global__ void __launch_bounds__(kThreads) mxq_colwise_kernel(
+__global__ void __launch_bounds__(kThreads, SR ? 1 : kColMinBlocks) mxq_colwise_kernel(
     const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
     const QuantArgs a0, const QuantArgs a1) {
     constexpr bool kCtaSync = ROTN >= 64;  // cross-warp Hadamard stages need CTA barriers
@@ -355,7 +408,10 @@ __global__ void __launch_bounds__(kThreads) mxq_colwise_kernel(
     float2 *xchg = reinterpret_cast<float2 *>(smem + kStages * kTileBytes + 1024);  // 64 KB
     __shared__ int abort_flag;
 
+    using G = ColTile<ROTN>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tbi = warp % G::TOKEN_BLOCKS;   // this warp's 32-token block in the tile
+    const int chalf = warp / G::TOKEN_BLOCKS;  // this warp's 64-channel slice of the tile
     const int total = a0.num_tiles + a1.num_tiles;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -374,8 +430,8 @@ __global__ void __launch_bounds__(kThreads) mxq_colwise_kernel(
         const int lt = second ? tile - a0.num_tiles : tile;
         const int inner = second ? a1.tiles_inner : a0.tiles_inner;
         mbar_arrive_expect_tx(&full[s], kTileBytes);
-        tma_load_2d(tiles + s * kTileBytes, second ? &map1 : &map0, &full[s], (lt % inner) * 64,
-                    (lt / inner) * 256);
+        tma_load_2d(tiles + s * kTileBytes, second ? &map1 : &map0, &full[s], (lt % inner) * G::TC,
+                    (lt / inner) * G::TT);
     };
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -397,8 +453,8 @@ __global__ void __launch_bounds__(kThreads) mxq_colwise_kernel(
         const int64_t katoms = second ? a1.katoms : a0.katoms;
         uint8_t *const codes = second ? a1.codes : a0.codes;
         uint8_t *const scales = second ? a1.scales : a0.scales;
-        const int64_t t0 = static_cast<int64_t>(lt / inner) * 256;
-        const int64_t c0 = static_cast<int64_t>(lt % inner) * 64;
+        const int64_t t0 = static_cast<int64_t>(lt / inner) * G::TT;
+        const int64_t c0 = static_cast<int64_t>(lt % inner) * G::TC;
 
         int ok = 1;
         if (lane == 0) ok = mbar_wait(&full[s], parity, a0.status, &abort_flag) ? 1 : 0;
@@ -409,13 +465,13 @@ __global__ void __launch_bounds__(kThreads) mxq_colwise_kernel(
             break;
         }
 
-        // Column pair (2*lane, 2*lane+1), tokens 32*warp .. 32*warp+31, as
+        // Column pair (64*chalf + 2*lane, +1), tokens 32*tbi .. 32*tbi+31, as
         // 32 register pairs {channel 2*lane, channel 2*lane+1}.
         uint64_t x[32];
         const uint32_t *tw = reinterpret_cast<const uint32_t *>(tiles + s * kTileBytes);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-            const uint32_t v = tw[(warp * 32 + i) * 32 + lane];
+            const uint32_t v = tw[(tbi * 32 + i) * (G::TC / 2) + chalf * 32 + lane];
             x[i] = pack2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
         }
         if (kCtaSync) {
@@ -435,7 +491,8 @@ __global__ void __launch_bounds__(kThreads) mxq_colwise_kernel(
 
         if (ROTN > 0) {
             if (RAND) {
-                const uint32_t bits = sign_bits32(a0.seed, static_cast<uint64_t>(t0 / 256), warp);
+                const uint32_t bits = sign_bits32(a0.seed, static_cast<uint64_t>(t0 / 256),
+                                                  static_cast<int>((t0 % 256) / 32) + tbi);
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
                     x[i] ^= ((bits >> i) & 1u) ? 0x8000000080000000ull : 0ull;
@@ -459,14 +516,16 @@ __global__ void __launch_bounds__(kThreads) mxq_colwise_kernel(
                     __syncthreads();
                 }
             }
-            const float cn = hadamard_norm<ROTN>();
-            const uint64_t cc = pack2(cn, cn);
+            if (SR) {  // round to nearest folds the factor into the scale multiply
+                const float cn = hadamard_norm<ROTN>();
+                const uint64_t cc = pack2(cn, cn);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) x[i] = mul2(x[i], cc);
+                for (int i = 0; i < 32; ++i) x[i] = mul2(x[i], cc);
+            }
         }
 
-        const int64_t tb = t0 + 32 * warp;   // first token of this thread's block
-        const int64_t c = c0 + 2 * lane;     // first of the thread's two channels
+        const int64_t tb = t0 + 32 * tbi;               // first token of this thread's block
+        const int64_t c = c0 + 64 * chalf + 2 * lane;  // first of the thread's two channels
         uint4 q0, q1;
         uint32_t s0, s1;
         if (SR) {
@@ -480,7 +539,7 @@ __global__ void __launch_bounds__(kThreads) mxq_colwise_kernel(
             sr_draws32(a0.seed, tag, static_cast<uint64_t>((c + 1) * L + tb), u);
             s1 = encode_block32<true>(x1, q1, u);
         } else {
-            encode_pair_rne(x, q0, q1, s0, s1);
+            encode_pair_rne<(ROTN > 0)>(x, ROTN > 0 ? hadamard_norm<ROTN>() : 1.0f, q0, q1, s0, s1);
         }
 
         if (tb < L) {
@@ -696,9 +755,9 @@ cudaError_t launch_dir(int rot, int rot_block, bool sr, const Operands &o, const
 }
 
 // Fills the per-operand arguments (and tensor map) of one encode.
-bool prepare_operand(const void *src, int64_t rows, int64_t cols, bool colwise, uint64_t seed,
-                     uint64_t sr_tag, void *codes, void *scales, const DeviceInfo &dev,
-                     CUtensorMap *map, QuantArgs *a) {
+bool prepare_operand(const void *src, int64_t rows, int64_t cols, bool colwise, int col_tt,
+                     uint64_t seed, uint64_t sr_tag, void *codes, void *scales,
+                     const DeviceInfo &dev, CUtensorMap *map, QuantArgs *a) {
     *a = QuantArgs{};
     a->L = colwise ? rows : cols;
     a->lines = colwise ? cols : rows;
@@ -710,15 +769,20 @@ bool prepare_operand(const void *src, int64_t rows, int64_t cols, bool colwise, 
     a->status = dev.status;
     // Tiles cover the padded scale layout: lines to a multiple of 128 and the
     // contraction dim to a multiple of 256, so padding scale bytes get zeros.
+    if (colwise) {
+        const int col_tc = 32768 / (2 * col_tt);
+        const int64_t line_tiles = scale_groups(a->lines) * (128 / col_tc);
+        const int64_t k_tiles = ((a->L + 255) / 256) * (256 / col_tt);
+        if (line_tiles * k_tiles > 0x3FFFFFFF) return false;
+        a->num_tiles = static_cast<int>(line_tiles * k_tiles);
+        a->tiles_inner = static_cast<int>(line_tiles);
+        return encode_tmap_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, src, cols, rows, cols * 2,
+                              col_tc, col_tt, CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
     const int64_t line_tiles = scale_groups(a->lines) * 2;  // 64 lines per tile
     const int64_t k_tiles = (a->L + 255) / 256;
     if (line_tiles * k_tiles > 0x3FFFFFFF) return false;
     a->num_tiles = static_cast<int>(line_tiles * k_tiles);
-    if (colwise) {
-        a->tiles_inner = static_cast<int>(line_tiles);
-        return encode_tmap_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, src, cols, rows, cols * 2, 64,
-                              256, CU_TENSOR_MAP_SWIZZLE_NONE);
-    }
     a->tiles_inner = static_cast<int>(k_tiles);
     return encode_tmap_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, src, cols, rows, cols * 2, 64, 64,
                           CU_TENSOR_MAP_SWIZZLE_128B);
@@ -732,7 +796,9 @@ cudaError_t launch_quantize(const void *src, int64_t rows, int64_t cols, int con
                             cudaStream_t stream) {
     const bool colwise = contract == 0;
     Operands o;
-    if (!prepare_operand(src, rows, cols, colwise, seed, sr_tag, codes, scales, dev, &o.map0, &o.a0))
+    const int tt = (rot != 0 && rot_block == 256) ? 256 : 128;
+    if (!prepare_operand(src, rows, cols, colwise, tt, seed, sr_tag, codes, scales, dev, &o.map0,
+                         &o.a0))
         return cudaErrorInvalidValue;
     o.map1 = o.map0;
     o.a1 = QuantArgs{};
@@ -746,8 +812,11 @@ cudaError_t launch_quantize_pair_colwise(const void *src0, int64_t rows0, int64_
                                          void *scales0, void *codes1, void *scales1,
                                          const DeviceInfo &dev, cudaStream_t stream) {
     Operands o;
-    if (!prepare_operand(src0, rows0, cols0, true, seed, 1, codes0, scales0, dev, &o.map0, &o.a0) ||
-        !prepare_operand(src1, rows1, cols1, true, seed, 2, codes1, scales1, dev, &o.map1, &o.a1))
+    const int tt = (rot != 0 && rot_block == 256) ? 256 : 128;
+    if (!prepare_operand(src0, rows0, cols0, true, tt, seed, 1, codes0, scales0, dev, &o.map0,
+                         &o.a0) ||
+        !prepare_operand(src1, rows1, cols1, true, tt, seed, 2, codes1, scales1, dev, &o.map1,
+                         &o.a1))
         return cudaErrorInvalidValue;
     return launch_dir<true>(rot, rot_block, rnd == 1, o, dev, stream);
 }
