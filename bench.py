@@ -319,6 +319,12 @@ def run_mine(args, world, rank, local):
                         world, dev)
     e2e_value = world * n_e2e * flops_step / (e2e_ms * 1e-3) / 1e12
 
+    # side measurement: the dual-output encode of dY (both backward encodings
+    # from one read) against the two single-direction encodes it replaces
+    dual = None
+    if rank == 0 and not args.no_extras:
+        dual = measure_dual(L, mx, dY, T, N, flush, stream, dev, hbm_gbs=load_peaks()[0]["hbm_gbs"])
+
     # parity spot check of the timed output (oracle entries, rank 0 only)
     parity = None
     if rank == 0 and not args.no_parity_check:
@@ -383,6 +389,7 @@ def run_mine(args, world, rank, local):
                     "d2h_bytes_per_step": dW_h.numel() * 4,
                     "ms_per_step": e2e_ms / n_e2e, "call": "mx_linear_wgrad"},
             "gpu_launches": 2 * n,
+            "dual_quantiser": dual,
             "clocks": clk,
             "parity_spot_check": parity}
     print(json.dumps(line), flush=True)
@@ -390,6 +397,55 @@ def run_mine(args, world, rank, local):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def measure_dual(L, mx, dY, T, N, flush, stream, dev, hbm_gbs, reps=30):
+    """mx_quantize_dual on dY [T, N] vs mx_quantize along T (rotated) + along N,
+    each rep after an L2 flush; algorithmic bytes 2 (bf16 read) + 2 x 0.53125."""
+    import torch
+    sp = stream.cuda_stream
+    ptr = lambda t: t.data_ptr()
+    ct = torch.empty(mx.codes_bytes(N, T), dtype=torch.uint8, device=dev)
+    st = torch.empty(mx.scales_bytes(N, T), dtype=torch.uint8, device=dev)
+    cn = torch.empty(mx.codes_bytes(T, N), dtype=torch.uint8, device=dev)
+    sn = torch.empty(mx.scales_bytes(T, N), dtype=torch.uint8, device=dev)
+    rot, nb = mx.ROT_HADAMARD_DET, 32
+
+    def dual():
+        return [L.mx_quantize_dual(ptr(dY), T, N, rot, nb, 0, 0, ptr(ct), ptr(st), ptr(cn),
+                                   ptr(sn), sp)]
+
+    def separate():
+        return [L.mx_quantize(ptr(dY), T, N, mx.CONTRACT_ROWS, rot, nb, 0, 0, ptr(ct), ptr(st), sp),
+                L.mx_quantize(ptr(dY), T, N, mx.CONTRACT_COLS, mx.ROT_NONE, 32, 0, 0, ptr(cn),
+                              ptr(sn), sp)]
+
+    def timed(fn):
+        for _ in range(3):
+            flush.zero_()
+            if any(fn()):
+                raise RuntimeError("dual-output measurement launch failed")
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ts.append(e0.elapsed_time(e1))
+        return sorted(ts)[len(ts) // 2]
+
+    t_dual, t_sep = timed(dual), timed(separate)
+    mx.check_status()
+    nbytes = T * N * (2 + 2 * (0.5 + 1 / 32))
+    return {"call": "mx_quantize_dual", "input": f"dY [{T},{N}] bf16",
+            "outputs": "along T (det-Hadamard 32, Wgrad operand) + along N (no rotation, "
+                       "Dgrad operand), RNE",
+            "ms": t_dual, "ms_two_separate_launches": t_sep,
+            "achieved_gbs": nbytes / (t_dual * 1e-3) / 1e9, "peak_gbs": hbm_gbs,
+            "frac": nbytes / (t_dual * 1e-3) / 1e9 / hbm_gbs,
+            "algorithmic_bytes": nbytes, "median_of": reps}
 
 
 def spot_check(d, dW, T, N, K):
@@ -421,6 +477,8 @@ def main():
     ap.add_argument("--ref-budget-s", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-parity-check", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the dual-output encode side measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -134,6 +134,27 @@ mx_status mx_quantize_pair(const void *d_src0, int64_t rows0, int64_t cols0, con
                            void *d_scales1, void *stream);
 
 /*
+ * mx_quantize_dual -- one read of the output gradient d_src[T][N] (bf16,
+ * row-major) writes both encodings a linear layer's backward pass needs
+ * ([36kr] "Fehlerdiagnoseexperiment": dY feeds both Dgrad dX = dY W,
+ * contracting N, and Wgrad dW = dY^T X, contracting T):
+ *   d_codes_t / d_scales_t  the Wgrad operand: as mx_quantize(d_src, T, N,
+ *                           MX_CONTRACT_ROWS, rot, rot_block, rnd, seed)
+ *                           (N lines, contraction T, rotated along T);
+ *   d_codes_n / d_scales_n  the Dgrad operand: as mx_quantize(d_src, T, N,
+ *                           MX_CONTRACT_COLS, MX_ROT_NONE, 32, rnd, seed)
+ *                           (T lines, contraction N, no rotation).
+ * Both encodings are bit-identical to the two separate calls; SR draws use
+ * key (seed, 1) for both (dY is operand A of both GEMMs), each with its own
+ * line*k + position counter.  Argument rules are the union of the two calls
+ * (T % 32, T % rot_block, N % 32, N % 8).  T == 0 or N == 0: MX_OK, nothing
+ * launched.
+ */
+mx_status mx_quantize_dual(const void *d_src, int64_t T, int64_t N, int rot, int rot_block,
+                           int rnd, uint64_t seed, void *d_codes_t, void *d_scales_t,
+                           void *d_codes_n, void *d_scales_n, void *stream);
+
+/*
  * mx_gemm -- C[M][N] (fp32, row-major, overwritten) = A . B^T, where A is an
  * encoded operand with M lines and B one with N lines, both of contraction
  * length K (K % 32 == 0).  Block-scaled FP4 tensor-core contraction with fp32

@@ -10,14 +10,14 @@ from ._binding import (CONTRACT_COLS, CONTRACT_ROWS, OP_DGRAD, OP_FPROP, OP_WGRA
                        ROT_HADAMARD_RAND, ROT_NONE, ROUND_RNE, ROUND_SR, MXError, check_status,
                        codes_bytes, debug_timeout_probe, gemm, gemm_into, lib, library_path,
                        linear_dgrad, linear_fprop, linear_wgrad, linear_wgrad_noalloc,
-                       linear_workspace_bytes, NOALLOC_SCRATCH_BYTES, quantize, quantize_pair,
-                       quantize_into, scales_bytes, status_string)
+                       linear_workspace_bytes, NOALLOC_SCRATCH_BYTES, quantize, quantize_dual,
+                       quantize_pair, quantize_into, scales_bytes, status_string)
 
 __all__ = [
     "CONTRACT_COLS", "CONTRACT_ROWS", "OP_DGRAD", "OP_FPROP", "OP_WGRAD", "ROT_HADAMARD_DET",
     "ROT_HADAMARD_RAND", "ROT_NONE", "ROUND_RNE", "ROUND_SR", "MXError", "check_status",
     "codes_bytes", "debug_timeout_probe", "gemm", "gemm_into", "lib", "library_path",
     "linear_dgrad", "linear_fprop", "linear_wgrad", "linear_wgrad_noalloc", "linear_workspace_bytes",
-    "NOALLOC_SCRATCH_BYTES", "quantize", "quantize_pair",
+    "NOALLOC_SCRATCH_BYTES", "quantize", "quantize_dual", "quantize_pair",
     "quantize_into", "scales_bytes", "status_string",
 ]

@@ -21,7 +21,8 @@ CONTRACT_ROWS, CONTRACT_COLS = 0, 1
 OP_FPROP, OP_DGRAD, OP_WGRAD = 0, 1, 2
 
 EXPORTED = [
-    "mx_codes_bytes", "mx_scales_bytes", "mx_quantize", "mx_quantize_pair", "mx_gemm", "mx_linear_workspace_bytes",
+    "mx_codes_bytes", "mx_scales_bytes", "mx_quantize", "mx_quantize_pair", "mx_quantize_dual",
+    "mx_gemm", "mx_linear_workspace_bytes",
     "mx_linear_wgrad", "mx_linear_fprop", "mx_linear_dgrad", "mx_linear_wgrad_noalloc",
     "mx_check_status",
     "mx_debug_timeout_probe", "mx_status_string", "mx_version",
@@ -62,6 +63,8 @@ def lib() -> ctypes.CDLL:
             L.mx_quantize_pair.argtypes = [P, i64, i64, P, i64, i64, i32, i32, i32, u64, P, P, P,
                                            P, P]
             L.mx_quantize_pair.restype = i32
+            L.mx_quantize_dual.argtypes = [P, i64, i64, i32, i32, i32, u64, P, P, P, P, P]
+            L.mx_quantize_dual.restype = i32
             L.mx_gemm.argtypes = [P, P, P, P, P, i64, i64, i64, P]
             L.mx_gemm.restype = i32
             L.mx_linear_workspace_bytes.argtypes = [i32, i64, i64, i64]
@@ -165,6 +168,26 @@ def quantize_pair(src0: torch.Tensor, src1: torch.Tensor, rot: int = ROT_HADAMAR
                                 _dev_ptr(out[1][1], "scales1"), _stream(stream))
     _check(st, "mx_quantize_pair")
     return out[0], out[1]
+
+
+def quantize_dual(src: torch.Tensor, rot: int = ROT_HADAMARD_DET, rot_block: int = 32,
+                  rnd: int = ROUND_RNE, seed: int = 0, stream=None):
+    """Both encodings of an output gradient dY [T, N] from one read: returns
+    ((codes_t, scales_t), (codes_n, scales_n)) -- the Wgrad operand (contraction
+    T, rotated) and the Dgrad operand (contraction N, no rotation)."""
+    src = _as_bf16_bits(src)
+    T, N = src.shape
+    d = src.device
+    codes_t = torch.empty((N, T // 2), dtype=torch.uint8, device=d)
+    scales_t = torch.empty((max(1, scales_bytes(N, T)),), dtype=torch.uint8, device=d)
+    codes_n = torch.empty((T, N // 2), dtype=torch.uint8, device=d)
+    scales_n = torch.empty((max(1, scales_bytes(T, N)),), dtype=torch.uint8, device=d)
+    st = lib().mx_quantize_dual(_dev_ptr(src, "src"), T, N, rot, rot_block, rnd, seed,
+                                _dev_ptr(codes_t, "codes_t"), _dev_ptr(scales_t, "scales_t"),
+                                _dev_ptr(codes_n, "codes_n"), _dev_ptr(scales_n, "scales_n"),
+                                _stream(stream))
+    _check(st, "mx_quantize_dual")
+    return (codes_t, scales_t), (codes_n, scales_n)
 
 
 def gemm_into(Aq, As, Bq, Bs, C: torch.Tensor, M: int, N: int, K: int, stream=None) -> None:

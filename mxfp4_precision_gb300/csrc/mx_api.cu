@@ -201,6 +201,20 @@ mx_status quantize_pair_impl(const void *src0, int64_t rows0, int64_t cols0, con
                                                   scales1, *dev, stream));
 }
 
+mx_status quantize_dual_impl(const void *src, int64_t T, int64_t N, int rot, int rot_block,
+                             int rnd, uint64_t seed, void *codes_t, void *scales_t, void *codes_n,
+                             void *scales_n, cudaStream_t stream) {
+    mx_status st = check_encode(src, T, N, MX_CONTRACT_ROWS, rot, rot_block, rnd, codes_t,
+                                scales_t);
+    if (st != MX_OK) return st;
+    st = check_encode(src, T, N, MX_CONTRACT_COLS, MX_ROT_NONE, 32, rnd, codes_n, scales_n);
+    if (st != MX_OK || T == 0 || N == 0) return st;
+    const DeviceInfo *dev = nullptr;
+    if ((st = device_or_error(&dev)) != MX_OK) return st;
+    return from_cuda(launch_quantize_dual(src, T, N, rot, rot_block, rnd, seed, codes_t, scales_t,
+                                          codes_n, scales_n, *dev, stream));
+}
+
 mx_status gemm_impl(const void *Aq, const void *As, const void *Bq, const void *Bs, float *C,
                     int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
     mx_status st = check_gemm(Aq, As, Bq, Bs, C, M, N, K);
@@ -283,6 +297,13 @@ mx_status mx_quantize_pair(const void *d_src0, int64_t rows0, int64_t cols0, con
     return quantize_pair_impl(d_src0, rows0, cols0, d_src1, rows1, cols1, rot, rot_block, rnd, seed,
                               d_codes0, d_scales0, d_codes1, d_scales1,
                               static_cast<cudaStream_t>(stream));
+}
+
+mx_status mx_quantize_dual(const void *d_src, int64_t T, int64_t N, int rot, int rot_block,
+                           int rnd, uint64_t seed, void *d_codes_t, void *d_scales_t,
+                           void *d_codes_n, void *d_scales_n, void *stream) {
+    return quantize_dual_impl(d_src, T, N, rot, rot_block, rnd, seed, d_codes_t, d_scales_t,
+                              d_codes_n, d_scales_n, static_cast<cudaStream_t>(stream));
 }
 
 mx_status mx_gemm(const void *d_Aq, const void *d_As, const void *d_Bq, const void *d_Bs,

@@ -39,6 +39,13 @@ cudaError_t launch_quantize_pair_colwise(const void *src0, int64_t rows0, int64_
                                          int rot_block, int rnd, uint64_t seed, void *codes0,
                                          void *scales0, void *codes1, void *scales1,
                                          const DeviceInfo &dev, cudaStream_t stream);
+// One read of src [rows, cols] writes its column-direction encoding (blocks
+// along rows, rotated) and its row-direction encoding (blocks along cols,
+// no rotation).
+cudaError_t launch_quantize_dual(const void *src, int64_t rows, int64_t cols, int rot,
+                                 int rot_block, int rnd, uint64_t seed, void *codes_t,
+                                 void *scales_t, void *codes_n, void *scales_n,
+                                 const DeviceInfo &dev, cudaStream_t stream);
 
 cudaError_t launch_gemm(const void *Aq, const void *As, const void *Bq, const void *Bs, float *C,
                         int64_t M, int64_t N, int64_t K, const DeviceInfo &dev,

@@ -372,6 +372,40 @@ __device__ __forceinline__ void flush_scales(const uint8_t *stage, const QuantAr
     }
 }
 
+// ---------------------------------------------------------------- dual output
+// Row-direction (channel-contiguous) encode of one 32-channel block of one
+// token, straight from a staged column-wise tile: no rotation, blocks of 32
+// along the row.  w holds the block's 16 words (two bf16 channels each,
+// channel 2i in the low half).
+template <bool SR>
+__device__ __forceinline__ uint32_t encode_row_block(const uint32_t (&w)[16], uint4 &q,
+                                                     uint64_t seed, uint64_t tag, uint64_t e0) {
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+    if (SR) {
+        uint32_t u[32];
+        sr_draws32(seed, tag, e0, u);
+        return encode_block32<true>(v, q, u);
+    }
+    float inv;
+    const uint32_t sb = scale_of(block_amax32(v), inv);
+    const uint64_t mult = pack2(inv, inv);
+    float r[32];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) unpack2(mul2(pack2(v[2 * i], v[2 * i + 1]), mult), r[2 * i], r[2 * i + 1]);
+    uint32_t c[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        c[j] = cvt_e2m1x8(r[8 * j], r[8 * j + 1], r[8 * j + 2], r[8 * j + 3], r[8 * j + 4],
+                          r[8 * j + 5], r[8 * j + 6], r[8 * j + 7]);
+    q = sb == 0xFFu ? make_uint4(0, 0, 0, 0) : make_uint4(c[0], c[1], c[2], c[3]);
+    return sb;
+}
+
 // ---------------------------------------------------------------- colwise
 // Byte offset of the scale of (line, block) in the tiled layout.
 __device__ __forceinline__ int64_t scale_offset(int64_t line, int64_t block, int64_t katoms) {
@@ -393,10 +427,13 @@ struct ColTile {
     static constexpr int TOKEN_BLOCKS = TT / 32;  // warps along tokens
 };
 
-template <int ROTN, bool RAND, bool SR>
+// With DUAL, the launch has one source operand (a0) and also writes its
+// row-direction encoding (blocks of 32 along the channels, no rotation) to
+// `ar`, from the same staged tiles: one HBM read serves both encodings.
+template <int ROTN, bool RAND, bool SR, bool DUAL>
 __global__ void __launch_bounds__(kThreads, SR ? 1 : kColMinBlocks) mxq_colwise_kernel(
     const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
-    const QuantArgs a0, const QuantArgs a1) {
+    const QuantArgs a0, const QuantArgs a1, const QuantArgs ar) {
     constexpr bool kCtaSync = ROTN >= 64;  // cross-warp Hadamard stages need CTA barriers
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned base, kept as a shared-space pointer (offset arithmetic
@@ -473,6 +510,43 @@ __global__ void __launch_bounds__(kThreads, SR ? 1 : kColMinBlocks) mxq_colwise_
         for (int i = 0; i < 32; ++i) {
             const uint32_t v = tw[(tbi * 32 + i) * (G::TC / 2) + chalf * 32 + lane];
             x[i] = pack2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+        }
+        if (DUAL) {
+            // Row direction: each thread encodes two (token, 32-channel) blocks
+            // of the tile.  The four 16-byte reads of a block start at a
+            // row-dependent chunk so that a warp's reads spread over all banks.
+            const int64_t row_lines_pad = (ar.lines + 127) / 128 * 128;
+            const int64_t grid_end = (a0.lines + 127) / 128 * 128;  // channels the tiles cover
+            const int64_t kb_pad = ar.katoms * 4;                    // padded blocks per row
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int b = threadIdx.x + kThreads * h;
+                const int trow = b / (G::TC / 32), cb = b % (G::TC / 32);
+                const int64_t t = t0 + trow;
+                if (t >= row_lines_pad) continue;
+                const int64_t c = c0 + 32 * cb;
+                uint32_t w[16];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int jj = (j + trow) & 3;
+                    const uint4 v = *reinterpret_cast<const uint4 *>(
+                        tw + trow * (G::TC / 2) + 16 * cb + 4 * jj);
+                    w[4 * jj] = v.x, w[4 * jj + 1] = v.y, w[4 * jj + 2] = v.z, w[4 * jj + 3] = v.w;
+                }
+                uint4 q;
+                const uint32_t sb = encode_row_block<SR>(w, q, a0.seed, ar.sr_tag,
+                                                         static_cast<uint64_t>(t * ar.L + c));
+                if (t < ar.lines && c < ar.L) st_global_16(ar.codes + t * (ar.L / 2) + c / 2, q);
+                ar.scales[scale_offset(t, c / 32, ar.katoms)] = static_cast<uint8_t>(sb);
+                // Padding blocks past the last channel tile: no tile covers them.
+                if (c0 + G::TC == grid_end) {
+#pragma unroll
+                    for (int e = 0; e < 128 / G::TC; ++e) {
+                        const int64_t pb = grid_end / 32 + cb + e * (G::TC / 32);
+                        if (pb < kb_pad) ar.scales[scale_offset(t, pb, ar.katoms)] = 0;
+                    }
+                }
+            }
         }
         if (kCtaSync) {
             __syncthreads();  // stage s fully consumed
@@ -714,6 +788,8 @@ cudaError_t launch_persistent(Kern kernel, int num_tiles, size_t smem, const Dev
 struct Operands {
     CUtensorMap map0, map1;
     QuantArgs a0, a1;
+    QuantArgs ar;  // row-direction output of a dual encode
+    bool dual = false;
 };
 
 template <bool COLWISE, int ROTN, bool RAND>
@@ -721,10 +797,15 @@ cudaError_t launch_rot(bool sr, const Operands &o, const DeviceInfo &dev, cudaSt
     if (COLWISE) {
         const size_t smem = kStages * kTileBytes + 1024 + (ROTN >= 64 ? 65536 : 0) + 1024;
         const int n = o.a0.num_tiles + o.a1.num_tiles;
-        return sr ? launch_persistent(mxq_colwise_kernel<ROTN, RAND, true>, n, smem, dev, stream,
-                                      o.map0, o.map1, o.a0, o.a1)
-                  : launch_persistent(mxq_colwise_kernel<ROTN, RAND, false>, n, smem, dev, stream,
-                                      o.map0, o.map1, o.a0, o.a1);
+        if (o.dual)
+            return sr ? launch_persistent(mxq_colwise_kernel<ROTN, RAND, true, true>, n, smem, dev,
+                                          stream, o.map0, o.map1, o.a0, o.a1, o.ar)
+                      : launch_persistent(mxq_colwise_kernel<ROTN, RAND, false, true>, n, smem,
+                                          dev, stream, o.map0, o.map1, o.a0, o.a1, o.ar);
+        return sr ? launch_persistent(mxq_colwise_kernel<ROTN, RAND, true, false>, n, smem, dev,
+                                      stream, o.map0, o.map1, o.a0, o.a1, o.ar)
+                  : launch_persistent(mxq_colwise_kernel<ROTN, RAND, false, false>, n, smem, dev,
+                                      stream, o.map0, o.map1, o.a0, o.a1, o.ar);
     }
     const size_t smem = kStages * kTileBytes + 1024 + 1024;
     return sr ? launch_persistent(mxq_rowwise_kernel<ROTN, RAND, true>, o.a0.num_tiles, smem, dev,
@@ -802,6 +883,7 @@ cudaError_t launch_quantize(const void *src, int64_t rows, int64_t cols, int con
         return cudaErrorInvalidValue;
     o.map1 = o.map0;
     o.a1 = QuantArgs{};
+    o.ar = QuantArgs{};
     if (colwise) return launch_dir<true>(rot, rot_block, rnd == 1, o, dev, stream);
     return launch_dir<false>(rot, rot_block, rnd == 1, o, dev, stream);
 }
@@ -818,6 +900,31 @@ cudaError_t launch_quantize_pair_colwise(const void *src0, int64_t rows0, int64_
         !prepare_operand(src1, rows1, cols1, true, tt, seed, 2, codes1, scales1, dev, &o.map1,
                          &o.a1))
         return cudaErrorInvalidValue;
+    o.ar = QuantArgs{};
+    return launch_dir<true>(rot, rot_block, rnd == 1, o, dev, stream);
+}
+
+cudaError_t launch_quantize_dual(const void *src, int64_t rows, int64_t cols, int rot,
+                                 int rot_block, int rnd, uint64_t seed, void *codes_t,
+                                 void *scales_t, void *codes_n, void *scales_n,
+                                 const DeviceInfo &dev, cudaStream_t stream) {
+    Operands o;
+    const int tt = (rot != 0 && rot_block == 256) ? 256 : 128;
+    if (!prepare_operand(src, rows, cols, true, tt, seed, 1, codes_t, scales_t, dev, &o.map0,
+                         &o.a0))
+        return cudaErrorInvalidValue;
+    o.map1 = o.map0;
+    o.a1 = QuantArgs{};
+    o.ar = QuantArgs{};
+    o.ar.L = cols;
+    o.ar.lines = rows;
+    o.ar.katoms = scale_katoms(cols);
+    o.ar.codes = static_cast<uint8_t *>(codes_n);
+    o.ar.scales = static_cast<uint8_t *>(scales_n);
+    o.ar.seed = seed;
+    o.ar.sr_tag = 1;
+    o.ar.status = dev.status;
+    o.dual = true;
     return launch_dir<true>(rot, rot_block, rnd == 1, o, dev, stream);
 }
 

@@ -93,6 +93,26 @@ def test_quantize_rejects_bad_arguments_before_launch(L):
     assert _q(L, rows=0) == 0 and _q(L, cols=0) == 0  # empty: nothing to do
 
 
+def _qd(L, src=0x1000, T=256, N=128, rot=1, nb=32, rnd=0, ct=0x2000, st=0x3000, cn=0x4000,
+        sn=0x5000):
+    return L.mx_quantize_dual(src, T, N, rot, nb, rnd, 0, ct, st, cn, sn, None)
+
+
+def test_quantize_dual_rejects_bad_arguments_before_launch(L):
+    # the union of the column-direction and row-direction rules
+    assert _qd(L, rot=3) == 1
+    assert _qd(L, nb=48) == 1
+    assert _qd(L, rnd=5) == 1
+    assert _qd(L, src=0) == 1
+    assert _qd(L, cn=0) == 1 and _qd(L, st=0) == 1
+    assert _qd(L, T=-1) == 2
+    assert _qd(L, T=100) == 2                      # contraction T not a multiple of 32
+    assert _qd(L, T=96, nb=64) == 2                # rot_block must divide T
+    assert _qd(L, N=72) == 2                       # contraction N not a multiple of 32
+    assert _qd(L, src=0x1001) == 3 and _qd(L, sn=0x5008) == 3
+    assert _qd(L, T=0) == 0 and _qd(L, N=0) == 0   # empty: nothing to do
+
+
 def test_gemm_rejects_bad_arguments_before_launch(L):
     g = lambda **k: L.mx_gemm(V(k.get("a", 0x1000)), V(0x2000), V(0x3000), V(0x4000),
                               V(k.get("c", 0x5000)), k.get("M", 128), k.get("N", 256),

@@ -156,3 +156,43 @@ def test_pair_launch_matches_oracle(rot, nb, rnd):
 def test_pair_launch_tiny_config():
     d = config_inputs("tiny", seed=0)
     _pair_check(d["dY"], d["X"], mx.ROT_HADAMARD_DET, 32, mx.ROUND_RNE, 0)
+
+
+def _dual_check(bits, rot, nb, rnd, seed):
+    (ct, st), (cn, sn) = mx.quantize_dual(
+        torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda(), rot, nb, rnd, seed)
+    mx.check_status()
+    T, N = bits.shape
+    # column direction (Wgrad operand): N lines, contraction T, rotated
+    oc, os_ = oracle.quantize(bits, oracle.CONTRACT_ROWS, rot, nb, rnd, seed, 1)
+    assert np.array_equal(ct.cpu().numpy(), oc)
+    assert np.array_equal(st.cpu().numpy(), tile_scales(os_, N, T))
+    # row direction (Dgrad operand): T lines, contraction N, no rotation
+    oc, os_ = oracle.quantize(bits, oracle.CONTRACT_COLS, oracle.ROT_NONE, 32, rnd, seed, 1)
+    assert np.array_equal(cn.cpu().numpy(), oc)
+    assert np.array_equal(sn.cpu().numpy(), tile_scales(os_, T, N))  # padding bytes are zero
+
+
+@pytest.mark.parametrize("rot,nb", ROTS)
+@pytest.mark.parametrize("rnd", [mx.ROUND_RNE, mx.ROUND_SR])
+def test_dual_parity(rot, nb, rnd):
+    # N = 352: ceil(N/128) is odd, so the row-direction scale padding reaches past
+    # the last channel tile; T = 1280 spans several token tiles
+    _dual_check(_rand_bits((1280, 352), 12), rot, nb, rnd, 5)
+
+
+@pytest.mark.parametrize("T,N", [(800, 96), (256, 128), (512, 224), (96, 32)])
+def test_dual_ragged_shapes(T, N):
+    # T = 800 / 96: the token tiles run past the row-direction padding
+    _dual_check(_rand_bits((T, N), 13), mx.ROT_HADAMARD_DET, 32, mx.ROUND_RNE, 0)
+
+
+def test_dual_edge_cases():
+    x = _edge_matrix()
+    _dual_check(x, mx.ROT_HADAMARD_DET, 32, mx.ROUND_RNE, 3)
+    _dual_check(x, mx.ROT_NONE, 32, mx.ROUND_SR, 3)
+
+
+def test_dual_tiny_config_dy():
+    d = config_inputs("tiny", seed=0, only=("dY",))
+    _dual_check(d["dY"], mx.ROT_HADAMARD_DET, 32, mx.ROUND_RNE, 0)
