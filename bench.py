@@ -297,26 +297,65 @@ def run_mine(args, world, rank, local):
     flops_step = 2.0 * N * K * T
     value = world * n * flops_step / (total_ms * 1e-3) / 1e12
 
-    # ---- e2e: public call with host buffers, copies inside the timed region
+    # ---- e2e: public call with host buffers, copies inside the timed region.
+    # Every step copies its inputs host -> device, calls mx_linear_wgrad and
+    # copies dW device -> host.  Steps are pipelined over three streams (input
+    # copies, compute, output copies) with two device buffer sets, so step i+1's
+    # input copy and step i-1's output copy overlap step i's compute, as in a
+    # training loop that streams its layers.  The serial time (one step at a
+    # time on one stream) is reported beside it.
     ws = torch.empty(mx.linear_workspace_bytes(mx.OP_WGRAD, T, N, K), dtype=torch.uint8, device=dev)
-    dW_h = torch.empty((N, K), dtype=torch.float32).pin_memory()
-    dY_d = torch.empty_like(dY)
-    X_d = torch.empty_like(X)
+    dW_h = [torch.empty((N, K), dtype=torch.float32).pin_memory() for _ in range(2)]
+    dY_d = [torch.empty_like(dY) for _ in range(2)]
+    X_d = [torch.empty_like(X) for _ in range(2)]
+    dW_d = [dW, torch.empty_like(dW)]
     n_e2e = max(3, min(n, args.e2e_steps))
-    e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_e2e + 2)]
-    for i in range(n_e2e + 2):       # first two are warm-up
-        flush.zero_()
-        e_ev[i][0].record(stream)
-        dY_d.copy_(dY_h, non_blocking=True)
-        X_d.copy_(X_h, non_blocking=True)
-        check(L.mx_linear_wgrad(ptr(dY_d), ptr(X_d), ptr(dW), T, N, K, rot, nb, rnd, seed,
-                                ptr(ws), ws.numel(), sp), "e2e")
-        dW_h.copy_(dW, non_blocking=True)
-        e_ev[i][1].record(stream)
-    torch.cuda.synchronize(dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    s_cmp = stream
+
+    def e2e_run(steps, pipelined):
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_cmp = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        t0.record(s_in if pipelined else s_cmp)
+        for i in range(steps):
+            b = i % 2 if pipelined else 0
+            if not pipelined:
+                dY_d[b].copy_(dY_h, non_blocking=True)
+                X_d[b].copy_(X_h, non_blocking=True)
+                check(L.mx_linear_wgrad(ptr(dY_d[b]), ptr(X_d[b]), ptr(dW_d[b]), T, N, K, rot, nb,
+                                        rnd, seed, ptr(ws), ws.numel(), sp), "e2e")
+                dW_h[b].copy_(dW_d[b], non_blocking=True)
+                continue
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_cmp[b])      # compute of step i-2 has read buffer b
+                dY_d[b].copy_(dY_h, non_blocking=True)
+                X_d[b].copy_(X_h, non_blocking=True)
+                ev_in[b].record(s_in)
+            s_cmp.wait_event(ev_in[b])
+            if i >= 2:
+                s_cmp.wait_event(ev_out[b])         # step i-2's dW[b] has been copied out
+            check(L.mx_linear_wgrad(ptr(dY_d[b]), ptr(X_d[b]), ptr(dW_d[b]), T, N, K, rot, nb,
+                                    rnd, seed, ptr(ws), ws.numel(), sp), "e2e")
+            ev_cmp[b].record(s_cmp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_cmp[b])
+                dW_h[b].copy_(dW_d[b], non_blocking=True)
+                ev_out[b].record(s_out)
+        if pipelined:
+            s_in.wait_stream(s_cmp)
+            s_in.wait_stream(s_out)
+        t1.record(s_in if pipelined else s_cmp)
+        torch.cuda.synchronize(dev)
+        return t0.elapsed_time(t1)
+
+    e2e_run(2, True)                                 # warm-up
+    e2e_ms = reduce_max(e2e_run(n_e2e, True), world, dev)
+    serial_ms = e2e_run(n_e2e, False)
     mx.check_status()
-    e2e_ms = reduce_max(sum(e_ev[i][0].elapsed_time(e_ev[i][1]) for i in range(2, n_e2e + 2)),
-                        world, dev)
     e2e_value = world * n_e2e * flops_step / (e2e_ms * 1e-3) / 1e12
 
     # side measurement: the dual-output encode of dY (both backward encodings
@@ -386,8 +425,12 @@ def run_mine(args, world, rank, local):
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": dY_h.numel() * 2 + X_h.numel() * 2,
-                    "d2h_bytes_per_step": dW_h.numel() * 4,
-                    "ms_per_step": e2e_ms / n_e2e, "call": "mx_linear_wgrad"},
+                    "d2h_bytes_per_step": dW_h[0].numel() * 4,
+                    "ms_per_step": e2e_ms / n_e2e, "call": "mx_linear_wgrad",
+                    "schedule": "steps pipelined over input-copy / compute / output-copy "
+                                "streams, two device buffer sets",
+                    "serial_ms_per_step": serial_ms / n_e2e,
+                    "serial_value": world * n_e2e * flops_step / (serial_ms * 1e-3) / 1e12},
             "gpu_launches": 2 * n,
             "dual_quantiser": dual,
             "clocks": clk,
