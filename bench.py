@@ -491,6 +491,164 @@ def measure_dual(L, mx, dY, T, N, flush, stream, dev, hbm_gbs, reps=30):
             "algorithmic_bytes": nbytes, "median_of": reps}
 
 
+def run_sweep(args):
+    """The measurements beside the headline (one GPU, one JSON line each):
+    the rotation / rounding ablation at down_proj shapes with its quantisation
+    error, the down_proj Hadamard-size sweep, the six GEMMs of the QKV +
+    gate/up layers, and a cuBLAS bf16 GEMM of the Wgrad shapes for context."""
+    import numpy as np
+    import torch
+
+    import mxfp4_precision_gb300 as mx
+    import oracle
+    from workloads import bf16_bits_to_f32, config_inputs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    L = mx.lib()
+    ptr = lambda t: t.data_ptr()
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    peaks, _ = load_peaks()
+    fp4_peak = peaks["bf16_tflops"] * NOMINAL_FP4_OVER_BF16
+    reps = args.sweep_reps
+
+    def timed(fn):
+        for _ in range(2):
+            flush.zero_()
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ts.append(e0.elapsed_time(e1))
+        mx.check_status()
+        return sorted(ts)[len(ts) // 2]
+
+    def ok(st, what):
+        if st != 0:
+            raise RuntimeError(f"{what}: {mx.status_string(st)}")
+
+    def emit(obj):
+        print(json.dumps(obj), flush=True)
+
+    # ---- down_proj shapes: ablation modes and Hadamard sizes
+    T, N, K = 8192, 4096, 14336
+    d = config_inputs("down_proj", seed=0, only=("dY", "X"))
+    dY = torch.from_numpy(d["dY"].view(np.int16)).to(dev)
+    X = torch.from_numpy(d["X"].view(np.int16)).to(dev)
+    aq = torch.empty(mx.codes_bytes(N, T), dtype=torch.uint8, device=dev)
+    as_ = torch.empty(mx.scales_bytes(N, T), dtype=torch.uint8, device=dev)
+    bq = torch.empty(mx.codes_bytes(K, T), dtype=torch.uint8, device=dev)
+    bs = torch.empty(mx.scales_bytes(K, T), dtype=torch.uint8, device=dev)
+    dW = torch.empty((N, K), dtype=torch.float32, device=dev)
+    flops = 2.0 * N * K * T
+    qbytes = (N + K) * T * (2 + 0.5 + 1 / 32)
+
+    def quant(rot, nb, rnd, seed):
+        ok(L.mx_quantize_pair(ptr(dY), T, N, ptr(X), T, K, rot, nb, rnd, seed, ptr(aq), ptr(as_),
+                              ptr(bq), ptr(bs), sp), "quantize_pair")
+
+    def gemm():
+        ok(L.mx_gemm(ptr(aq), ptr(as_), ptr(bq), ptr(bs), ptr(dW), N, K, T, sp), "gemm")
+
+    rng = np.random.default_rng(7)
+    la = np.sort(rng.choice(N, 32, replace=False))
+    lb = np.sort(rng.choice(K, 32, replace=False))
+    rows = np.sort(rng.choice(N, 16, replace=False))
+    dyf = bf16_bits_to_f32(d["dY"]).astype(np.float64)
+    xf = bf16_bits_to_f32(d["X"]).astype(np.float64)
+    exact = dyf[:, rows].T @ xf                     # rows of dY^T X, in double
+
+    def element_rms(bits, lines, rot, nb, rnd, seed, tag):
+        codes, scales = oracle.quantize(bits, oracle.CONTRACT_ROWS, rot, nb, rnd, seed, tag,
+                                        lines=lines)
+        deq = oracle.dequantize(codes, scales)
+        r = np.stack([oracle.rotate_line(bits[:, c], rot, nb, seed) for c in lines]).astype(
+            np.float64)
+        return float(np.sqrt(((deq - r) ** 2).sum() / (r ** 2).sum()))
+
+    for name, rot, nb, rnd, seed in [("none", mx.ROT_NONE, 32, mx.ROUND_RNE, 0),
+                                     ("hadamard_det_32", mx.ROT_HADAMARD_DET, 32, mx.ROUND_RNE, 0),
+                                     ("hadamard_rand_32", mx.ROT_HADAMARD_RAND, 32, mx.ROUND_RNE, 1),
+                                     ("sr", mx.ROT_NONE, 32, mx.ROUND_SR, 1)]:
+        t_q = timed(lambda: quant(rot, nb, rnd, seed))
+        quant(rot, nb, rnd, seed)
+        t_g = timed(gemm)
+        got = dW[torch.from_numpy(rows).to(dev)].double().cpu().numpy()
+        out_rms = float(np.linalg.norm(got - exact) / np.linalg.norm(exact))
+        emit({"sweep": "ablation", "workload": f"down_proj Wgrad T={T} N={N} K={K}", "mode": name,
+              "quantize_pair_ms": t_q, "gemm_ms": t_g,
+              "tflops_incl_quant": flops / ((t_q + t_g) * 1e-3) / 1e12,
+              "quantizer_gbs": qbytes / (t_q * 1e-3) / 1e9,
+              "element_rel_rms": {"dY": element_rms(d["dY"], la, rot, nb, rnd, seed, 1),
+                                  "X": element_rms(d["X"], lb, rot, nb, rnd, seed, 2),
+                                  "sample": "32 channels of each operand, full T, rotated domain"},
+              "output_rel_rms": out_rms,
+              "output_sample": "16 rows of dW (all 14336 columns) against dY^T X in double",
+              "graded": False})
+
+    for nb in (16, 32, 64, 128, 256):
+        t_q = timed(lambda: quant(mx.ROT_HADAMARD_DET, nb, mx.ROUND_RNE, 0))
+        quant(mx.ROT_HADAMARD_DET, nb, mx.ROUND_RNE, 0)
+        t_g = timed(gemm)
+        emit({"sweep": "hadamard_size", "workload": f"down_proj Wgrad T={T} N={N} K={K}",
+              "rot_block": nb, "quantize_pair_ms": t_q, "gemm_ms": t_g,
+              "quantizer_gbs": qbytes / (t_q * 1e-3) / 1e9,
+              "quantizer_frac_hbm": qbytes / (t_q * 1e-3) / 1e9 / peaks["hbm_gbs"],
+              "gemm_tflops": flops / (t_g * 1e-3) / 1e12,
+              "gemm_frac_fp4": flops / (t_g * 1e-3) / 1e12 / fp4_peak,
+              "tflops_incl_quant": flops / ((t_q + t_g) * 1e-3) / 1e12})
+
+    # cuBLAS bf16 GEMM of the same Wgrad shapes (context only, not the path)
+    for wl, (tt, nn, kk) in (("o_proj", (8192, 4096, 4096)), ("down_proj", (T, N, K))):
+        a = dY.view(torch.bfloat16)[:tt, :nn]
+        b = X.view(torch.bfloat16)[:tt, :kk]
+        t_b = timed(lambda: torch.matmul(a.t(), b))
+        emit({"sweep": "cublas_bf16_reference", "workload": f"{wl} Wgrad shape T={tt} N={nn} K={kk}",
+              "call": "torch.matmul(dY.t(), X), bf16 in and out", "ms": t_b,
+              "tflops": 2.0 * nn * kk * tt / (t_b * 1e-3) / 1e12})
+    del dY, X, aq, as_, bq, bs, dW, d
+    torch.cuda.empty_cache()
+
+    # ---- QKV + gate/up: Fprop, Dgrad and Wgrad of both weights (six GEMMs)
+    T4 = 16384
+    d4 = config_inputs("qkv_gateup", seed=0)
+    t4 = {k: torch.from_numpy(v.view(np.int16)).to(dev) for k, v in d4.items()}
+    del d4
+    total_ms, total_flops = 0.0, 0.0
+    for w, dy in (("W_qkv", "dY_qkv"), ("W_gu", "dY_gu")):
+        Wt, dYt, Xt = t4[w], t4[dy], t4["X"]
+        Nw, Kx = Wt.shape[0], Xt.shape[1]
+        for op, fn, a, b, shape, rot in (
+                ("fprop", "mx_linear_fprop", Xt, Wt, (T4, Nw), mx.ROT_NONE),
+                ("dgrad", "mx_linear_dgrad", dYt, Wt, (T4, Kx), mx.ROT_NONE),
+                ("wgrad", "mx_linear_wgrad", dYt, Xt, (Nw, Kx), mx.ROT_HADAMARD_DET)):
+            opc = {"fprop": mx.OP_FPROP, "dgrad": mx.OP_DGRAD, "wgrad": mx.OP_WGRAD}[op]
+            ws = torch.empty(max(256, mx.linear_workspace_bytes(opc, T4, Nw, Kx)),
+                             dtype=torch.uint8, device=dev)
+            out = torch.empty(shape, dtype=torch.float32, device=dev)
+            f = getattr(L, fn)
+            run = lambda: ok(f(ptr(a), ptr(b), ptr(out), T4, Nw, Kx, rot, 32, mx.ROUND_RNE, 0,
+                               ptr(ws), ws.numel(), sp), fn)
+            t_op = timed(run)
+            fl = 2.0 * T4 * Nw * Kx
+            total_ms += t_op
+            total_flops += fl
+            emit({"sweep": "qkv_gateup", "weight": w, "op": op, "call": fn,
+                  "shape": {"T": T4, "N": Nw, "K": Kx}, "ms": t_op,
+                  "tflops_incl_quant": fl / (t_op * 1e-3) / 1e12})
+            del ws, out
+    emit({"sweep": "qkv_gateup", "op": "all six", "ms": total_ms,
+          "gflop": total_flops / 1e9, "tflops_incl_quant": total_flops / (total_ms * 1e-3) / 1e12})
+    return 0
+
+
 def spot_check(d, dW, T, N, K):
     """Oracle check of 32 x 32 sampled entries of the timed dW."""
     import numpy as np
@@ -520,12 +678,18 @@ def main():
     ap.add_argument("--ref-budget-s", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-parity-check", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="print the ablation / Hadamard-size / QKV+gate-up / cuBLAS reference "
+                         "measurements instead of the headline line (one GPU)")
+    ap.add_argument("--sweep-reps", type=int, default=10)
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the dual-output encode side measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world, rank, local = dist_setup()
+    if args.sweep:
+        return run_sweep(args) if rank == 0 else 0
     if args.impl == "reference":
         return run_reference(args, world, rank)
     return run_mine(args, world, rank, local)
