@@ -413,17 +413,58 @@ __device__ __forceinline__ int64_t scale_offset(int64_t line, int64_t block, int
            (block % 4);
 }
 
-// One launch encodes up to two operands (the two Wgrad operands): tiles
-// [0, a0.num_tiles) belong to operand 0, the rest to operand 1.  For Hadamard
-// sizes up to 32 every warp works on its own 32-token slice of the tile and
-// no CTA-wide barrier is taken inside the loop: each warp marks the stage
-// consumed on an mbarrier and thread 0 refills it once all eight have.
-// Column-wise tile: TT tokens x TC channels of bf16 (32 KB).  128 x 128 gives
-// 256-byte contiguous row segments; a 256-token Hadamard needs 256 x 64.
+// Row direction of a dual encode: each thread encodes two (token, 32-channel)
+// blocks of a staged TT x TC column tile.  The four 16-byte reads of a block
+// start at a row-dependent chunk so that a warp's reads spread over all banks.
+template <int TC, bool SR>
+__device__ __forceinline__ void dual_rows(const uint32_t *tw, int64_t t0, int64_t c0,
+                                          const QuantArgs &a0, const QuantArgs &ar) {
+    const int64_t row_lines_pad = (ar.lines + 127) / 128 * 128;
+    const int64_t grid_end = (a0.lines + 127) / 128 * 128;  // channels the tiles cover
+    const int64_t kb_pad = ar.katoms * 4;                    // padded blocks per row
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int b = threadIdx.x + kThreads * h;
+        const int trow = b / (TC / 32), cb = b % (TC / 32);
+        const int64_t t = t0 + trow;
+        if (t >= row_lines_pad) continue;
+        const int64_t c = c0 + 32 * cb;
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int jj = (j + trow) & 3;
+            const uint4 v = *reinterpret_cast<const uint4 *>(tw + trow * (TC / 2) + 16 * cb + 4 * jj);
+            w[4 * jj] = v.x, w[4 * jj + 1] = v.y, w[4 * jj + 2] = v.z, w[4 * jj + 3] = v.w;
+        }
+        uint4 q;
+        const uint32_t sb =
+            encode_row_block<SR>(w, q, a0.seed, ar.sr_tag, static_cast<uint64_t>(t * ar.L + c));
+        if (t < ar.lines && c < ar.L) st_global_16(ar.codes + t * (ar.L / 2) + c / 2, q);
+        ar.scales[scale_offset(t, c / 32, ar.katoms)] = static_cast<uint8_t>(sb);
+        // Padding blocks past the last channel tile: no tile covers them.
+        if (c0 + TC == grid_end) {
+#pragma unroll
+            for (int e = 0; e < 128 / TC; ++e) {
+                const int64_t pb = grid_end / 32 + cb + e * (TC / 32);
+                if (pb < kb_pad) ar.scales[scale_offset(t, pb, ar.katoms)] = 0;
+            }
+        }
+    }
+}
+
+
+// Column-wise encode for no rotation and Hadamard sizes 16 and 32.  One
+// launch encodes up to two operands (the two Wgrad operands): tiles
+// [0, a0.num_tiles) belong to operand 0, the rest to operand 1.  Every warp
+// works on its own 32-token slice of the tile, so no CTA-wide barrier is taken
+// inside the loop: each warp marks the stage consumed on an mbarrier and
+// thread 0 refills it once all eight have.  Tile: 128 tokens x 128 channels of
+// bf16 (32 KB, 256-byte contiguous row segments).
 template <int ROTN>
 struct ColTile {
-    static constexpr int TT = ROTN == 256 ? 256 : 128;
-    static constexpr int TC = 32768 / (2 * TT);
+    static_assert(ROTN <= 32, "larger Hadamard sizes use mxq_colwise_wide_kernel");
+    static constexpr int TT = 128;
+    static constexpr int TC = 128;
     static constexpr int TOKEN_BLOCKS = TT / 32;  // warps along tokens
 };
 
@@ -434,7 +475,6 @@ template <int ROTN, bool RAND, bool SR, bool DUAL>
 __global__ void __launch_bounds__(kThreads, SR ? 1 : kColMinBlocks) mxq_colwise_kernel(
     const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
     const QuantArgs a0, const QuantArgs a1, const QuantArgs ar) {
-    constexpr bool kCtaSync = ROTN >= 64;  // cross-warp Hadamard stages need CTA barriers
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned base, kept as a shared-space pointer (offset arithmetic
     // only) so that the compiler emits shared-memory loads.
@@ -442,7 +482,6 @@ __global__ void __launch_bounds__(kThreads, SR ? 1 : kColMinBlocks) mxq_colwise_
     uint8_t *tiles = smem;                                   // kStages x 32 KB
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kTileBytes);
     uint64_t *empty = full + kStages;
-    float2 *xchg = reinterpret_cast<float2 *>(smem + kStages * kTileBytes + 1024);  // 64 KB
     __shared__ int abort_flag;
 
     using G = ColTile<ROTN>;
@@ -496,11 +535,7 @@ __global__ void __launch_bounds__(kThreads, SR ? 1 : kColMinBlocks) mxq_colwise_
         int ok = 1;
         if (lane == 0) ok = mbar_wait(&full[s], parity, a0.status, &abort_flag) ? 1 : 0;
         ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-        if (kCtaSync) {
-            if (__syncthreads_or(!ok)) break;
-        } else if (!ok) {
-            break;
-        }
+        if (!ok) break;
 
         // Column pair (64*chalf + 2*lane, +1), tokens 32*tbi .. 32*tbi+31, as
         // 32 register pairs {channel 2*lane, channel 2*lane+1}.
@@ -511,56 +546,12 @@ __global__ void __launch_bounds__(kThreads, SR ? 1 : kColMinBlocks) mxq_colwise_
             const uint32_t v = tw[(tbi * 32 + i) * (G::TC / 2) + chalf * 32 + lane];
             x[i] = pack2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
         }
-        if (DUAL) {
-            // Row direction: each thread encodes two (token, 32-channel) blocks
-            // of the tile.  The four 16-byte reads of a block start at a
-            // row-dependent chunk so that a warp's reads spread over all banks.
-            const int64_t row_lines_pad = (ar.lines + 127) / 128 * 128;
-            const int64_t grid_end = (a0.lines + 127) / 128 * 128;  // channels the tiles cover
-            const int64_t kb_pad = ar.katoms * 4;                    // padded blocks per row
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int b = threadIdx.x + kThreads * h;
-                const int trow = b / (G::TC / 32), cb = b % (G::TC / 32);
-                const int64_t t = t0 + trow;
-                if (t >= row_lines_pad) continue;
-                const int64_t c = c0 + 32 * cb;
-                uint32_t w[16];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int jj = (j + trow) & 3;
-                    const uint4 v = *reinterpret_cast<const uint4 *>(
-                        tw + trow * (G::TC / 2) + 16 * cb + 4 * jj);
-                    w[4 * jj] = v.x, w[4 * jj + 1] = v.y, w[4 * jj + 2] = v.z, w[4 * jj + 3] = v.w;
-                }
-                uint4 q;
-                const uint32_t sb = encode_row_block<SR>(w, q, a0.seed, ar.sr_tag,
-                                                         static_cast<uint64_t>(t * ar.L + c));
-                if (t < ar.lines && c < ar.L) st_global_16(ar.codes + t * (ar.L / 2) + c / 2, q);
-                ar.scales[scale_offset(t, c / 32, ar.katoms)] = static_cast<uint8_t>(sb);
-                // Padding blocks past the last channel tile: no tile covers them.
-                if (c0 + G::TC == grid_end) {
-#pragma unroll
-                    for (int e = 0; e < 128 / G::TC; ++e) {
-                        const int64_t pb = grid_end / 32 + cb + e * (G::TC / 32);
-                        if (pb < kb_pad) ar.scales[scale_offset(t, pb, ar.katoms)] = 0;
-                    }
-                }
-            }
-        }
-        if (kCtaSync) {
-            __syncthreads();  // stage s fully consumed
-            if (threadIdx.x == 0) {
-                const int nt = tile + kStages * gridDim.x;
-                if (nt < total) issue(nt, s);
-            }
-        } else {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
-            if (threadIdx.x == 0) {
-                const int nt = tile + kStages * gridDim.x;
-                if (nt < total && mbar_wait(&empty[s], parity, a0.status, &abort_flag)) issue(nt, s);
-            }
+        if (DUAL) dual_rows<G::TC, SR>(tw, t0, c0, a0, ar);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        if (threadIdx.x == 0) {
+            const int nt = tile + kStages * gridDim.x;
+            if (nt < total && mbar_wait(&empty[s], parity, a0.status, &abort_flag)) issue(nt, s);
         }
 
         if (ROTN > 0) {
@@ -572,24 +563,6 @@ __global__ void __launch_bounds__(kThreads, SR ? 1 : kColMinBlocks) mxq_colwise_
                     x[i] ^= ((bits >> i) & 1u) ? 0x8000000080000000ull : 0ull;
             }
             fwht_pairs<ROTN>(x);
-            if (ROTN >= 64) {
-                uint64_t *xw = reinterpret_cast<uint64_t *>(xchg);
-#pragma unroll
-                for (int h = 32; h < ROTN; h <<= 1) {
-                    const int m = h / 32;
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) xw[(warp * 32 + i) * 32 + lane] = x[i];
-                    __syncthreads();
-                    const int pw = warp ^ m;
-                    const bool lower = (warp & m) == 0;
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const uint64_t o = xw[(pw * 32 + i) * 32 + lane];
-                        x[i] = lower ? add2(x[i], o) : sub2(o, x[i]);
-                    }
-                    __syncthreads();
-                }
-            }
             if (SR) {  // round to nearest folds the factor into the scale multiply
                 const float cn = hadamard_norm<ROTN>();
                 const uint64_t cc = pack2(cn, cn);
@@ -624,6 +597,171 @@ __global__ void __launch_bounds__(kThreads, SR ? 1 : kColMinBlocks) mxq_colwise_
         const int64_t kb = tb / 32;
         scales[scale_offset(c, kb, katoms)] = static_cast<uint8_t>(s0);
         scales[scale_offset(c + 1, kb, katoms)] = static_cast<uint8_t>(s1);
+    }
+}
+
+// Column-wise encode for Hadamard sizes 64, 128 and 256.  Each thread owns
+// one channel x 64 consecutive tokens of the tile, held as 32 register pairs
+// {token i, token i+32}: butterfly strides 1..16 run on the pairs, stride 32
+// inside each pair, and strides 64 and 128 pair this thread with the lane that
+// holds the same channel's neighbouring 64 tokens (one warp shuffle per
+// element per stage).  The two MX blocks of the segment are the pairs' low and
+// high halves.  No shared-memory exchange and no CTA barrier is needed.
+template <int ROTN>
+struct WideTile {
+    // 128 x 128 tiles; a 256-token Hadamard block needs 256 tokens x 64 channels.
+    static constexpr int TT = ROTN == 256 ? 256 : 128;  // tokens per tile
+    static constexpr int TC = 32768 / (2 * TT);           // channels per tile
+    static constexpr int LPC = ROTN / 64;                 // lanes per channel
+    static constexpr int CPW = 32 / LPC;                  // channels per warp (ROTN > 64)
+};
+
+template <int ROTN, bool RAND, bool SR, bool DUAL>
+__global__ void __launch_bounds__(kThreads, SR ? 1 : kColMinBlocks) mxq_colwise_wide_kernel(
+    const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
+    const QuantArgs a0, const QuantArgs a1, const QuantArgs ar) {
+    static_assert(ROTN == 64 || ROTN == 128 || ROTN == 256, "sizes 64..256 only");
+    using G = WideTile<ROTN>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t *tiles = smem;                                   // kStages x 32 KB
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kTileBytes);
+    uint64_t *empty = full + kStages;
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // This thread's channel of the tile and its 64-token segment.
+    const int ch = ROTN == 64 ? (warp % 4) * 32 + lane : warp * G::CPW + lane % G::CPW;
+    const int seg = ROTN == 64 ? warp / 4 : lane / G::CPW;
+    const int total = a0.num_tiles + a1.num_tiles;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kThreads / 32);
+        }
+        abort_flag = 0;
+        fence_barrier_init();
+        prefetch_tmap(&map0);
+        if (a1.num_tiles > 0) prefetch_tmap(&map1);
+    }
+    __syncthreads();
+
+    auto issue = [&](int tile, int s) {
+        const bool second = tile >= a0.num_tiles;
+        const int lt = second ? tile - a0.num_tiles : tile;
+        const int inner = second ? a1.tiles_inner : a0.tiles_inner;
+        mbar_arrive_expect_tx(&full[s], kTileBytes);
+        tma_load_2d(tiles + s * kTileBytes, second ? &map1 : &map0, &full[s], (lt % inner) * G::TC,
+                    (lt / inner) * G::TT);
+    };
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            const int tile = blockIdx.x + s * gridDim.x;
+            if (tile < total) issue(tile, s);
+        }
+    }
+
+    for (int it = 0;; ++it) {
+        const int tile = blockIdx.x + it * gridDim.x;
+        if (tile >= total) break;
+        const int s = it % kStages;
+        const uint32_t parity = (it / kStages) & 1u;
+        const bool second = tile >= a0.num_tiles;
+        const int lt = second ? tile - a0.num_tiles : tile;
+        const int inner = second ? a1.tiles_inner : a0.tiles_inner;
+        const int64_t L = second ? a1.L : a0.L;
+        const int64_t lines = second ? a1.lines : a0.lines;
+        const int64_t katoms = second ? a1.katoms : a0.katoms;
+        uint8_t *const codes = second ? a1.codes : a0.codes;
+        uint8_t *const scales = second ? a1.scales : a0.scales;
+        const int64_t t0 = static_cast<int64_t>(lt / inner) * G::TT;
+        const int64_t c0 = static_cast<int64_t>(lt % inner) * G::TC;
+
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait(&full[s], parity, a0.status, &abort_flag) ? 1 : 0;
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (!ok) break;
+
+        uint64_t x[32];
+        const uint16_t *th = reinterpret_cast<const uint16_t *>(tiles + s * kTileBytes);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const uint32_t lo = th[(seg * 64 + i) * G::TC + ch];
+            const uint32_t hi = th[(seg * 64 + 32 + i) * G::TC + ch];
+            x[i] = pack2(__uint_as_float(lo << 16), __uint_as_float(hi << 16));
+        }
+        if (DUAL)
+            dual_rows<G::TC, SR>(reinterpret_cast<const uint32_t *>(th), t0, c0, a0, ar);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        if (threadIdx.x == 0) {
+            const int nt = tile + kStages * gridDim.x;
+            if (nt < total && mbar_wait(&empty[s], parity, a0.status, &abort_flag)) issue(nt, s);
+        }
+
+        const int64_t tb = t0 + 64 * seg;  // first token of this thread's segment
+        if (RAND) {
+            // Both 32-bit sign words of the segment come from one Philox block.
+            uint64_t o[4];
+            philox4x64_10(static_cast<uint64_t>(tb / 256), a0.seed, 0, o);
+            const uint64_t w = o[(tb % 256) / 64];
+            const uint32_t blo = static_cast<uint32_t>(w), bhi = static_cast<uint32_t>(w >> 32);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                x[i] ^= (((blo >> i) & 1u) ? 0x80000000ull : 0ull) |
+                        (((bhi >> i) & 1u) ? 0x8000000000000000ull : 0ull);
+        }
+        fwht_pairs<64>(x);  // strides 1 .. 16
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {  // stride 32: within each pair
+            float a, b;
+            unpack2(x[i], a, b);
+            x[i] = pack2(__fadd_rn(a, b), __fsub_rn(a, b));
+        }
+#pragma unroll
+        for (int m = 1; 64 * m < ROTN; m <<= 1) {  // strides 64, 128: across lanes
+            // The lower segment takes o + x, the upper one o - x = o + (-x):
+            // the same fp32 results as the canonical (a + b, a - b).
+            // (Selecting between the two results measured faster for 128,
+            // the sign flip for 256; both give identical values.)
+            const bool lower = (seg & m) == 0;
+            const uint64_t neg = lower ? 0ull : 0x8000000080000000ull;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, static_cast<unsigned long long>(x[i]),
+                                                   m * G::CPW);
+                if constexpr (ROTN == 128)
+                    x[i] = lower ? add2(x[i], o) : sub2(o, x[i]);
+                else
+                    x[i] = add2(o, x[i] ^ neg);
+            }
+        }
+
+        const int64_t c = c0 + ch;
+        uint4 q0, q1;
+        uint32_t s0, s1;
+        if (SR) {
+            const float cn = hadamard_norm<ROTN>();
+            const uint64_t cc = pack2(cn, cn);
+            float x0[32], x1[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) unpack2(mul2(x[i], cc), x0[i], x1[i]);
+            const uint64_t tag = second ? a1.sr_tag : a0.sr_tag;
+            uint32_t u[32];
+            sr_draws32(a0.seed, tag, static_cast<uint64_t>(c * L + tb), u);
+            s0 = encode_block32<true>(x0, q0, u);
+            sr_draws32(a0.seed, tag, static_cast<uint64_t>(c * L + tb + 32), u);
+            s1 = encode_block32<true>(x1, q1, u);
+        } else {
+            encode_pair_rne<true>(x, hadamard_norm<ROTN>(), q0, q1, s0, s1);
+        }
+        if (tb < L && c < lines) {
+            st_global_16(codes + c * (L / 2) + tb / 2, q0);
+            st_global_16(codes + c * (L / 2) + tb / 2 + 16, q1);
+        }
+        const int64_t kb = tb / 32;
+        scales[scale_offset(c, kb, katoms)] = static_cast<uint8_t>(s0);
+        scales[scale_offset(c, kb + 1, katoms)] = static_cast<uint8_t>(s1);
     }
 }
 
@@ -794,8 +932,21 @@ struct Operands {
 
 template <bool COLWISE, int ROTN, bool RAND>
 cudaError_t launch_rot(bool sr, const Operands &o, const DeviceInfo &dev, cudaStream_t stream) {
-    if (COLWISE) {
-        const size_t smem = kStages * kTileBytes + 1024 + (ROTN >= 64 ? 65536 : 0) + 1024;
+    if constexpr (COLWISE && ROTN >= 64) {
+        const size_t smem = kStages * kTileBytes + 1024 + 1024;
+        const int n = o.a0.num_tiles + o.a1.num_tiles;
+        if (o.dual)
+            return sr ? launch_persistent(mxq_colwise_wide_kernel<ROTN, RAND, true, true>, n, smem,
+                                          dev, stream, o.map0, o.map1, o.a0, o.a1, o.ar)
+                      : launch_persistent(mxq_colwise_wide_kernel<ROTN, RAND, false, true>, n, smem,
+                                          dev, stream, o.map0, o.map1, o.a0, o.a1, o.ar);
+        return sr ? launch_persistent(mxq_colwise_wide_kernel<ROTN, RAND, true, false>, n, smem,
+                                      dev, stream, o.map0, o.map1, o.a0, o.a1, o.ar)
+                  : launch_persistent(mxq_colwise_wide_kernel<ROTN, RAND, false, false>, n, smem,
+                                      dev, stream, o.map0, o.map1, o.a0, o.a1, o.ar);
+    }
+    else if constexpr (COLWISE) {
+        const size_t smem = kStages * kTileBytes + 1024 + 1024;
         const int n = o.a0.num_tiles + o.a1.num_tiles;
         if (o.dual)
             return sr ? launch_persistent(mxq_colwise_kernel<ROTN, RAND, true, true>, n, smem, dev,
