@@ -153,6 +153,15 @@ def reduce_max(value: float, world: int, device) -> float:
     return float(t.item())
 
 
+def job_throughput(local_total_ms: float, steps: int, units_per_step: float, world: int,
+                   device) -> tuple:
+    """Whole-job throughput of weak-scaled replicas: every rank processes
+    `steps` x `units_per_step` units; the job takes as long as its slowest
+    rank.  Returns (units per second over all ranks, max-over-ranks ms)."""
+    total_ms = reduce_max(local_total_ms, world, device)
+    return world * steps * units_per_step / (total_ms * 1e-3), total_ms
+
+
 def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
@@ -293,9 +302,9 @@ def run_mine(args, world, rank, local):
     qp = [ev[i][0].elapsed_time(ev[i][1]) for i in range(n)]
     gm = [ev[i][1].elapsed_time(ev[i][2]) for i in range(n)]
     step_ms = [a + b for a, b in zip(qp, gm)]
-    total_ms = reduce_max(sum(step_ms), world, dev)
     flops_step = 2.0 * N * K * T
-    value = world * n * flops_step / (total_ms * 1e-3) / 1e12
+    flops_per_s, total_ms = job_throughput(sum(step_ms), n, flops_step, world, dev)
+    value = flops_per_s / 1e12
 
     # ---- e2e: public call with host buffers, copies inside the timed region.
     # Every step copies its inputs host -> device, calls mx_linear_wgrad and
