@@ -56,6 +56,7 @@ struct GemmArgs {
     int k_tiles;
     int n_tiles;
     int num_tiles;
+    int c_v8;            // C rows allow 32-byte stores (N % 8 == 0, C 32-byte aligned)
     int *status;
 };
 
@@ -73,6 +74,13 @@ __device__ __forceinline__ void st_global_v4f(float *p, uint32_t a, uint32_t b, 
                                               uint32_t d) {
     asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
                  "r"(d)
+                 : "memory");
+}
+
+// One full 32-byte sector per store (the address must be 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(float *p, const uint32_t *v) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]),
+                 "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                  : "memory");
 }
 
@@ -229,6 +237,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t col0 = static_cast<int64_t>(nb) * kBN + 128 * half;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
+                    if (g.c_v8 && col0 + 32 * c + 31 < g.N) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) st_global_v8(crow + col0 + 32 * c + 8 * j, &v[c][8 * j]);
+                        continue;
+                    }
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const int64_t col = col0 + 32 * c + 4 * j;
@@ -284,6 +297,7 @@ cudaError_t launch_gemm(const void *Aq, const void *As, const void *Bq, const vo
     if (m_tiles * n_tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
     g.n_tiles = static_cast<int>(n_tiles);
     g.num_tiles = static_cast<int>(m_tiles * n_tiles);
+    g.c_v8 = (N % 8 == 0 && (reinterpret_cast<uintptr_t>(C) & 31) == 0) ? 1 : 0;
     g.status = dev.status;
     cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kGemmSmem));
