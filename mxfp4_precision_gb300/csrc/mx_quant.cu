@@ -41,7 +41,8 @@ constexpr int kStages = MXQ_STAGES;  // TMA ring depth per CTA
 // the round-to-nearest colwise kernels are held to 128 registers so that the
 // random-sign variants do not fall to one CTA per SM.
 constexpr int kColMinBlocks = 2;
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;           // compute threads (8 warps)
+constexpr int kColProducerThreads = kThreads + 32;  // + a TMA producer warp
 constexpr uint32_t kTileBytes = 32768;  // 256 x 64 bf16 (colwise) / 64 x 256 bf16 (rowwise)
 constexpr uint32_t kScaleStage = 512;   // two half-atoms of scales per tile
 
@@ -471,8 +472,13 @@ struct ColTile {
 // With DUAL, the launch has one source operand (a0) and also writes its
 // row-direction encoding (blocks of 32 along the channels, no rotation) to
 // `ar`, from the same staged tiles: one HBM read serves both encodings.
+// Without DUAL, a ninth warp is the TMA producer: it refills each stage once
+// all eight compute warps have released it, so no compute warp waits for the
+// slowest one.  (The dual variant keeps its registers for the row encode and
+// refills from thread 0 instead.)
 template <int ROTN, bool RAND, bool SR, bool DUAL>
-__global__ void __launch_bounds__(kThreads, SR ? 1 : kColMinBlocks) mxq_colwise_kernel(
+__global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads, SR ? 1 : kColMinBlocks)
+    mxq_colwise_kernel(
     const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
     const QuantArgs a0, const QuantArgs a1, const QuantArgs ar) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -509,11 +515,28 @@ __global__ void __launch_bounds__(kThreads, SR ? 1 : kColMinBlocks) mxq_colwise_
         tma_load_2d(tiles + s * kTileBytes, second ? &map1 : &map0, &full[s], (lt % inner) * G::TC,
                     (lt / inner) * G::TT);
     };
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            const int tile = blockIdx.x + s * gridDim.x;
-            if (tile < total) issue(tile, s);
+    if (DUAL) {
+        if (threadIdx.x == 0) {
+            for (int s = 0; s < kStages; ++s) {
+                const int tile = blockIdx.x + s * gridDim.x;
+                if (tile < total) issue(tile, s);
+            }
         }
+    } else if (warp == kThreads / 32) {
+        // ---- producer warp: stage s of iteration it is refilled once the
+        // compute warps have released its previous use (iteration it - kStages).
+        if (lane == 0) {
+            for (int it = 0;; ++it) {
+                const int tile = blockIdx.x + it * gridDim.x;
+                if (tile >= total) break;
+                const int s = it % kStages;
+                if (it >= kStages &&
+                    !mbar_wait(&empty[s], ((it / kStages) - 1) & 1u, a0.status, &abort_flag))
+                    break;
+                issue(tile, s);
+            }
+        }
+        return;
     }
 
     for (int it = 0;; ++it) {
@@ -549,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, SR ? 1 : kColMinBlocks) mxq_colwise_
         if (DUAL) dual_rows<G::TC, SR>(tw, t0, c0, a0, ar);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
-        if (threadIdx.x == 0) {
+        if (DUAL && threadIdx.x == 0) {
             const int nt = tile + kStages * gridDim.x;
             if (nt < total && mbar_wait(&empty[s], parity, a0.status, &abort_flag)) issue(nt, s);
         }
@@ -909,18 +932,24 @@ __global__ void __launch_bounds__(kThreads) mxq_rowwise_kernel(const __grid_cons
 
 // ---------------------------------------------------------------- dispatch
 template <typename Kern, typename... Args>
-cudaError_t launch_persistent(Kern kernel, int num_tiles, size_t smem, const DeviceInfo &dev,
-                              cudaStream_t stream, Args... args) {
+cudaError_t launch_persistent_n(Kern kernel, int threads, int num_tiles, size_t smem,
+                                const DeviceInfo &dev, cudaStream_t stream, Args... args) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
     const int grid = num_tiles < dev.sm_count * per_sm ? num_tiles : dev.sm_count * per_sm;
-    kernel<<<grid, kThreads, smem, stream>>>(args...);
+    kernel<<<grid, threads, smem, stream>>>(args...);
     return cudaGetLastError();
+}
+
+template <typename Kern, typename... Args>
+cudaError_t launch_persistent(Kern kernel, int num_tiles, size_t smem, const DeviceInfo &dev,
+                              cudaStream_t stream, Args... args) {
+    return launch_persistent_n(kernel, kThreads, num_tiles, smem, dev, stream, args...);
 }
 
 struct Operands {
@@ -953,10 +982,12 @@ cudaError_t launch_rot(bool sr, const Operands &o, const DeviceInfo &dev, cudaSt
                                           stream, o.map0, o.map1, o.a0, o.a1, o.ar)
                       : launch_persistent(mxq_colwise_kernel<ROTN, RAND, false, true>, n, smem,
                                           dev, stream, o.map0, o.map1, o.a0, o.a1, o.ar);
-        return sr ? launch_persistent(mxq_colwise_kernel<ROTN, RAND, true, false>, n, smem, dev,
-                                      stream, o.map0, o.map1, o.a0, o.a1, o.ar)
-                  : launch_persistent(mxq_colwise_kernel<ROTN, RAND, false, false>, n, smem, dev,
-                                      stream, o.map0, o.map1, o.a0, o.a1, o.ar);
+        return sr ? launch_persistent_n(mxq_colwise_kernel<ROTN, RAND, true, false>,
+                                        kColProducerThreads, n, smem, dev, stream, o.map0, o.map1,
+                                        o.a0, o.a1, o.ar)
+                  : launch_persistent_n(mxq_colwise_kernel<ROTN, RAND, false, false>,
+                                        kColProducerThreads, n, smem, dev, stream, o.map0, o.map1,
+                                        o.a0, o.a1, o.ar);
     }
     const size_t smem = kStages * kTileBytes + 1024 + 1024;
     return sr ? launch_persistent(mxq_rowwise_kernel<ROTN, RAND, true>, o.a0.num_tiles, smem, dev,
