@@ -100,6 +100,17 @@ size_t mx_codes_bytes(int64_t mn, int64_t k);
 size_t mx_scales_bytes(int64_t mn, int64_t k);
 
 /*
+ * mx_scales_to_canonical -- copy a tiled scale array (the layout above, as
+ * written by mx_quantize) into plain row-major bytes d_canon[lines][k/32]
+ * (scale of line r, block b at r*(k/32) + b), dropping the padding.  For
+ * tests and for handing scales to code that expects the canonical order.
+ * k % 32 == 0; lines == 0 or k == 0: MX_OK, nothing launched.  Asynchronous
+ * on `stream`; both buffers are device memory owned by the caller.
+ */
+mx_status mx_scales_to_canonical(const void *d_scales, int64_t lines, int64_t k, void *d_canon,
+                                 void *stream);
+
+/*
  * mx_quantize -- rotate and MXFP4-encode a bf16 matrix d_src[rows][cols].
  *   contract   MX_CONTRACT_ROWS: lines = columns, k = rows (needs cols % 8 == 0)
  *              MX_CONTRACT_COLS: lines = rows,    k = cols

@@ -11,7 +11,8 @@ from ._binding import (CONTRACT_COLS, CONTRACT_ROWS, OP_DGRAD, OP_FPROP, OP_WGRA
                        codes_bytes, debug_timeout_probe, gemm, gemm_into, lib, library_path,
                        linear_dgrad, linear_fprop, linear_wgrad, linear_wgrad_noalloc,
                        linear_workspace_bytes, NOALLOC_SCRATCH_BYTES, quantize, quantize_dual,
-                       quantize_pair, quantize_into, scales_bytes, status_string)
+                       quantize_pair, quantize_into, scales_bytes, scales_to_canonical,
+                       status_string)
 
 __all__ = [
     "CONTRACT_COLS", "CONTRACT_ROWS", "OP_DGRAD", "OP_FPROP", "OP_WGRAD", "ROT_HADAMARD_DET",
@@ -19,5 +20,5 @@ __all__ = [
     "codes_bytes", "debug_timeout_probe", "gemm", "gemm_into", "lib", "library_path",
     "linear_dgrad", "linear_fprop", "linear_wgrad", "linear_wgrad_noalloc", "linear_workspace_bytes",
     "NOALLOC_SCRATCH_BYTES", "quantize", "quantize_dual", "quantize_pair",
-    "quantize_into", "scales_bytes", "status_string",
+    "quantize_into", "scales_bytes", "scales_to_canonical", "status_string",
 ]

@@ -21,7 +21,7 @@ CONTRACT_ROWS, CONTRACT_COLS = 0, 1
 OP_FPROP, OP_DGRAD, OP_WGRAD = 0, 1, 2
 
 EXPORTED = [
-    "mx_codes_bytes", "mx_scales_bytes", "mx_quantize", "mx_quantize_pair", "mx_quantize_dual",
+    "mx_codes_bytes", "mx_scales_bytes", "mx_scales_to_canonical", "mx_quantize", "mx_quantize_pair", "mx_quantize_dual",
     "mx_gemm", "mx_linear_workspace_bytes",
     "mx_linear_wgrad", "mx_linear_fprop", "mx_linear_dgrad", "mx_linear_wgrad_noalloc",
     "mx_check_status",
@@ -65,6 +65,8 @@ def lib() -> ctypes.CDLL:
             L.mx_quantize_pair.restype = i32
             L.mx_quantize_dual.argtypes = [P, i64, i64, i32, i32, i32, u64, P, P, P, P, P]
             L.mx_quantize_dual.restype = i32
+            L.mx_scales_to_canonical.argtypes = [P, i64, i64, P, P]
+            L.mx_scales_to_canonical.restype = i32
             L.mx_gemm.argtypes = [P, P, P, P, P, i64, i64, i64, P]
             L.mx_gemm.restype = i32
             L.mx_linear_workspace_bytes.argtypes = [i32, i64, i64, i64]
@@ -188,6 +190,15 @@ def quantize_dual(src: torch.Tensor, rot: int = ROT_HADAMARD_DET, rot_block: int
                                 _stream(stream))
     _check(st, "mx_quantize_dual")
     return (codes_t, scales_t), (codes_n, scales_n)
+
+
+def scales_to_canonical(scales: torch.Tensor, lines: int, k: int, stream=None) -> torch.Tensor:
+    """Tiled scales -> canonical uint8 [lines, k/32] on the same device."""
+    out = torch.empty((lines, k // 32), dtype=torch.uint8, device=scales.device)
+    st = lib().mx_scales_to_canonical(_dev_ptr(scales, "scales"), lines, k, _dev_ptr(out, "canon"),
+                                      _stream(stream))
+    _check(st, "mx_scales_to_canonical")
+    return out
 
 
 def gemm_into(Aq, As, Bq, Bs, C: torch.Tensor, M: int, N: int, K: int, stream=None) -> None:

@@ -306,6 +306,19 @@ mx_status mx_quantize_dual(const void *d_src, int64_t T, int64_t N, int rot, int
                               d_codes_n, d_scales_n, static_cast<cudaStream_t>(stream));
 }
 
+mx_status mx_scales_to_canonical(const void *d_scales, int64_t lines, int64_t k, void *d_canon,
+                                 void *stream) {
+    if (lines < 0 || k < 0) return MX_ERR_SHAPE;
+    if (k % 32 != 0) return MX_ERR_SHAPE;
+    if (lines == 0 || k == 0) return MX_OK;
+    if (d_scales == nullptr || d_canon == nullptr) return MX_ERR_INVALID_ARG;
+    const DeviceInfo *dev = nullptr;
+    mx_status st = device_or_error(&dev);
+    if (st != MX_OK) return st;
+    return from_cuda(launch_scales_to_canonical(d_scales, lines, k, d_canon, *dev,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
 mx_status mx_gemm(const void *d_Aq, const void *d_As, const void *d_Bq, const void *d_Bs,
                   float *d_C, int64_t M, int64_t N, int64_t K, void *stream) {
     return gemm_impl(d_Aq, d_As, d_Bq, d_Bs, d_C, M, N, K, static_cast<cudaStream_t>(stream));

@@ -42,6 +42,9 @@ cudaError_t launch_quantize_pair_colwise(const void *src0, int64_t rows0, int64_
 // One read of src [rows, cols] writes its column-direction encoding (blocks
 // along rows, rotated) and its row-direction encoding (blocks along cols,
 // no rotation).
+// tiled scales [mx_scales_bytes(lines, k)] -> canonical [lines][k/32].
+cudaError_t launch_scales_to_canonical(const void *tiled, int64_t lines, int64_t k, void *canon,
+                                       const DeviceInfo &dev, cudaStream_t stream);
 cudaError_t launch_quantize_dual(const void *src, int64_t rows, int64_t cols, int rot,
                                  int rot_block, int rnd, uint64_t seed, void *codes_t,
                                  void *scales_t, void *codes_n, void *scales_n,

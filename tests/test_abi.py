@@ -113,6 +113,14 @@ def test_quantize_dual_rejects_bad_arguments_before_launch(L):
     assert _qd(L, T=0) == 0 and _qd(L, N=0) == 0   # empty: nothing to do
 
 
+def test_scales_to_canonical_rejects_bad_arguments_before_launch(L):
+    f = lambda sc=0x1000, lines=128, k=256, out=0x2000: L.mx_scales_to_canonical(sc, lines, k, out,
+                                                                               None)
+    assert f(k=100) == 2 and f(lines=-1) == 2
+    assert f(sc=0) == 1 and f(out=0) == 1
+    assert f(lines=0) == 0 and f(k=0) == 0
+
+
 def test_gemm_rejects_bad_arguments_before_launch(L):
     g = lambda **k: L.mx_gemm(V(k.get("a", 0x1000)), V(0x2000), V(0x3000), V(0x4000),
                               V(k.get("c", 0x5000)), k.get("M", 128), k.get("N", 256),

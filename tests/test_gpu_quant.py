@@ -196,3 +196,22 @@ def test_dual_edge_cases():
 def test_dual_tiny_config_dy():
     d = config_inputs("tiny", seed=0, only=("dY",))
     _dual_check(d["dY"], mx.ROT_HADAMARD_DET, 32, mx.ROUND_RNE, 0)
+
+
+@pytest.mark.parametrize("lines,k", [(128, 256), (200, 800), (4096, 8192), (7, 32)])
+def test_scales_to_canonical_matches_the_documented_layout(lines, k):
+    MP, KB = 128 * ((lines + 127) // 128), 8 * ((k + 255) // 256)
+    tiled = np.random.default_rng(lines + k).integers(0, 256, MP * KB, dtype=np.uint8)
+    got = mx.scales_to_canonical(torch.from_numpy(tiled).cuda(), lines, k)
+    mx.check_status()
+    assert np.array_equal(got.cpu().numpy(), untile_scales(tiled, lines, k))
+
+
+def test_scales_to_canonical_of_an_encode_equals_the_oracle_scales():
+    bits = _rand_bits((800, 136), 17)
+    codes, scales = mx.quantize(torch.from_numpy(bits.view(np.int16)).cuda(), mx.CONTRACT_ROWS,
+                                mx.ROT_HADAMARD_DET, 32)
+    got = mx.scales_to_canonical(scales, 136, 800)
+    mx.check_status()
+    _, os_ = oracle.quantize(bits, oracle.CONTRACT_ROWS, oracle.ROT_HADAMARD_DET, 32)
+    assert np.array_equal(got.cpu().numpy(), os_)
