@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD_DIR, "libmx.so")
-SOURCES = ["mx_api.cu", "mx_quant.cu", "mx_gemm.cu", "mx_noalloc.cu"]
+SOURCES = ["mx_api.cu", "mx_quant.cu", "mx_gemm.cu", "mx_noalloc.cu", "mx_scales.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--expt-relaxed-constexpr", "-I", INCLUDE]

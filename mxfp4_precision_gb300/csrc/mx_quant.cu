@@ -414,16 +414,6 @@ __device__ __forceinline__ int64_t scale_offset(int64_t line, int64_t block, int
            (block % 4);
 }
 
-// Canonical [lines][k/32] copy of a tiled scale array (a test and interchange
-// helper: one byte per thread, grid-stride).
-__global__ void mx_scales_canon_kernel(const uint8_t *__restrict__ tiled, uint8_t *__restrict__ canon,
-                                       int64_t lines, int64_t blocks, int64_t katoms) {
-    const int64_t n = lines * blocks;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-        canon[i] = tiled[scale_offset(i / blocks, i % blocks, katoms)];
-}
-
 // Row direction of a dual encode: each thread encodes two (token, 32-channel)
 // blocks of a staged TT x TC column tile.  The four 16-byte reads of a block
 // start at a row-dependent chunk so that a warp's reads spread over all banks.
@@ -1118,17 +1108,6 @@ cudaError_t launch_quantize_dual(const void *src, int64_t rows, int64_t cols, in
     o.ar.status = dev.status;
     o.dual = true;
     return launch_dir<true>(rot, rot_block, rnd == 1, o, dev, stream);
-}
-
-cudaError_t launch_scales_to_canonical(const void *tiled, int64_t lines, int64_t k, void *canon,
-                                       const DeviceInfo &dev, cudaStream_t stream) {
-    const int64_t blocks = k / 32, n = lines * blocks;
-    const int64_t want = (n + 255) / 256;
-    const int grid = static_cast<int>(want < 4 * dev.sm_count ? want : 4 * dev.sm_count);
-    mx_scales_canon_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint8_t *>(tiled),
-                                                     static_cast<uint8_t *>(canon), lines, blocks,
-                                                     scale_katoms(k));
-    return cudaGetLastError();
 }
 
 }  // namespace mx
