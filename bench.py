@@ -168,6 +168,23 @@ def barrier(world: int):
         dist.barrier()
 
 
+# Rotation / rounding of the measured step (set from the command line in main).
+ROT_NAMES = {"none": 0, "hadamard_det": 1, "hadamard_rand": 2}
+ROUND_NAMES = {"rne": 0, "sr": 1}
+MODE = {"rot": "hadamard_det", "rot_block": 32, "round": "rne", "seed": 0}
+
+
+def mode_args():
+    """(rot, rot_block, rnd, seed) as the C ABI and the oracle take them."""
+    return (ROT_NAMES[MODE["rot"]], MODE["rot_block"], ROUND_NAMES[MODE["round"]], MODE["seed"])
+
+
+def mode_text():
+    rot = {"none": "no rotation", "hadamard_det": f"deterministic Hadamard {MODE['rot_block']}",
+           "hadamard_rand": f"random-sign Hadamard {MODE['rot_block']}"}[MODE["rot"]]
+    return f"{rot} along T, {MODE['round'].upper()}, seed {MODE['seed']}"
+
+
 def oracle_sample(d, T, N, K, s_lines, seed=0):
     """One bounded oracle sample: encode s_lines lines of each operand over the
     full T and contract them (s_lines^2 outputs).  Returns (seconds, flops)."""
@@ -177,10 +194,9 @@ def oracle_sample(d, T, N, K, s_lines, seed=0):
     la = np.sort(rng.choice(N, s_lines, replace=False))
     lb = np.sort(rng.choice(K, s_lines, replace=False))
     t0 = time.perf_counter()
-    Aq, As = oracle.quantize(d["dY"], oracle.CONTRACT_ROWS, oracle.ROT_HADAMARD_DET, 32,
-                             oracle.ROUND_RNE, 0, 1, lines=la)
-    Bq, Bs = oracle.quantize(d["X"], oracle.CONTRACT_ROWS, oracle.ROT_HADAMARD_DET, 32,
-                             oracle.ROUND_RNE, 0, 2, lines=lb)
+    rot, nb, rnd, qseed = mode_args()
+    Aq, As = oracle.quantize(d["dY"], oracle.CONTRACT_ROWS, rot, nb, rnd, qseed, 1, lines=la)
+    Bq, Bs = oracle.quantize(d["X"], oracle.CONTRACT_ROWS, rot, nb, rnd, qseed, 2, lines=lb)
     oracle.gemm(Aq, As, Bq, Bs)
     return time.perf_counter() - t0, 2.0 * s_lines * s_lines * T
 
@@ -212,7 +228,7 @@ def run_reference(args, world, rank):
     tot = sum(times)
     value = flops / tot / 1e12
     sample = (f"per step: {s} lines of dY and {s} lines of X (full T={T}) encoded with "
-              f"det-Hadamard-32 + RNE, then their {s}x{s} block of dW contracted in double")
+              f"{mode_text()}, then their {s}x{s} block of dW contracted in double")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True,
@@ -229,8 +245,9 @@ def run_reference(args, world, rank):
 
 def workload_config(args, T, N, K):
     return {"workload": f"{args.workload} Wgrad: dY [{T},{N}] x X [{T},{K}] -> dW [{N},{K}] fp32, "
-                        f"deterministic Hadamard 32 along T, MXFP4 block 32, RNE",
-            "T": T, "N": N, "K": K, "rot": "hadamard_det", "rot_block": 32, "round": "rne",
+                        f"{mode_text()}, MXFP4 block 32",
+            "T": T, "N": N, "K": K, "rot": MODE["rot"], "rot_block": MODE["rot_block"],
+            "round": MODE["round"], "seed": MODE["seed"],
             "l2": "flushed before every timed step (512 MB write, outside the events)",
             "parallelism": "replicas" if args.gpus > 1 else "single-gpu"}
 
@@ -256,7 +273,7 @@ def run_mine(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     L = mx.lib()
     sp = stream.cuda_stream
-    rot, nb, rnd, seed = mx.ROT_HADAMARD_DET, 32, mx.ROUND_RNE, 0
+    rot, nb, rnd, seed = mode_args()
 
     aq = torch.empty(mx.codes_bytes(N, T), dtype=torch.uint8, device=dev)
     as_ = torch.empty(mx.scales_bytes(N, T), dtype=torch.uint8, device=dev)
@@ -419,7 +436,7 @@ def run_mine(args, world, rank, local):
         dt, f = oracle_sample(d, T, N, K, s)
         cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
                "sample": f"{s} lines of dY and {s} lines of X (full T={T}) encoded "
-                         f"(det-Hadamard-32, RNE), then their {s}x{s} block of dW contracted "
+                         f"({mode_text()}), then their {s}x{s} block of dW contracted "
                          f"in double; {dt:.1f} s single-threaded"}
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": n, "warmup": args.warmup, "ms_per_step": total_ms / n,
@@ -665,10 +682,9 @@ def spot_check(d, dW, T, N, K):
     rng = np.random.default_rng(123)
     ia = np.sort(rng.choice(N, 32, replace=False))
     jb = np.sort(rng.choice(K, 32, replace=False))
-    Aq, As = oracle.quantize(d["dY"], oracle.CONTRACT_ROWS, oracle.ROT_HADAMARD_DET, 32,
-                             oracle.ROUND_RNE, 0, 1, lines=ia)
-    Bq, Bs = oracle.quantize(d["X"], oracle.CONTRACT_ROWS, oracle.ROT_HADAMARD_DET, 32,
-                             oracle.ROUND_RNE, 0, 2, lines=jb)
+    rot, nb, rnd, qseed = mode_args()
+    Aq, As = oracle.quantize(d["dY"], oracle.CONTRACT_ROWS, rot, nb, rnd, qseed, 1, lines=ia)
+    Bq, Bs = oracle.quantize(d["X"], oracle.CONTRACT_ROWS, rot, nb, rnd, qseed, 2, lines=jb)
     C, Ca = oracle.gemm(Aq, As, Bq, Bs)
     got = dW.cpu().numpy()[np.ix_(ia, jb)].astype(np.float64)
     ratio = float((np.abs(got - C) / np.maximum(Ca, 1e-300)).max())
@@ -687,6 +703,11 @@ def main():
     ap.add_argument("--ref-budget-s", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-parity-check", action="store_true")
+    ap.add_argument("--rot", choices=sorted(ROT_NAMES), default="hadamard_det",
+                    help="rotation of both operands along T (default: deterministic Hadamard)")
+    ap.add_argument("--rot-block", type=int, choices=[16, 32, 64, 128, 256], default=32)
+    ap.add_argument("--round", choices=sorted(ROUND_NAMES), default="rne")
+    ap.add_argument("--seed", type=int, default=0, help="sign / SR seed")
     ap.add_argument("--sweep", action="store_true",
                     help="print the ablation / Hadamard-size / QKV+gate-up / cuBLAS reference "
                          "measurements instead of the headline line (one GPU)")
@@ -694,6 +715,7 @@ def main():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the dual-output encode side measurement")
     args = ap.parse_args()
+    MODE.update(rot=args.rot, rot_block=args.rot_block, round=args.round, seed=args.seed)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world, rank, local = dist_setup()

@@ -54,7 +54,9 @@ typedef enum {
     MX_ERR_WORKSPACE = 4,   /* workspace smaller than mx_linear_workspace_bytes() */
     MX_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed */
     MX_ERR_TIMEOUT = 6,     /* a device-side bounded wait expired (see mx_check_status) */
-    MX_ERR_UNSUPPORTED = 7  /* the current device is not sm_103 / sm_100 family */
+    MX_ERR_UNSUPPORTED = 7, /* the current device is not sm_103 / sm_100 family */
+    MX_ERR_BOUNDS = 8       /* bounds-checked build only (MX_CHECKED=1): a kernel store fell
+                               outside its buffer and was skipped (see mx_check_status) */
 } mx_status;
 
 typedef enum {

@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/mx.h"
+#include <nvtx3/nvToolsExt.h>
 #include "mx_internal.h"
 #include "mx_ptx.cuh"
 
@@ -271,6 +272,16 @@ mx_status linear_impl(int op, const void *a_src, int64_t a_rows, int64_t a_cols,
 }
 }  // namespace
 
+namespace {
+// Names each exported call in profiler timelines (NVTX; free without a tool attached).
+struct TraceRange {
+    explicit TraceRange(const char *name) { nvtxRangePushA(name); }
+    ~TraceRange() { nvtxRangePop(); }
+    TraceRange(const TraceRange &) = delete;
+    TraceRange &operator=(const TraceRange &) = delete;
+};
+}  // namespace
+
 extern "C" {
 
 size_t mx_codes_bytes(int64_t mn, int64_t k) {
@@ -286,6 +297,7 @@ size_t mx_scales_bytes(int64_t mn, int64_t k) {
 mx_status mx_quantize(const void *d_src, int64_t rows, int64_t cols, int contract, int rot,
                       int rot_block, int rnd, uint64_t seed, void *d_codes, void *d_scales,
                       void *stream) {
+    TraceRange trace("mx_quantize");
     return quantize_impl(d_src, rows, cols, contract, rot, rot_block, rnd, seed, 1, d_codes,
                          d_scales, static_cast<cudaStream_t>(stream));
 }
@@ -294,6 +306,7 @@ mx_status mx_quantize_pair(const void *d_src0, int64_t rows0, int64_t cols0, con
                            int64_t rows1, int64_t cols1, int rot, int rot_block, int rnd,
                            uint64_t seed, void *d_codes0, void *d_scales0, void *d_codes1,
                            void *d_scales1, void *stream) {
+    TraceRange trace("mx_quantize_pair");
     return quantize_pair_impl(d_src0, rows0, cols0, d_src1, rows1, cols1, rot, rot_block, rnd, seed,
                               d_codes0, d_scales0, d_codes1, d_scales1,
                               static_cast<cudaStream_t>(stream));
@@ -302,12 +315,14 @@ mx_status mx_quantize_pair(const void *d_src0, int64_t rows0, int64_t cols0, con
 mx_status mx_quantize_dual(const void *d_src, int64_t T, int64_t N, int rot, int rot_block,
                            int rnd, uint64_t seed, void *d_codes_t, void *d_scales_t,
                            void *d_codes_n, void *d_scales_n, void *stream) {
+    TraceRange trace("mx_quantize_dual");
     return quantize_dual_impl(d_src, T, N, rot, rot_block, rnd, seed, d_codes_t, d_scales_t,
                               d_codes_n, d_scales_n, static_cast<cudaStream_t>(stream));
 }
 
 mx_status mx_scales_to_canonical(const void *d_scales, int64_t lines, int64_t k, void *d_canon,
                                  void *stream) {
+    TraceRange trace("mx_scales_to_canonical");
     if (lines < 0 || k < 0) return MX_ERR_SHAPE;
     if (k % 32 != 0) return MX_ERR_SHAPE;
     if (lines == 0 || k == 0) return MX_OK;
@@ -321,6 +336,7 @@ mx_status mx_scales_to_canonical(const void *d_scales, int64_t lines, int64_t k,
 
 mx_status mx_gemm(const void *d_Aq, const void *d_As, const void *d_Bq, const void *d_Bs,
                   float *d_C, int64_t M, int64_t N, int64_t K, void *stream) {
+    TraceRange trace("mx_gemm");
     return gemm_impl(d_Aq, d_As, d_Bq, d_Bs, d_C, M, N, K, static_cast<cudaStream_t>(stream));
 }
 
@@ -334,6 +350,7 @@ size_t mx_linear_workspace_bytes(int op, int64_t T, int64_t N, int64_t K) {
 mx_status mx_linear_wgrad(const void *d_dY, const void *d_X, float *d_dW, int64_t T, int64_t N,
                           int64_t K, int rot, int rot_block, int rnd, uint64_t seed, void *d_ws,
                           size_t ws_bytes, void *stream) {
+    TraceRange trace("mx_linear_wgrad");
     // dW[N][K] = dY^T X: both operands encoded down their rows (contraction T).
     return linear_impl(MX_OP_WGRAD, d_dY, T, N, MX_CONTRACT_ROWS, d_X, T, K, MX_CONTRACT_ROWS,
                        d_dW, T, N, K, rot, rot_block, rnd, seed, d_ws, ws_bytes,
@@ -343,6 +360,7 @@ mx_status mx_linear_wgrad(const void *d_dY, const void *d_X, float *d_dW, int64_
 mx_status mx_linear_fprop(const void *d_X, const void *d_W, float *d_Y, int64_t T, int64_t N,
                           int64_t K, int rot, int rot_block, int rnd, uint64_t seed, void *d_ws,
                           size_t ws_bytes, void *stream) {
+    TraceRange trace("mx_linear_fprop");
     // Y[T][N] = X W^T: X[T][K] and W[N][K] encoded along their rows (contraction K).
     return linear_impl(MX_OP_FPROP, d_X, T, K, MX_CONTRACT_COLS, d_W, N, K, MX_CONTRACT_COLS, d_Y,
                        T, N, K, rot, rot_block, rnd, seed, d_ws, ws_bytes,
@@ -352,6 +370,7 @@ mx_status mx_linear_fprop(const void *d_X, const void *d_W, float *d_Y, int64_t 
 mx_status mx_linear_dgrad(const void *d_dY, const void *d_W, float *d_dX, int64_t T, int64_t N,
                           int64_t K, int rot, int rot_block, int rnd, uint64_t seed, void *d_ws,
                           size_t ws_bytes, void *stream) {
+    TraceRange trace("mx_linear_dgrad");
     // dX[T][K] = dY W: dY[T][N] along its rows, W[N][K] down its rows (contraction N).
     return linear_impl(MX_OP_DGRAD, d_dY, T, N, MX_CONTRACT_COLS, d_W, N, K, MX_CONTRACT_ROWS,
                        d_dX, T, N, K, rot, rot_block, rnd, seed, d_ws, ws_bytes,
@@ -359,6 +378,7 @@ mx_status mx_linear_dgrad(const void *d_dY, const void *d_W, float *d_dX, int64_
 }
 
 mx_status mx_check_status(void *stream) {
+    TraceRange trace("mx_check_status");
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return MX_ERR_CUDA;
     const DeviceInfo *dev = nullptr;
@@ -371,12 +391,13 @@ mx_status mx_check_status(void *stream) {
         const int zero = 0;
         if (cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
             return MX_ERR_CUDA;
-        return v == kDevTimeout ? MX_ERR_TIMEOUT : MX_ERR_CUDA;
+        return v == kDevTimeout ? MX_ERR_TIMEOUT : v == kDevBounds ? MX_ERR_BOUNDS : MX_ERR_CUDA;
     }
     return MX_OK;
 }
 
 mx_status mx_debug_timeout_probe(int64_t limit_us, void *stream) {
+    TraceRange trace("mx_debug_timeout_probe");
     if (limit_us <= 0 || limit_us > 10 * 1000 * 1000) return MX_ERR_INVALID_ARG;
     const DeviceInfo *dev = nullptr;
     mx_status st = device_or_error(&dev);
@@ -396,6 +417,7 @@ const char *mx_status_string(int status) {
         case MX_ERR_CUDA: return "MX_ERR_CUDA";
         case MX_ERR_TIMEOUT: return "MX_ERR_TIMEOUT";
         case MX_ERR_UNSUPPORTED: return "MX_ERR_UNSUPPORTED";
+        case MX_ERR_BOUNDS: return "MX_ERR_BOUNDS";
         default: return "MX_ERR_UNKNOWN";
     }
 }

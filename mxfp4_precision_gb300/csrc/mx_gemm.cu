@@ -57,6 +57,7 @@ struct GemmArgs {
     int n_tiles;
     int num_tiles;
     int c_v8;            // C rows allow 32-byte stores (N % 8 == 0, C 32-byte aligned)
+    size_t c_bytes;      // extent of C (store guards)
     int *status;
 };
 
@@ -239,19 +240,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 4; ++c) {
                     if (g.c_v8 && col0 + 32 * c + 31 < g.N) {
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) st_global_v8(crow + col0 + 32 * c + 8 * j, &v[c][8 * j]);
+                        for (int j = 0; j < 4; ++j)
+                            if (MX_STORE_OK(crow + col0 + 32 * c + 8 * j, 32, g.C, g.c_bytes, g.status))
+                                st_global_v8(crow + col0 + 32 * c + 8 * j, &v[c][8 * j]);
                         continue;
                     }
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const int64_t col = col0 + 32 * c + 4 * j;
                         if (col + 3 < g.N) {
-                            st_global_v4f(crow + col, v[c][4 * j], v[c][4 * j + 1],
-                                          v[c][4 * j + 2], v[c][4 * j + 3]);
+                            if (MX_STORE_OK(crow + col, 16, g.C, g.c_bytes, g.status))
+                                st_global_v4f(crow + col, v[c][4 * j], v[c][4 * j + 1],
+                                              v[c][4 * j + 2], v[c][4 * j + 3]);
                         } else {
 #pragma unroll
                             for (int e = 0; e < 4; ++e)
-                                if (col + e < g.N) crow[col + e] = __uint_as_float(v[c][4 * j + e]);
+                                if (col + e < g.N &&
+                                    MX_STORE_OK(crow + col + e, 4, g.C, g.c_bytes, g.status))
+                                    crow[col + e] = __uint_as_float(v[c][4 * j + e]);
                         }
                     }
                 }
@@ -298,6 +304,7 @@ cudaError_t launch_gemm(const void *Aq, const void *As, const void *Bq, const vo
     g.n_tiles = static_cast<int>(n_tiles);
     g.num_tiles = static_cast<int>(m_tiles * n_tiles);
     g.c_v8 = (N % 8 == 0 && (reinterpret_cast<uintptr_t>(C) & 31) == 0) ? 1 : 0;
+    g.c_bytes = static_cast<size_t>(M) * static_cast<size_t>(N) * sizeof(float);
     g.status = dev.status;
     cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kGemmSmem));

@@ -9,7 +9,24 @@
 namespace mx {
 
 // Device status codes written into the per-device status word.
-enum : int { kDevOk = 0, kDevTimeout = 6 };
+enum : int { kDevOk = 0, kDevTimeout = 6, kDevBounds = 8 };
+
+// Store guard.  In a build with MX_CHECKED=1 every global store of the
+// kernels first checks that [p, p + n) lies inside [base, base + size); a
+// store that would not is skipped and recorded as kDevBounds in the status
+// word (no trap).  Normal builds compile the guard away.
+#if defined(MX_CHECKED) && MX_CHECKED
+__device__ __forceinline__ bool mx_store_ok(const void *p, size_t n, const void *base, size_t size,
+                                            int *status) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(base);
+    if (a >= b && a + n <= b + size) return true;
+    if (status != nullptr) atomicExch(status, kDevBounds);
+    return false;
+}
+#define MX_STORE_OK(p, n, base, size, status) mx_store_ok((p), (n), (base), (size), (status))
+#else
+#define MX_STORE_OK(p, n, base, size, status) true
+#endif
 
 // Every spin-wait in this library gives up after this long (or after
 // kWaitMaxPolls polls, whichever comes first) and records kDevTimeout.

@@ -52,6 +52,8 @@ struct QuantArgs {
     int64_t katoms;    // scale k-atoms per 128-line group
     uint8_t *codes;
     uint8_t *scales;
+    size_t codes_bytes;   // extents of the two output buffers (store guards)
+    size_t scales_bytes;
     uint64_t seed;
     uint64_t sr_tag;
     int *status;
@@ -369,7 +371,9 @@ __device__ __forceinline__ void flush_scales(const uint8_t *stage, const QuantAr
         const uint64_t v = *reinterpret_cast<const uint64_t *>(stage + a * 256 + g * 8);
         const int64_t half = (line0 % 128) / 64;
         const int64_t atom = (line0 / 128) * p.katoms + k0 / 128 + a;
-        *reinterpret_cast<uint64_t *>(p.scales + atom * 512 + g * 16 + half * 8) = v;
+        uint8_t *dst = p.scales + atom * 512 + g * 16 + half * 8;
+        if (MX_STORE_OK(dst, 8, p.scales, p.scales_bytes, p.status))
+            *reinterpret_cast<uint64_t *>(dst) = v;
     }
 }
 
@@ -440,14 +444,20 @@ __device__ __forceinline__ void dual_rows(const uint32_t *tw, int64_t t0, int64_
         uint4 q;
         const uint32_t sb =
             encode_row_block<SR>(w, q, a0.seed, ar.sr_tag, static_cast<uint64_t>(t * ar.L + c));
-        if (t < ar.lines && c < ar.L) st_global_16(ar.codes + t * (ar.L / 2) + c / 2, q);
-        ar.scales[scale_offset(t, c / 32, ar.katoms)] = static_cast<uint8_t>(sb);
+        uint8_t *cdst = ar.codes + t * (ar.L / 2) + c / 2;
+        if (t < ar.lines && c < ar.L && MX_STORE_OK(cdst, 16, ar.codes, ar.codes_bytes, ar.status))
+            st_global_16(cdst, q);
+        uint8_t *sdst = ar.scales + scale_offset(t, c / 32, ar.katoms);
+        if (MX_STORE_OK(sdst, 1, ar.scales, ar.scales_bytes, ar.status))
+            *sdst = static_cast<uint8_t>(sb);
         // Padding blocks past the last channel tile: no tile covers them.
         if (c0 + TC == grid_end) {
 #pragma unroll
             for (int e = 0; e < 128 / TC; ++e) {
                 const int64_t pb = grid_end / 32 + cb + e * (TC / 32);
-                if (pb < kb_pad) ar.scales[scale_offset(t, pb, ar.katoms)] = 0;
+                uint8_t *pdst = ar.scales + scale_offset(t, pb, ar.katoms);
+                if (pb < kb_pad && MX_STORE_OK(pdst, 1, ar.scales, ar.scales_bytes, ar.status))
+                    *pdst = 0;
             }
         }
     }
@@ -552,6 +562,10 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads, SR ? 1 
         const int64_t katoms = second ? a1.katoms : a0.katoms;
         uint8_t *const codes = second ? a1.codes : a0.codes;
         uint8_t *const scales = second ? a1.scales : a0.scales;
+        const size_t codes_bytes = second ? a1.codes_bytes : a0.codes_bytes;
+        const size_t scales_bytes = second ? a1.scales_bytes : a0.scales_bytes;
+        (void)codes_bytes;
+        (void)scales_bytes;
         const int64_t t0 = static_cast<int64_t>(lt / inner) * G::TT;
         const int64_t c0 = static_cast<int64_t>(lt % inner) * G::TC;
 
@@ -613,13 +627,16 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads, SR ? 1 
         }
 
         if (tb < L) {
-            if (c < lines) st_global_16(codes + c * (L / 2) + tb / 2, q0);
-            if (c + 1 < lines) st_global_16(codes + (c + 1) * (L / 2) + tb / 2, q1);
+            uint8_t *d0 = codes + c * (L / 2) + tb / 2, *d1 = codes + (c + 1) * (L / 2) + tb / 2;
+            if (c < lines && MX_STORE_OK(d0, 16, codes, codes_bytes, a0.status)) st_global_16(d0, q0);
+            if (c + 1 < lines && MX_STORE_OK(d1, 16, codes, codes_bytes, a0.status))
+                st_global_16(d1, q1);
         }
         // Scale bytes (padding lines / blocks included: their input is zero).
         const int64_t kb = tb / 32;
-        scales[scale_offset(c, kb, katoms)] = static_cast<uint8_t>(s0);
-        scales[scale_offset(c + 1, kb, katoms)] = static_cast<uint8_t>(s1);
+        uint8_t *e0 = scales + scale_offset(c, kb, katoms), *e1 = scales + scale_offset(c + 1, kb, katoms);
+        if (MX_STORE_OK(e0, 1, scales, scales_bytes, a0.status)) *e0 = static_cast<uint8_t>(s0);
+        if (MX_STORE_OK(e1, 1, scales, scales_bytes, a0.status)) *e1 = static_cast<uint8_t>(s1);
     }
 }
 
@@ -697,6 +714,10 @@ __global__ void __launch_bounds__(kThreads, SR ? 1 : kColMinBlocks) mxq_colwise_
         const int64_t katoms = second ? a1.katoms : a0.katoms;
         uint8_t *const codes = second ? a1.codes : a0.codes;
         uint8_t *const scales = second ? a1.scales : a0.scales;
+        const size_t codes_bytes = second ? a1.codes_bytes : a0.codes_bytes;
+        const size_t scales_bytes = second ? a1.scales_bytes : a0.scales_bytes;
+        (void)codes_bytes;
+        (void)scales_bytes;
         const int64_t t0 = static_cast<int64_t>(lt / inner) * G::TT;
         const int64_t c0 = static_cast<int64_t>(lt % inner) * G::TC;
 
@@ -779,12 +800,16 @@ __global__ void __launch_bounds__(kThreads, SR ? 1 : kColMinBlocks) mxq_colwise_
             encode_pair_rne<true>(x, hadamard_norm<ROTN>(), q0, q1, s0, s1);
         }
         if (tb < L && c < lines) {
-            st_global_16(codes + c * (L / 2) + tb / 2, q0);
-            st_global_16(codes + c * (L / 2) + tb / 2 + 16, q1);
+            uint8_t *d = codes + c * (L / 2) + tb / 2;
+            if (MX_STORE_OK(d, 32, codes, codes_bytes, a0.status)) {
+                st_global_16(d, q0);
+                st_global_16(d + 16, q1);
+            }
         }
         const int64_t kb = tb / 32;
-        scales[scale_offset(c, kb, katoms)] = static_cast<uint8_t>(s0);
-        scales[scale_offset(c, kb + 1, katoms)] = static_cast<uint8_t>(s1);
+        uint8_t *e0 = scales + scale_offset(c, kb, katoms), *e1 = scales + scale_offset(c, kb + 1, katoms);
+        if (MX_STORE_OK(e0, 1, scales, scales_bytes, a0.status)) *e0 = static_cast<uint8_t>(s0);
+        if (MX_STORE_OK(e1, 1, scales, scales_bytes, a0.status)) *e1 = static_cast<uint8_t>(s1);
     }
 }
 
@@ -920,8 +945,9 @@ __global__ void __launch_bounds__(kThreads) mxq_rowwise_kernel(const __grid_cons
         if (SR) sr_draws32(p.seed, p.sr_tag, static_cast<uint64_t>(row * p.L + cb), u);
         const uint32_t sb = encode_block32<SR>(xb, qb, u);
         if (row < p.lines) {
-            if (ca < p.L) st_global_16(p.codes + row * (p.L / 2) + ca / 2, qa);
-            if (cb < p.L) st_global_16(p.codes + row * (p.L / 2) + cb / 2, qb);
+            uint8_t *da = p.codes + row * (p.L / 2) + ca / 2, *db = p.codes + row * (p.L / 2) + cb / 2;
+            if (ca < p.L && MX_STORE_OK(da, 16, p.codes, p.codes_bytes, p.status)) st_global_16(da, qa);
+            if (cb < p.L && MX_STORE_OK(db, 16, p.codes, p.codes_bytes, p.status)) st_global_16(db, qb);
         }
         sstage[stage_offset(r, blk_a)] = static_cast<uint8_t>(sa);
         sstage[stage_offset(r, blk_a + 4)] = static_cast<uint8_t>(sb);
@@ -1027,6 +1053,9 @@ bool prepare_operand(const void *src, int64_t rows, int64_t cols, bool colwise, 
     a->katoms = scale_katoms(a->L);
     a->codes = static_cast<uint8_t *>(codes);
     a->scales = static_cast<uint8_t *>(scales);
+    a->codes_bytes = static_cast<size_t>(a->lines) * static_cast<size_t>(a->L / 2);
+    a->scales_bytes = static_cast<size_t>(128 * scale_groups(a->lines)) *
+                      static_cast<size_t>(4 * scale_katoms(a->L));
     a->seed = seed;
     a->sr_tag = sr_tag;
     a->status = dev.status;
@@ -1103,6 +1132,9 @@ cudaError_t launch_quantize_dual(const void *src, int64_t rows, int64_t cols, in
     o.ar.katoms = scale_katoms(cols);
     o.ar.codes = static_cast<uint8_t *>(codes_n);
     o.ar.scales = static_cast<uint8_t *>(scales_n);
+    o.ar.codes_bytes = static_cast<size_t>(rows) * static_cast<size_t>(cols / 2);
+    o.ar.scales_bytes = static_cast<size_t>(128 * scale_groups(rows)) *
+                        static_cast<size_t>(4 * scale_katoms(cols));
     o.ar.seed = seed;
     o.ar.sr_tag = 1;
     o.ar.status = dev.status;
