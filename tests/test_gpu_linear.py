@@ -2,6 +2,8 @@
 the oracle, on small ragged shapes (full outputs) and on the full-size
 Llama-3.1-8B-shaped workloads (every code byte where affordable, otherwise
 sampled lines; sampled output entries computed one by one by the oracle)."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -61,6 +63,46 @@ def check_op(op, a, b, rot, nb, rnd=mx.ROUND_RNE, seed=0, sample=None):
     Cref, Cabs = oracle.gemm(Aq, As, Bq, Bs)
     got = out if sample is None else out[np.ix_(ia, jb)]
     return assert_gemm_close(got, Cref, Cabs, f"op {op} rot {rot}/{nb} rnd {rnd}")
+
+
+def _par_gemm(Aq, As, Bq, Bs, split_b):
+    """oracle.gemm partitioned over the host cores (the oracle's C code releases
+    the GIL), by blocks of B's lines (output columns) or of A's lines (rows)."""
+    from concurrent.futures import ThreadPoolExecutor
+    n = (Bq if split_b else Aq).shape[0]
+    parts = max(1, min(os.cpu_count() or 1, n // 8))
+    edges = np.linspace(0, n, parts + 1).astype(int)
+    def one(i):
+        lo, hi = edges[i], edges[i + 1]
+        if split_b:
+            return oracle.gemm(Aq, As, Bq[lo:hi], Bs[lo:hi])
+        return oracle.gemm(Aq[lo:hi], As[lo:hi], Bq, Bs)
+    with ThreadPoolExecutor(parts) as ex:
+        res = list(ex.map(one, range(parts)))
+    axis = 1 if split_b else 0
+    return np.concatenate([r[0] for r in res], axis), np.concatenate([r[1] for r in res], axis)
+
+
+def check_op_rows_cols(op, a, b, rot, nb, rnd=mx.ROUND_RNE, seed=0, n_rows=64, n_cols=64,
+                       n_rand=4096):
+    """Full-size check: n_rows full output rows, n_cols full output columns and
+    n_rand random entries, each computed by the oracle from every encoded line."""
+    out = run_op(op, a, b, rot, nb, rnd, seed).cpu().numpy()
+    (ca, na), (cb, nb_lines) = _operands(op, a, b)
+    Aq, As = oracle.quantize(a, OC[ca], rot, nb, rnd, seed, 1)
+    Bq, Bs = oracle.quantize(b, OC[cb], rot, nb, rnd, seed, 2)
+    rows = sample_lines(na, n_rows, 11)
+    cols = sample_lines(nb_lines, n_cols, 12)
+    worst = 0.0
+    Cr, Car = _par_gemm(Aq[rows], As[rows], Bq, Bs, split_b=True)
+    worst = max(worst, assert_gemm_close(out[rows], Cr, Car, f"op {op}: {rows.size} full rows"))
+    Cc, Cac = _par_gemm(Aq, As, Bq[cols], Bs[cols], split_b=False)
+    worst = max(worst, assert_gemm_close(out[:, cols], Cc, Cac, f"op {op}: {cols.size} full cols"))
+    rng = np.random.default_rng(13)
+    ii, jj = rng.integers(0, na, n_rand), rng.integers(0, nb_lines, n_rand)
+    Ce, Cae = oracle.gemm_entries(Aq, As, Bq, Bs, ii, jj)
+    worst = max(worst, assert_gemm_close(out[ii, jj], Ce, Cae, f"op {op}: {n_rand} entries"))
+    return worst
 
 
 def _bits(shape, seed, scale=1.0):
@@ -124,7 +166,7 @@ def test_o_proj_full_size():
     d = config_inputs("o_proj", seed=0)
     for name in ("dY", "X"):
         _compare_codes(d[name], mx.CONTRACT_ROWS, mx.ROT_HADAMARD_DET, 32, mx.ROUND_RNE, 0)
-    worst = check_op(mx.OP_WGRAD, d["dY"], d["X"], mx.ROT_HADAMARD_DET, 32, sample=48)
+    worst = check_op_rows_cols(mx.OP_WGRAD, d["dY"], d["X"], mx.ROT_HADAMARD_DET, 32)
     assert worst < 1e-5
 
 
@@ -154,6 +196,7 @@ def test_qkv_gateup_all_three_gemms():
     X = d["X"]
     for w, dy in (("W_qkv", "dY_qkv"), ("W_gu", "dY_gu")):
         W, dY = d[w], d[dy]
-        check_op(mx.OP_FPROP, X, W, mx.ROT_NONE, 32, sample=24)
-        check_op(mx.OP_DGRAD, dY, W, mx.ROT_NONE, 32, sample=24)
-        check_op(mx.OP_WGRAD, dY, X, mx.ROT_HADAMARD_DET, 32, sample=24)
+        # each GEMM: >= 64 full rows, >= 64 full columns and 4,096 random entries
+        check_op_rows_cols(mx.OP_FPROP, X, W, mx.ROT_NONE, 32)
+        check_op_rows_cols(mx.OP_DGRAD, dY, W, mx.ROT_NONE, 32)
+        check_op_rows_cols(mx.OP_WGRAD, dY, X, mx.ROT_HADAMARD_DET, 32)
