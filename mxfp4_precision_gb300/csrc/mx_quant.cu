@@ -8,19 +8,28 @@
 // minus 2, the largest E2M1 exponent) and each element is rounded to E2M1
 // (nearest-even, or stochastically) and packed two per byte.
 //
-// Two kernels, both persistent with a 3-deep TMA ring:
-//   mxq_colwise  contraction down the rows of src[T][C] (Wgrad operands,
-//                Dgrad's W): a 256-token x 64-channel tile is loaded by TMA;
-//                each thread owns 2 adjacent channels x 32 tokens, so the
-//                transpose is free (it reads a column pair from shared
-//                memory) and the Hadamard up to 32 and the block amax stay in
-//                registers.  Hadamard stages of stride >= 32 cross warps
-//                through a shared-memory exchange.
-//   mxq_rowwise  contraction along the rows of src[R][C] (Fprop operands,
-//                Dgrad's dY): a 64-row x 256-column tile arrives as four
-//                128-byte-swizzled TMA boxes; each thread owns 2 blocks of 32
-//                of one row; Hadamard stages of stride 32/64 use warp
-//                shuffles, stride 128 is in-thread.
+// Three kernels, all persistent with a 2-deep ring of 32 KB TMA tiles (up to
+// two resident CTAs per SM):
+//   mxq_colwise       contraction down the rows of src[T][C] (Wgrad operands,
+//                     Dgrad's W), no rotation or Hadamard 16/32: a 128-token
+//                     x 128-channel tile; each thread owns 2 adjacent
+//                     channels x 32 tokens as packed f32x2 pairs, so the
+//                     transpose is free (it reads a column pair from shared
+//                     memory) and the Hadamard and the block amax stay in
+//                     registers.  A ninth warp refills the ring.  With DUAL
+//                     it also encodes the staged tile along the channels
+//                     (the Dgrad encoding of the same dY).
+//   mxq_colwise_wide  the same direction for Hadamard 64/128/256 (128 x 128
+//                     tiles, 256 x 64 for 256): each thread owns one
+//                     channel x 64 tokens as pairs {t, t+32}; the
+//                     stride-64 and stride-128 stages pair lanes by warp
+//                     shuffles.
+//   mxq_rowwise       contraction along the rows of src[R][C] (Fprop
+//                     operands, Dgrad's dY): a 64-row x 256-column tile
+//                     arrives as four 128-byte-swizzled TMA boxes; each
+//                     thread owns 2 blocks of 32 of one row; Hadamard stages
+//                     of stride 32/64 use warp shuffles, stride 128 is
+//                     in-thread.
 // Fp32 arithmetic uses explicit round-to-nearest intrinsics so that the
 // rotated values are bit-identical to the canonical butterfly order.
 #include <cstdint>
@@ -43,7 +52,7 @@ constexpr int kStages = MXQ_STAGES;  // TMA ring depth per CTA
 constexpr int kColMinBlocks = 2;
 constexpr int kThreads = 256;           // compute threads (8 warps)
 constexpr int kColProducerThreads = kThreads + 32;  // + a TMA producer warp
-constexpr uint32_t kTileBytes = 32768;  // 256 x 64 bf16 (colwise) / 64 x 256 bf16 (rowwise)
+constexpr uint32_t kTileBytes = 32768;  // one staged bf16 tile (128 x 128, 256 x 64 or 64 x 256)
 constexpr uint32_t kScaleStage = 512;   // two half-atoms of scales per tile
 
 struct QuantArgs {
@@ -468,8 +477,8 @@ __device__ __forceinline__ void dual_rows(const uint32_t *tw, int64_t t0, int64_
 // launch encodes up to two operands (the two Wgrad operands): tiles
 // [0, a0.num_tiles) belong to operand 0, the rest to operand 1.  Every warp
 // works on its own 32-token slice of the tile, so no CTA-wide barrier is taken
-// inside the loop: each warp marks the stage consumed on an mbarrier and
-// thread 0 refills it once all eight have.  Tile: 128 tokens x 128 channels of
+// inside the loop: each warp marks the stage consumed on an mbarrier, and the
+// stage is refilled once all eight have.  Tile: 128 tokens x 128 channels of
 // bf16 (32 KB, 256-byte contiguous row segments).
 template <int ROTN>
 struct ColTile {
