@@ -50,6 +50,34 @@ def test_gemm_parity(M, N, K):
     assert worst < 1e-5
 
 
+def _sm_count():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("N", [2048, 2048 - 100, 1792 + 100])
+def test_gemm_small_last_round(N):
+    """More 128 x 256 tiles than SMs, with a last round of at most 8 tiles.
+    N = 1948 and N = 1892 leave the last column tile 156 and 100 wide."""
+    m_tiles = _sm_count() // 8 + 1
+    M, K = 128 * m_tiles - 37, 512
+    Aq, As = _operand(M, K, 11, 1e-3)
+    Bq, Bs = _operand(N, K, 12)
+    C = run_gemm(Aq, As, Bq, Bs, M, N, K)
+    Cref, Cabs = oracle.gemm(Aq, As, Bq, Bs)
+    assert assert_gemm_close(C, Cref, Cabs, f"small last round {M}x{N}x{K}") < 1e-5
+
+
+def test_gemm_large_last_round():
+    """More tiles than SMs, with a last round of more than 100 tiles."""
+    m_tiles = (_sm_count() + 100) // 8 + 1
+    M, N, K = 128 * m_tiles, 2048, 256
+    Aq, As = _operand(M, K, 13, 1e-3)
+    Bq, Bs = _operand(N, K, 14)
+    C = run_gemm(Aq, As, Bq, Bs, M, N, K)
+    Cref, Cabs = oracle.gemm(Aq, As, Bq, Bs)
+    assert assert_gemm_close(C, Cref, Cabs, f"large last round {M}x{N}x{K}") < 1e-5
+
+
 def test_gemm_zero_and_nan_scales():
     # a block whose scale byte is 0 (all-zero block) contributes nothing
     M, N, K = 128, 256, 512
