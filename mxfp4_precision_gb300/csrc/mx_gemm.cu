@@ -7,6 +7,19 @@
 // accumulation.
 //
 // Design (one CTA per SM, persistent over 128 x 256 output tiles):
+//   schedule     CTA b takes work items b, b + G, b + 2G, ... (G CTAs, in
+//                clusters of two).  An item is a whole tile, except in a last
+//                round that would leave at least half of the CTAs idle (tiles
+//                mod G <= G/2): there each remaining tile becomes two items,
+//                the two halves of its K range, run by the two CTAs of one
+//                cluster.  Each CTA then stores one column half of the tile:
+//                it leaves its fp32 partial of the other column half in its
+//                own shared memory (its stage ring is idle by then), reads
+//                the partner's partial of its own half through distributed
+//                shared memory, adds the two (fp32 addition of the two K
+//                halves is commutative, so both CTAs' sums are the same bits)
+//                and stores.  The last round then takes about half a tile
+//                time instead of a whole one.
 //   warp 0       TMA producer: 128B-swizzled A/B code tiles (K-tile of 256
 //                FP4 = 128 bytes per row) and the two matching 1 KB scale
 //                slabs per 128 rows, into a 4-stage shared-memory ring.
@@ -21,6 +34,7 @@
 //                the next tile's main loop runs.
 // Every wait is bounded (see mx_ptx.cuh); a timeout records an error and the
 // CTA unwinds without faulting.
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -56,6 +70,9 @@ struct GemmArgs {
     int k_tiles;
     int n_tiles;
     int num_tiles;
+    int num_items;       // whole tiles [0, dp_tiles), then two K halves per remaining tile
+    int dp_tiles;
+    int k_split;         // first K-tile of a second half
     int c_v8;            // C rows allow 32-byte stores (N % 8 == 0, C 32-byte aligned)
     size_t c_bytes;      // extent of C (store guards)
     int *status;
@@ -67,6 +84,7 @@ struct SharedCtl {
     uint64_t acc_full;
     uint64_t acc_empty;
     uint64_t drain;
+    uint64_t part_ready;  // split tile: the partner's partial of this CTA's column half is in place
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -85,7 +103,26 @@ __device__ __forceinline__ void st_global_v8(float *p, const uint32_t *v) {
                  : "memory");
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// Work item w: output tile, K-tile range [k0, k1), and which K half it is
+// (-1: the whole range).
+struct Item {
+    int tile, k0, k1, khalf;
+};
+__device__ __forceinline__ Item item_of(const GemmArgs &g, int w) {
+    if (w < g.dp_tiles) return Item{w, 0, g.k_tiles, -1};
+    const int j = w - g.dp_tiles, h = j % 2;
+    return Item{g.dp_tiles + j / 2, h == 0 ? 0 : g.k_split, h == 0 ? g.k_split : g.k_tiles, h};
+}
+
+// A split tile's partial of one column half: the 128 epilogue threads that
+// hold that half (4 warps) keep 128 fp32 values each, as 32 chunks of 16
+// bytes; chunk i of thread t of the half sits at (i * 128 + t) * 16, so a
+// warp's 16-byte accesses to one chunk are contiguous.
+constexpr int kHalfThreads = 16 * kEpiWarps;
+constexpr uint32_t kPartialBytes = 32u * kHalfThreads * 16u;  // 64 KB
+static_assert(kPartialBytes <= kStages * kStageBytes, "the partial lives in the stage ring");
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b, const GemmArgs g) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -103,6 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&ctl->acc_full, 1);
         mbar_init(&ctl->acc_empty, kEpiWarps);
         mbar_init(&ctl->drain, 1);
+        mbar_init(&ctl->part_ready, kEpiWarps / 2);
         ctl->abort_flag = 0;
         fence_barrier_init();
         prefetch_tmap(&map_a);
@@ -113,7 +151,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    // Both CTAs of the cluster have initialised their barriers before either
+    // signals the other.
+    __syncwarp();
+    cluster_sync();
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
     volatile int *abort = &ctl->abort_flag;
@@ -124,9 +165,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < g.num_tiles; tile += gridDim.x) {
-                const int mb = tile / g.n_tiles, nb = tile % g.n_tiles;
-                for (int kt = 0; kt < g.k_tiles; ++kt) {
+            for (int w = blockIdx.x; ok && w < g.num_items; w += gridDim.x) {
+                const Item it = item_of(g, w);
+                const int mb = it.tile / g.n_tiles, nb = it.tile % g.n_tiles;
+                for (int kt = it.k0; kt < it.k1; ++kt) {
                     if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, g.status, abort)) {
                         ok = false;
                         break;
@@ -160,10 +202,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < g.num_tiles; tile += gridDim.x) {
+            for (int w = blockIdx.x; ok && w < g.num_items; w += gridDim.x) {
+                const Item it = item_of(g, w);
                 if (!mbar_wait(&ctl->acc_empty, acc_phase ^ 1u, g.status, abort)) break;
                 tc_fence_after();
-                for (int kt = 0; kt < g.k_tiles; ++kt) {
+                for (int kt = it.k0; kt < it.k1; ++kt) {
                     if (!mbar_wait(&ctl->full[stage], phase, g.status, abort)) {
                         ok = false;
                         break;
@@ -191,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_mxf4(tmem + kAccCol, sdesc_sw128(sa + 32u * j),
                                  sdesc_sw128(sb + 32u * j), idesc_mxf4(kBM, kBN, sf_id, sf_id),
                                  sf_col + 4u * ka, sf_col + 8u + 8u * ka,
-                                 (kt > 0 || j > 0) ? 1u : 0u);
+                                 (kt > it.k0 || j > 0) ? 1u : 0u);
                     }
                     tc_commit(&ctl->empty[stage]);
                     if (++stage == kStages) {
@@ -212,8 +255,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;           // TMEM lane quarter this warp may access
         const int half = (warp - 2) / 4;  // column half of the 256-wide tile
         uint32_t acc_phase = 0;
-        for (int tile = blockIdx.x; tile < g.num_tiles; tile += gridDim.x) {
-            const int mb = tile / g.n_tiles, nb = tile % g.n_tiles;
+        const int ht = ((warp - 2) & 3) * 32 + lane;  // thread index within its column half
+        for (int w = blockIdx.x; w < g.num_items; w += gridDim.x) {
+            const Item it = item_of(g, w);
+            const int mb = it.tile / g.n_tiles, nb = it.tile % g.n_tiles;
             // One lane waits; the verdict is broadcast so the warp stays
             // converged for the .sync.aligned tensor-memory loads.
             int ok = 1;
@@ -231,6 +276,51 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->acc_empty);
             acc_phase ^= 1u;
+
+            if (it.khalf >= 0) {
+                // Split tile: CTA rank r (= it.khalf) stores column half r.
+                if (half != it.khalf) {
+                    // Leave this half's partial for the partner and signal it.
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(
+                                smem + (static_cast<uint32_t>((8 * c + j) * kHalfThreads + ht) << 4));
+                            *dst = make_uint4(v[c][4 * j], v[c][4 * j + 1], v[c][4 * j + 2],
+                                              v[c][4 * j + 3]);
+                        }
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->part_ready), 1u - it.khalf));
+                    continue;
+                }
+                int okp = 1;
+                if (lane == 0) okp = mbar_wait_cluster(&ctl->part_ready, 0, g.status, abort) ? 1 : 0;
+                okp = __shfl_sync(0xFFFFFFFFu, okp, 0);
+                if (!okp) break;
+                // Every lane takes the acquire itself (the phase is complete).
+                mbar_wait_cluster(&ctl->part_ready, 0, g.status, abort);
+                const uint32_t peer = mapa_shared(smem_u32(smem), 1u - it.khalf);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint4 p[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        p[j] = ld_shared_cluster_v4(
+                            peer + (static_cast<uint32_t>((8 * c + j) * kHalfThreads + ht) << 4));
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        v[c][4 * j] = __float_as_uint(__uint_as_float(v[c][4 * j]) + __uint_as_float(p[j].x));
+                        v[c][4 * j + 1] =
+                            __float_as_uint(__uint_as_float(v[c][4 * j + 1]) + __uint_as_float(p[j].y));
+                        v[c][4 * j + 2] =
+                            __float_as_uint(__uint_as_float(v[c][4 * j + 2]) + __uint_as_float(p[j].z));
+                        v[c][4 * j + 3] =
+                            __float_as_uint(__uint_as_float(v[c][4 * j + 3]) + __uint_as_float(p[j].w));
+                    }
+                }
+            }
 
             const int64_t row = static_cast<int64_t>(mb) * kBM + 32 * q + lane;
             if (row < g.M) {
@@ -268,6 +358,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tc_fence_before();
     __syncthreads();
+    // Neither CTA of a cluster leaves while the other may still read its
+    // shared memory.
+    __syncwarp();
+    cluster_sync();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -275,6 +369,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 constexpr size_t kGemmSmem = kStages * kStageBytes + sizeof(SharedCtl) + 1024;
+
+// Co-resident 2-CTA clusters of mx_gemm_kernel on a device, measured once.
+int gemm_clusters(const DeviceInfo &dev) {
+    static std::atomic<int> cache[64];
+    const int idx = dev.ordinal >= 0 && dev.ordinal < 64 ? dev.ordinal : 0;
+    int n = cache[idx].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+    if (cudaFuncSetAttribute(mx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kGemmSmem)) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kGemmSmem;
+    if (cudaOccupancyMaxActiveClusters(&n, mx_gemm_kernel, &cfg) != cudaSuccess || n < 1) return 0;
+    cache[idx].store(n, std::memory_order_relaxed);
+    return n;
+}
 
 }  // namespace
 
@@ -309,7 +421,20 @@ cudaError_t launch_gemm(const void *Aq, const void *As, const void *Bq, const vo
     cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kGemmSmem));
     if (e != cudaSuccess) return e;
-    const int grid = g.num_tiles < dev.sm_count ? g.num_tiles : dev.sm_count;
+    // Resident CTAs: as many 2-CTA clusters as fit at once.
+    const int slots = 2 * gemm_clusters(dev);
+    if (slots < 2) return cudaErrorLaunchOutOfResources;
+    const int rem = g.num_tiles % slots;
+    g.dp_tiles = g.num_tiles;
+    g.num_items = g.num_tiles;
+    g.k_split = g.k_tiles;
+    if (rem > 0 && 2 * rem <= slots && g.k_tiles >= 2) {
+        g.dp_tiles = g.num_tiles - rem;
+        g.num_items = g.dp_tiles + 2 * rem;
+        g.k_split = g.k_tiles / 2;
+    }
+    int grid = g.num_items < slots ? g.num_items : slots;
+    grid += grid & 1;
     mx_gemm_kernel<<<grid, kThreads, kGemmSmem, stream>>>(map_a, map_b, g);
     return cudaGetLastError();
 }

@@ -128,6 +128,54 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Shared::cluster address of the object at shared address `saddr` in the
+// CTA of rank `rank` within this cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+// Arrive on an mbarrier given by its shared::cluster address, releasing this
+// thread's prior writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+// Bounded wait on an mbarrier of this CTA with acquire at cluster scope, for
+// phases completed by arrivals from other CTAs of the cluster.  Same limits
+// and error reporting as mbar_wait.
+static __device__ __noinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, int *status,
+                                                      volatile int *abort) {
+    const uint32_t addr = smem_u32(bar);
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t poll = 0; poll < kWaitMaxPolls; ++poll) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(addr), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if ((poll & 63u) == 63u) {
+            if (abort != nullptr && *abort) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) break;
+        }
+    }
+    if (status != nullptr) atomicExch(status, kDevTimeout);
+    if (abort != nullptr) *abort = 1;
+    return false;
+}
+// 16-byte load from the shared memory of a CTA of this cluster.
+__device__ __forceinline__ uint4 ld_shared_cluster_v4(uint32_t cluster_addr) {
+    uint4 v;
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
+}
 // 2-D tiled load delivered to the same shared offset of every CTA in
 // `cta_mask`; each destination's mbarrier (same offset) receives the bytes.
 __device__ __forceinline__ void tma_load_2d_mc(void *dst, const CUtensorMap *map, uint64_t *bar,
