@@ -31,11 +31,15 @@
 //   warps 2..9   epilogue: tcgen05.ld the accumulator (each warp one 32-lane
 //                quarter x 128 columns) into registers, release tensor
 //                memory to the MMA warp at once, then store fp32 rows while
-//                the next tile's main loop runs.
+//                the next tile's main loop runs.  A CTA's last item, whose
+//                stores nothing overlaps, is staged in the idle stage ring
+//                (128-byte swizzled 32 x 32 boxes) and written by TMA stores
+//                of whole lines.
 // Every wait is bounded (see mx_ptx.cuh); a timeout records an error and the
 // CTA unwinds without faulting.
 #include <atomic>
 #include <cstdint>
+#include <cstring>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -74,6 +78,7 @@ struct GemmArgs {
     int dp_tiles;
     int k_split;         // first K-tile of a second half
     int c_v8;            // C rows allow 32-byte stores (N % 8 == 0, C 32-byte aligned)
+    int c_tma;           // C allows TMA stores (N % 4 == 0, C 16-byte aligned)
     size_t c_bytes;      // extent of C (store guards)
     int *status;
 };
@@ -121,10 +126,16 @@ __device__ __forceinline__ Item item_of(const GemmArgs &g, int w) {
 constexpr int kHalfThreads = 16 * kEpiWarps;
 constexpr uint32_t kPartialBytes = 32u * kHalfThreads * 16u;  // 64 KB
 static_assert(kPartialBytes <= kStages * kStageBytes, "the partial lives in the stage ring");
+// TMA-store staging of a last item: per epilogue warp, four 32 x 32 fp32
+// boxes (4 KB each, 128-byte swizzle), after the partial.
+constexpr uint32_t kStageOutBytes = 4u * 4096u;
+static_assert(kPartialBytes + kEpiWarps * kStageOutBytes <= kStages * kStageBytes,
+              "the output staging lives in the stage ring");
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
-                   const __grid_constant__ CUtensorMap map_b, const GemmArgs g) {
+                   const __grid_constant__ CUtensorMap map_b,
+                   const __grid_constant__ CUtensorMap map_c, const GemmArgs g) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned base, kept as a shared-space pointer (offset arithmetic
     // only) so that the compiler emits shared-memory loads.
@@ -145,6 +156,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         fence_barrier_init();
         prefetch_tmap(&map_a);
         prefetch_tmap(&map_b);
+        if (g.c_tma) prefetch_tmap(&map_c);
     }
     if (warp == 1) {
         tmem_alloc(&ctl->tmem_base, kTmemCols);
@@ -322,6 +334,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
             }
 
+            if (g.c_tma && w + static_cast<int>(gridDim.x) >= g.num_items) {
+                // Last item: stage this warp's 32 rows x 128 columns as four
+                // swizzled boxes and store them with TMA (rows and columns
+                // outside C are not written).
+                uint8_t *stg = smem + kPartialBytes + static_cast<uint32_t>(warp - 2) * kStageOutBytes;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(
+                            stg + c * 4096 + lane * 128 + (((j ^ (lane & 7)) & 7) << 4));
+                        *dst = make_uint4(v[c][4 * j], v[c][4 * j + 1], v[c][4 * j + 2],
+                                          v[c][4 * j + 3]);
+                    }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const int32_t r0 = mb * kBM + 32 * q;
+                    const int32_t cb = nb * kBN + 128 * half;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        if (cb + 32 * c < g.N && r0 < g.M)  // boxes that start inside C only
+                            tma_store_2d(&map_c, stg + c * 4096, cb + 32 * c, r0);
+                    bulk_commit_group();
+                    bulk_wait_group_0();
+                }
+                __syncwarp();
+                continue;
+            }
             const int64_t row = static_cast<int64_t>(mb) * kBM + 32 * q + lane;
             if (row < g.M) {
                 float *crow = g.C + row * g.N;
@@ -393,7 +434,7 @@ int gemm_clusters(const DeviceInfo &dev) {
 cudaError_t launch_gemm(const void *Aq, const void *As, const void *Bq, const void *Bs, float *C,
                         int64_t M, int64_t N, int64_t K, const DeviceInfo &dev,
                         cudaStream_t stream) {
-    CUtensorMap map_a, map_b;
+    CUtensorMap map_a, map_b, map_c;
     if (!encode_tmap_2d(&map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, Aq, K / 2, M, K / 2, kBKBytes, kBM,
                         CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
@@ -416,6 +457,13 @@ cudaError_t launch_gemm(const void *Aq, const void *As, const void *Bq, const vo
     g.n_tiles = static_cast<int>(n_tiles);
     g.num_tiles = static_cast<int>(m_tiles * n_tiles);
     g.c_v8 = (N % 8 == 0 && (reinterpret_cast<uintptr_t>(C) & 31) == 0) ? 1 : 0;
+    std::memset(&map_c, 0, sizeof(map_c));
+    g.c_tma = (N % 4 == 0 && (reinterpret_cast<uintptr_t>(C) & 15) == 0 &&
+               encode_tmap_2d(&map_c, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M,
+                              static_cast<uint64_t>(N) * sizeof(float), 32, 32,
+                              CU_TENSOR_MAP_SWIZZLE_128B))
+                  ? 1
+                  : 0;
     g.c_bytes = static_cast<size_t>(M) * static_cast<size_t>(N) * sizeof(float);
     g.status = dev.status;
     cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -435,7 +483,7 @@ cudaError_t launch_gemm(const void *Aq, const void *As, const void *Bq, const vo
     }
     int grid = g.num_items < slots ? g.num_items : slots;
     grid += grid & 1;
-    mx_gemm_kernel<<<grid, kThreads, kGemmSmem, stream>>>(map_a, map_b, g);
+    mx_gemm_kernel<<<grid, kThreads, kGemmSmem, stream>>>(map_a, map_b, map_c, g);
     return cudaGetLastError();
 }
 

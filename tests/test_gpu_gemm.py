@@ -40,7 +40,8 @@ def run_gemm(Aq, As, Bq, Bs, M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 256), (200, 328, 800), (512, 768, 2048),
-                                   (384, 1024, 1024), (136, 120, 96), (256, 512, 8192)])
+                                   (384, 1024, 1024), (136, 120, 96), (256, 512, 8192),
+                                   (130, 252, 512), (300, 1028, 1024)])
 def test_gemm_parity(M, N, K):
     Aq, As = _operand(M, K, 1, 1e-3)
     Bq, Bs = _operand(N, K, 2)
