@@ -79,6 +79,21 @@ def test_gemm_large_last_round():
     assert assert_gemm_close(C, Cref, Cabs, f"large last round {M}x{N}x{K}") < 1e-5
 
 
+def test_gemm_split_rounds_deterministic():
+    """Runs whose last round is split along K give the same bits every time:
+    the two halves are summed in a fixed order."""
+    m_tiles = _sm_count() // 8 + 1
+    M, N, K = 128 * m_tiles, 2048, 1024
+    Aq, As = _operand(M, K, 21, 1e-3)
+    Bq, Bs = _operand(N, K, 22)
+    args = (_dev(Aq), _dev(tile_scales(As, M, K)), _dev(Bq), _dev(tile_scales(Bs, N, K)), M, N, K)
+    first = mx.gemm(*args)
+    for _ in range(3):
+        again = mx.gemm(*args)
+        assert torch.equal(first, again)
+    mx.check_status()
+
+
 def test_gemm_zero_and_nan_scales():
     # a block whose scale byte is 0 (all-zero block) contributes nothing
     M, N, K = 128, 256, 512
