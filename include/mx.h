@@ -255,6 +255,34 @@ mx_status mx_check_status(void *stream);
  * MX_ERR_TIMEOUT.  Exists to test the timeout path without hanging a GPU. */
 mx_status mx_debug_timeout_probe(int64_t limit_us, void *stream);
 
+/*
+ * mx_bench_mma -- tensor-core issue-rate microbenchmark (measurement only; no
+ * counterpart in the pages, which report no kernel-level figure).  Every SM
+ * (one CTA each, or one 2-CTA cluster per SM pair for cta_group = 2) issues
+ * `iters` iterations of: `copies_per_iter` scale copies shared -> tensor
+ * memory, then `mmas_per_iter` tcgen05.mma of M = 128*cta_group, N = n, on
+ * operands resident in shared memory, with fp32 accumulation in tensor memory.
+ *   kind        0 mxf4 (E2M1, UE8M0/32, K=64)   1 mxf4nvf4 2X (same scales)
+ *               2 mxf4nvf4 4X (UE4M3/16)        3 f8f6f4 E4M3 (K=32)
+ *               4 f16 with bf16 inputs (K=16)   5 mxf8f6f4 E4M3, UE8M0/32 (K=32)
+ *   copy_shape  0 32x128b.warpx4, 1 128x256b, 2 128x128b
+ *   depth       0: no handshake; 1..7: commit every iteration to an mbarrier
+ *               and wait for the commit of iteration it - depth (a ring of
+ *               `depth` stages in flight, as in a pipelined GEMM)
+ *   flags       bit 0: the copies fill the NEXT iteration's scale columns;
+ *               bit 1: with depth > 0, commit every iteration but never wait;
+ *               bit 2: four more warps keep storing to unused tensor-memory
+ *               columns (tcgen05.st) while the MMAs run
+ *   d_ns        device int64[256]: per CTA, ns from the first to the last
+ *               MMA's completion (0 for the second CTA of a pair; -1 if a
+ *               bounded wait expired)
+ *   h_ctas      host int: CTAs launched
+ * MMA flops per CTA = 2 * 128 * n * K * mmas_per_iter * iters.
+ */
+mx_status mx_bench_mma(int kind, int cta_group, int n, int mmas_per_iter, int copies_per_iter,
+                       int copy_shape, int depth, int flags, int64_t iters, int64_t *d_ns,
+                       int *h_ctas, void *stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *mx_status_string(int status);
 

@@ -7,7 +7,8 @@ in the library's CUDA kernels; there is no CPU fallback -- if the library is
 missing or fails to load, every call raises.
 """
 from ._binding import (CONTRACT_COLS, CONTRACT_ROWS, OP_DGRAD, OP_FPROP, OP_WGRAD, ROT_HADAMARD_DET,
-                       ROT_HADAMARD_RAND, ROT_NONE, ROUND_RNE, ROUND_SR, MXError, check_status,
+                       ROT_HADAMARD_RAND, ROT_NONE, ROUND_RNE, ROUND_SR, MMA_KINDS, MXError, bench_mma,
+                       check_status,
                        codes_bytes, debug_timeout_probe, gemm, gemm_into, lib, library_path,
                        linear_dgrad, linear_fprop, linear_wgrad, linear_wgrad_noalloc,
                        linear_workspace_bytes, NOALLOC_SCRATCH_BYTES, quantize, quantize_dual,
@@ -16,7 +17,8 @@ from ._binding import (CONTRACT_COLS, CONTRACT_ROWS, OP_DGRAD, OP_FPROP, OP_WGRA
 
 __all__ = [
     "CONTRACT_COLS", "CONTRACT_ROWS", "OP_DGRAD", "OP_FPROP", "OP_WGRAD", "ROT_HADAMARD_DET",
-    "ROT_HADAMARD_RAND", "ROT_NONE", "ROUND_RNE", "ROUND_SR", "MXError", "check_status",
+    "ROT_HADAMARD_RAND", "ROT_NONE", "ROUND_RNE", "ROUND_SR", "MMA_KINDS", "MXError", "bench_mma",
+    "check_status",
     "codes_bytes", "debug_timeout_probe", "gemm", "gemm_into", "lib", "library_path",
     "linear_dgrad", "linear_fprop", "linear_wgrad", "linear_wgrad_noalloc", "linear_workspace_bytes",
     "NOALLOC_SCRATCH_BYTES", "quantize", "quantize_dual", "quantize_pair",

@@ -25,7 +25,7 @@ EXPORTED = [
     "mx_gemm", "mx_linear_workspace_bytes",
     "mx_linear_wgrad", "mx_linear_fprop", "mx_linear_dgrad", "mx_linear_wgrad_noalloc",
     "mx_check_status",
-    "mx_debug_timeout_probe", "mx_status_string", "mx_version",
+    "mx_debug_timeout_probe", "mx_bench_mma", "mx_status_string", "mx_version",
 ]
 
 _lock = threading.Lock()
@@ -81,6 +81,8 @@ def lib() -> ctypes.CDLL:
             L.mx_check_status.restype = i32
             L.mx_debug_timeout_probe.argtypes = [i64, P]
             L.mx_debug_timeout_probe.restype = i32
+            L.mx_bench_mma.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i64, P, P, P]
+            L.mx_bench_mma.restype = i32
             L.mx_status_string.argtypes = [i32]
             L.mx_status_string.restype = ctypes.c_char_p
             L.mx_version.argtypes = []
@@ -280,3 +282,34 @@ def debug_timeout_probe(limit_us: int, stream=None) -> int:
     """Launch the never-completed-barrier probe; returns mx_check_status's code."""
     _check(lib().mx_debug_timeout_probe(limit_us, _stream(stream)), "mx_debug_timeout_probe")
     return int(lib().mx_check_status(_stream(stream)))
+
+
+# Kinds of mx_bench_mma and the K one MMA instruction covers.
+MMA_KINDS = {0: ("mxf4", 64), 1: ("mxf4nvf4.2X", 64), 2: ("mxf4nvf4.4X", 64), 3: ("f8f6f4.e4m3", 32),
+             4: ("f16.bf16", 16), 5: ("mxf8f6f4.e4m3", 32)}
+
+
+def bench_mma(kind: int, cta_group: int = 1, n: int = 256, mmas_per_iter: int = 4,
+              copies_per_iter: int = 0, copy_shape: int = 0, depth: int = 0, flags: int = 0,
+              iters: int = 20000, stream=None) -> dict:
+    """Runs the tensor-core issue-rate microbenchmark once and returns the
+    per-MMA time and the implied whole-GPU rate (the slowest CTA sets it)."""
+    ns = torch.zeros(256, dtype=torch.int64, device="cuda")
+    ctas = ctypes.c_int(0)
+    _check(lib().mx_bench_mma(kind, cta_group, n, mmas_per_iter, copies_per_iter, copy_shape,
+                              depth, flags, iters, _dev_ptr(ns, "ns"), ctypes.byref(ctas), _stream(stream)),
+           "mx_bench_mma")
+    check_status(stream)
+    t = ns[:ctas.value].cpu().numpy()
+    issuing = t[::cta_group] if cta_group == 2 else t
+    if (issuing <= 0).any():
+        raise MXError(6, "mx_bench_mma: a bounded wait expired")
+    k = MMA_KINDS[kind][1]
+    mmas = mmas_per_iter * iters
+    flop_per_mma_sm = 2.0 * 128 * n * k
+    ns_per_mma = float(issuing.max()) / mmas
+    return {"kind": MMA_KINDS[kind][0], "cta_group": cta_group, "n": n, "ctas": ctas.value,
+            "mmas_per_iter": mmas_per_iter, "copies_per_iter": copies_per_iter,
+            "copy_shape": copy_shape, "depth": depth, "flags": flags, "iters": iters,
+            "ns_per_mma": ns_per_mma, "ns_per_mma_median": float(sorted(issuing)[len(issuing) // 2]) / mmas,
+            "tflops": flop_per_mma_sm * ctas.value / ns_per_mma / 1e3}

@@ -21,7 +21,8 @@ LIB = os.path.join(BUILD_DIR, "libmx.so")
 # used by the tests only.
 CHECKED_DIR = os.path.join(HERE, "_build_checked")
 CHECKED_LIB = os.path.join(CHECKED_DIR, "libmx.so")
-SOURCES = ["mx_api.cu", "mx_quant.cu", "mx_gemm.cu", "mx_noalloc.cu", "mx_scales.cu"]
+SOURCES = ["mx_api.cu", "mx_quant.cu", "mx_gemm.cu", "mx_noalloc.cu", "mx_scales.cu",
+           "mx_peak.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--expt-relaxed-constexpr", "-I", INCLUDE]

@@ -6,35 +6,36 @@
 // "Fehlerdiagnoseexperiment", run on native FP4 tensor cores with fp32
 // accumulation.
 //
-// Design (one CTA per SM, persistent over 128 x 256 output tiles):
-//   schedule     CTA b takes work items b, b + G, b + 2G, ... (G CTAs, in
-//                clusters of two).  An item is a whole tile, except in a last
-//                round that would leave at least half of the CTAs idle (tiles
-//                mod G <= G/2): there each remaining tile becomes two items,
-//                the two halves of its K range, run by the two CTAs of one
-//                cluster.  Each CTA then stores one column half of the tile:
-//                it leaves its fp32 partial of the other column half in its
-//                own shared memory (its stage ring is idle by then), reads
-//                the partner's partial of its own half through distributed
-//                shared memory, adds the two (fp32 addition of the two K
-//                halves is commutative, so both CTAs' sums are the same bits)
-//                and stores.  The last round then takes about half a tile
-//                time instead of a whole one.
-//   warp 0       TMA producer: 128B-swizzled A/B code tiles (K-tile of 256
-//                FP4 = 128 bytes per row) and the two matching 1 KB scale
-//                slabs per 128 rows, into a 4-stage shared-memory ring.
-//   warp 1       tensor-memory allocator and single-thread MMA issuer: per
-//                stage, tcgen05.cp moves the scale slabs into tensor memory,
-//                then four tcgen05.mma kind::mxf4 (K = 64 each, two E8M0
-//                scales per row per MMA) accumulate into a 128 x 256 fp32
-//                tile held in tensor memory; tcgen05.commit frees the stage.
-//   warps 2..9   epilogue: tcgen05.ld the accumulator (each warp one 32-lane
-//                quarter x 128 columns) into registers, release tensor
-//                memory to the MMA warp at once, then store fp32 rows while
-//                the next tile's main loop runs.  A CTA's last item, whose
-//                stores nothing overlaps, is staged in the idle stage ring
-//                (128-byte swizzled 32 x 32 boxes) and written by TMA stores
-//                of whole lines.
+// Design (persistent; one 2-CTA cluster per SM pair; 256 x 256 output tiles):
+//   A tile's 256 rows and B tile's 256 rows are split 128/128 between the two
+//   CTAs of the pair; tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 64) is
+//   issued by one thread of the even CTA and leaves rows 0..127 of the fp32
+//   tile in the even CTA's tensor memory and rows 128..255 in the odd one's.
+//   Each CTA thereby reads only half of B from its own shared memory.
+//
+//   warp 0       operand producer: this CTA's 128 rows of A and of B, two
+//                256-wide K sub-tiles (128-byte swizzle) per stage, into a
+//                3-stage shared-memory ring.  Both CTAs' operand loads
+//                complete on the even CTA's stage barrier.
+//   warp 2       scale producer: the stage's block scales (this CTA's A rows;
+//                all 256 B rows) on a barrier of their own, so that the scale
+//                writers start while the operands are still in flight.
+//   warp 1       tensor-memory allocation (pair); in the even CTA, the MMA
+//                issuer: per stage, 8 MMAs and one commit that frees the
+//                stage in both CTAs.
+//   warps 4..7   scale writers: warp 4+q moves the stage's block scales from
+//                shared memory into lane quarter q of its CTA's tensor memory
+//                with tcgen05.st (copy instructions would enter the MMA pipe
+//                and serialise with the MMAs), then signals the MMA thread.
+//   warps 8..15  epilogue: tcgen05.ld the CTA's 128 x 256 accumulator half
+//                (each warp one 32-lane quarter x 128 columns) into registers,
+//                release tensor memory to the MMA thread at once, then store
+//                fp32 rows.  The stores are spread over the next tile's main
+//                loop (one 32-byte store per thread per loaded stage), so that
+//                the output of all SMs does not reach L2 in one burst that
+//                would stall the operand loads.
+//   The producer, MMA and scale-writer warpgroups give up registers
+//   (setmaxnreg) so that the epilogue can hold 128 values per thread.
 // Every wait is bounded (see mx_ptx.cuh); a timeout records an error and the
 // CTA unwinds without faulting.
 #include <atomic>
@@ -49,20 +50,32 @@
 namespace mx {
 namespace {
 
-constexpr int kBM = 128;
-constexpr int kBN = 256;
-constexpr int kBKBytes = 128;                 // 256 FP4 values per row per K-tile
-constexpr int kStages = 4;
-constexpr int kThreads = 320;                 // 10 warps
+constexpr int kTile = 256;                        // output tile (rows and columns) per pair
+constexpr int kHalf = 128;                        // rows of A / of B per CTA
+constexpr int kBKBytes = 128;                     // 256 FP4 per row per K sub-tile
+constexpr int kKSub = 2;                          // K sub-tiles per stage (K = 512)
+constexpr int kStages = 3;
+constexpr int kThreads = 512;                     // 16 warps
+constexpr int kWriterWarp0 = 4;                   // warps 4..7: scale writers
+constexpr int kEpiWarp0 = 8;                      // warps 8..15: epilogue
 constexpr int kEpiWarps = 8;
-constexpr uint32_t kABytes = kBM * kBKBytes;  // 16 KB
-constexpr uint32_t kBBytes = kBN * kBKBytes;  // 32 KB
-constexpr uint32_t kSFABytes = 1024;          // 128 rows x 8 blocks
-constexpr uint32_t kSFBBytes = 2048;          // 256 rows x 8 blocks
-constexpr uint32_t kStageBytes = kABytes + kBBytes + kSFABytes + kSFBBytes;  // 52 KB
+// Register split (setmaxnreg): 512 threads x 128 launch registers =
+// 256 threads x kRegsLow (producers, MMA, scale writers) + 256 x kRegsHigh.
+constexpr int kRegsLow = 56;
+constexpr int kRegsHigh = 200;
+static_assert(256 * kRegsLow + 256 * kRegsHigh <= kThreads * 128, "register split fits the launch");
+constexpr uint32_t kSubBytes = kHalf * kBKBytes;  // 16 KB: 128 rows x one K sub-tile
+constexpr uint32_t kSFSub = 1024;                 // scales of 128 rows x one K sub-tile
+constexpr uint32_t kOffA = 0;
+constexpr uint32_t kOffB = kKSub * kSubBytes;
+constexpr uint32_t kOffSFA = 2 * kKSub * kSubBytes;
+constexpr uint32_t kOffSFB = kOffSFA + kKSub * kSFSub;           // two 128-row groups of B
+constexpr uint32_t kStageBytes = kOffSFB + 2 * kKSub * kSFSub;   // 70 KB
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCol = 0;               // accumulator: columns [0, 256)
-constexpr uint32_t kSFCol = 256;              // per-stage scale columns: 32 per stage
+constexpr uint32_t kAccCol = 0;                    // accumulator: columns [0, 256)
+constexpr uint32_t kSFCol = 256;                   // scale slots: 24 columns per K sub-tile
+constexpr uint32_t kSFSlot = 24 * kKSub;
+static_assert(kSFCol + kStages * kSFSlot <= kTmemCols, "scale slots fit in tensor memory");
 
 struct GemmArgs {
     const uint8_t *As;
@@ -70,28 +83,28 @@ struct GemmArgs {
     float *C;
     int64_t M, N, K;
     int64_t katoms;      // scale k-atoms per 128-row group
-    int64_t b_groups;    // 128-row scale groups that exist for B
-    int k_tiles;
+    int64_t a_groups;    // 128-row scale groups that exist for A
+    int64_t b_groups;    // ... and for B
+    int k_tiles;         // 256-wide K sub-tiles
+    int k_stages;        // stages per tile (ceil(k_tiles / kKSub))
     int n_tiles;
     int num_tiles;
-    int num_items;       // whole tiles [0, dp_tiles), then two K halves per remaining tile
-    int dp_tiles;
-    int k_split;         // first K-tile of a second half
     int c_v8;            // C rows allow 32-byte stores (N % 8 == 0, C 32-byte aligned)
-    int c_tma;           // C allows TMA stores (N % 4 == 0, C 16-byte aligned)
     size_t c_bytes;      // extent of C (store guards)
     int *status;
 };
 
 struct SharedCtl {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    uint64_t acc_full;
-    uint64_t acc_empty;
+    uint64_t full[kStages];      // even CTA: both CTAs' operand bytes of the stage have landed
+    uint64_t sf_full[kStages];   // this CTA's scale bytes of the stage have landed
+    uint64_t empty[kStages];     // the pair's MMAs have finished reading the stage
+    uint64_t sf_ready[kStages];  // even CTA: both CTAs' scales of the stage are in tensor memory
+    uint64_t acc_full;           // the tile's accumulator is complete
+    uint64_t acc_empty;          // even CTA: both CTAs' epilogues have read the accumulator
     uint64_t drain;
-    uint64_t part_ready;  // split tile: the partner's partial of this CTA's column half is in place
     uint32_t tmem_base;
     int abort_flag;
+    int issued;                  // stages whose operand loads this CTA has issued (monotonic)
 };
 
 __device__ __forceinline__ void st_global_v4f(float *p, uint32_t a, uint32_t b, uint32_t c,
@@ -108,290 +121,339 @@ __device__ __forceinline__ void st_global_v8(float *p, const uint32_t *v) {
                  : "memory");
 }
 
-// Work item w: output tile, K-tile range [k0, k1), and which K half it is
-// (-1: the whole range).
-struct Item {
-    int tile, k0, k1, khalf;
-};
-__device__ __forceinline__ Item item_of(const GemmArgs &g, int w) {
-    if (w < g.dp_tiles) return Item{w, 0, g.k_tiles, -1};
-    const int j = w - g.dp_tiles, h = j % 2;
-    return Item{g.dp_tiles + j / 2, h == 0 ? 0 : g.k_split, h == 0 ? g.k_split : g.k_tiles, h};
+// Arrive on the barrier `bar` of the even CTA of this pair (a local arrive in
+// the even CTA, a remote one in the odd CTA).  The arrivals here only order
+// tensor-memory work, which the tcgen05 fences around them cover.
+__device__ __forceinline__ void arrive_even(uint64_t *bar) {
+    mbar_arrive_remote(mapa_shared(smem_u32(bar), 0u));
 }
 
-// A split tile's partial of one column half: the 128 epilogue threads that
-// hold that half (4 warps) keep 128 fp32 values each, as 32 chunks of 16
-// bytes; chunk i of thread t of the half sits at (i * 128 + t) * 16, so a
-// warp's 16-byte accesses to one chunk are contiguous.
-constexpr int kHalfThreads = 16 * kEpiWarps;
-constexpr uint32_t kPartialBytes = 32u * kHalfThreads * 16u;  // 64 KB
-static_assert(kPartialBytes <= kStages * kStageBytes, "the partial lives in the stage ring");
-// TMA-store staging of a last item: per epilogue warp, four 32 x 32 fp32
-// boxes (4 KB each, 128-byte swizzle), after the partial.
-constexpr uint32_t kStageOutBytes = 4u * 4096u;
-static_assert(kPartialBytes + kEpiWarps * kStageOutBytes <= kStages * kStageBytes,
-              "the output staging lives in the stage ring");
+// Stores 32 fp32 values of one C row starting at column cc (columns past N
+// are skipped).
+__device__ __forceinline__ void store_row32(const GemmArgs &g, float *crow, int64_t cc,
+                                            const uint32_t (&v)[32]) {
+    if (g.c_v8 && cc + 31 < g.N) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (MX_STORE_OK(crow + cc + 8 * j, 32, g.C, g.c_bytes, g.status))
+                st_global_v8(crow + cc + 8 * j, &v[8 * j]);
+        return;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int64_t col = cc + 4 * j;
+        if (col + 3 < g.N) {
+            if (MX_STORE_OK(crow + col, 16, g.C, g.c_bytes, g.status))
+                st_global_v4f(crow + col, v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (col + e < g.N && MX_STORE_OK(crow + col + e, 4, g.C, g.c_bytes, g.status))
+                    crow[col + e] = __uint_as_float(v[4 * j + e]);
+        }
+    }
+}
+
+// Bounded wait until this CTA's producer has issued at least `target` stages
+// (a monotonic counter, so no phase can be mistaken for another).  Lane 0
+// polls; the warp follows.  Returns false on timeout or abort.
+__device__ __forceinline__ bool wait_issued(const SharedCtl *ctl, int target, int *status,
+                                            volatile int *abort) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) {
+        const volatile int *issued = &ctl->issued;
+        if (*issued < target) {
+            const uint64_t t0 = global_timer_ns();
+            while (*issued < target) {
+                if (*abort || global_timer_ns() - t0 > kWaitLimitNs) {
+                    if (!*abort) atomicExch(status, kDevTimeout);
+                    *abort = 1;
+                    ok = 0;
+                    break;
+                }
+                __nanosleep(64);
+            }
+        }
+    }
+    return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+}
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
-                   const __grid_constant__ CUtensorMap map_b,
-                   const __grid_constant__ CUtensorMap map_c, const GemmArgs g) {
+                   const __grid_constant__ CUtensorMap map_b, const GemmArgs g) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned base, kept as a shared-space pointer (offset arithmetic
-    // only) so that the compiler emits shared-memory loads.
+    // only) so that the compiler emits shared-memory loads.  The offset is the
+    // same in both CTAs of the pair (same kernel, same static layout).
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     SharedCtl *ctl = reinterpret_cast<SharedCtl *>(smem + kStages * kStageBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&ctl->full[s], 1);
+            mbar_init(&ctl->sf_full[s], 1);
             mbar_init(&ctl->empty[s], 1);
+            mbar_init(&ctl->sf_ready[s], 2 * 4);
         }
         mbar_init(&ctl->acc_full, 1);
-        mbar_init(&ctl->acc_empty, kEpiWarps);
+        mbar_init(&ctl->acc_empty, 2 * kEpiWarps);
         mbar_init(&ctl->drain, 1);
-        mbar_init(&ctl->part_ready, kEpiWarps / 2);
         ctl->abort_flag = 0;
+        ctl->issued = 0;
         fence_barrier_init();
         prefetch_tmap(&map_a);
         prefetch_tmap(&map_b);
-        if (g.c_tma) prefetch_tmap(&map_c);
     }
     if (warp == 1) {
-        tmem_alloc(&ctl->tmem_base, kTmemCols);
-        tmem_relinquish();
+        tmem_alloc_pair(&ctl->tmem_base, kTmemCols);
+        tmem_relinquish_pair();
     }
     tc_fence_before();
-    // Both CTAs of the cluster have initialised their barriers before either
-    // signals the other.
+    // Both CTAs of the pair have initialised their barriers (and allocated
+    // tensor memory) before either signals the other.
     __syncwarp();
     cluster_sync();
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
     volatile int *abort = &ctl->abort_flag;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            int stage = 0;
+    if (warp < kWriterWarp0) {
+        // Warpgroup 0: producers and the MMA issuer need few registers.
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow) : "memory");
+        if ((warp == 0 || warp == 2) && lane == 0) {
+            // ------------------------------------------------------------ producers
+            const bool scales = warp == 2;
+            int stage = 0, n_issued = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int w = blockIdx.x; ok && w < g.num_items; w += gridDim.x) {
-                const Item it = item_of(g, w);
-                const int mb = it.tile / g.n_tiles, nb = it.tile % g.n_tiles;
-                for (int kt = it.k0; kt < it.k1; ++kt) {
-                    if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, g.status, abort)) {
+            for (int tile = pair; ok && tile < g.num_tiles; tile += npairs) {
+                const int mb = tile / g.n_tiles, nb = tile % g.n_tiles;
+                const int64_t ga = 2 * static_cast<int64_t>(mb) + rank;  // this CTA's A scale group
+                for (int ks = 0; ks < g.k_stages; ++ks) {
+                    if (!mbar_wait_inl(&ctl->empty[stage], phase ^ 1u, g.status, abort)) {
                         ok = false;
                         break;
                     }
-                    uint8_t *sa = smem + stage * kStageBytes;
-                    uint8_t *sb = sa + kABytes;
-                    uint8_t *sfa = sb + kBBytes;
-                    uint8_t *sfb = sfa + kSFABytes;
-                    const int64_t g0 = 2 * static_cast<int64_t>(nb);
-                    const uint32_t nsfb = (g0 + 1 < g.b_groups) ? 2u : 1u;
-                    mbar_arrive_expect_tx(&ctl->full[stage],
-                                          kABytes + kBBytes + kSFABytes + nsfb * 1024u);
-                    tma_load_2d(sa, &map_a, &ctl->full[stage], kt * kBKBytes, mb * kBM);
-                    tma_load_2d(sb, &map_b, &ctl->full[stage], kt * kBKBytes, nb * kBN);
-                    bulk_load(sfa, g.As + (static_cast<int64_t>(mb) * g.katoms + 2 * kt) * 512,
-                              1024u, &ctl->full[stage]);
-                    for (uint32_t rb = 0; rb < nsfb; ++rb)
-                        bulk_load(sfb + rb * 1024u,
-                                  g.Bs + ((g0 + rb) * g.katoms + 2 * kt) * 512, 1024u,
-                                  &ctl->full[stage]);
+                    const int kt0 = ks * kKSub;
+                    const int nsub = g.k_tiles - kt0 < kKSub ? g.k_tiles - kt0 : kKSub;
+                    uint8_t *st = smem + stage * kStageBytes;
+                    if (scales) {
+                        uint32_t bytes = 0;
+                        if (ga < g.a_groups) bytes += static_cast<uint32_t>(nsub) * kSFSub;
+                        for (int rb = 0; rb < 2; ++rb)
+                            if (2 * static_cast<int64_t>(nb) + rb < g.b_groups)
+                                bytes += static_cast<uint32_t>(nsub) * kSFSub;
+                        mbar_arrive_expect_tx(&ctl->sf_full[stage], bytes);
+                        if (ga < g.a_groups)
+                            bulk_load(st + kOffSFA, g.As + (ga * g.katoms + 2 * kt0) * 512,
+                                      static_cast<uint32_t>(nsub) * kSFSub, &ctl->sf_full[stage]);
+                        for (int rb = 0; rb < 2; ++rb) {
+                            const int64_t gb = 2 * static_cast<int64_t>(nb) + rb;
+                            if (gb < g.b_groups)
+                                bulk_load(st + kOffSFB + rb * kKSub * kSFSub,
+                                          g.Bs + (gb * g.katoms + 2 * kt0) * 512,
+                                          static_cast<uint32_t>(nsub) * kSFSub, &ctl->sf_full[stage]);
+                        }
+                    } else {
+                        // Both CTAs' operand loads complete on the even CTA's
+                        // barrier, which the even CTA arms with the pair's bytes
+                        // (boxes partly or wholly outside the operand still count
+                        // in full; the TMA fills them with zeros).
+                        if (rank == 0)
+                            mbar_arrive_expect_tx(&ctl->full[stage],
+                                                  static_cast<uint32_t>(nsub) * 4u * kSubBytes);
+                        const uint32_t full_even = mapa_shared(smem_u32(&ctl->full[stage]), 0u);
+                        for (int u = 0; u < nsub; ++u) {
+                            tma_load_2d_pair(st + kOffA + u * kSubBytes, &map_a, full_even,
+                                             (kt0 + u) * kBKBytes, mb * kTile + kHalf * rank);
+                            tma_load_2d_pair(st + kOffB + u * kSubBytes, &map_b, full_even,
+                                             (kt0 + u) * kBKBytes, nb * kTile + kHalf * rank);
+                        }
+                        *reinterpret_cast<volatile int *>(&ctl->issued) = ++n_issued;
+                    }
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        } else if (warp == 1 && lane == 0 && rank == 0) {
+            // ------------------------------------------------------------ MMA issuer
             int stage = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            for (int w = blockIdx.x; ok && w < g.num_items; w += gridDim.x) {
-                const Item it = item_of(g, w);
-                if (!mbar_wait(&ctl->acc_empty, acc_phase ^ 1u, g.status, abort)) break;
+            const uint32_t idesc0 = idesc_mxf4(2 * kHalf, kTile, 0, 0);
+            const uint32_t idesc2 = idesc_mxf4(2 * kHalf, kTile, 2, 2);
+            for (int tile = pair; ok && tile < g.num_tiles; tile += npairs) {
+                if (!mbar_wait_inl(&ctl->acc_empty, acc_phase ^ 1u, g.status, abort)) break;
                 tc_fence_after();
-                for (int kt = it.k0; kt < it.k1; ++kt) {
-                    if (!mbar_wait(&ctl->full[stage], phase, g.status, abort)) {
+                for (int ks = 0; ks < g.k_stages; ++ks) {
+                    if (!mbar_wait_inl(&ctl->sf_ready[stage], phase, g.status, abort) ||
+                        !mbar_wait_inl(&ctl->full[stage], phase, g.status, abort)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + stage * kStageBytes);
-                    const uint32_t sb = sa + kABytes;
-                    const uint32_t sfa = sb + kBBytes;
-                    const uint32_t sfb = sfa + kSFABytes;
-                    const uint32_t sf_col = tmem + kSFCol + 32u * stage;
-                    // Scale slabs -> tensor memory.  A: 4 columns per k-atom.
-                    // B: per k-atom, 4 columns per 128-row group (rows 128..255
-                    // of the 256-row tile follow rows 0..127).
+                    const int kt0 = ks * kKSub;
+                    const int nsub = g.k_tiles - kt0 < kKSub ? g.k_tiles - kt0 : kKSub;
+                    const uint32_t sbase = smem_u32(smem + stage * kStageBytes);
+                    const uint32_t slot = tmem + kSFCol + kSFSlot * static_cast<uint32_t>(stage);
+                    for (int u = 0; u < nsub; ++u) {
+                        const uint32_t sa = sbase + kOffA + u * kSubBytes;
+                        const uint32_t sb = sbase + kOffB + u * kSubBytes;
+                        const uint32_t sf = slot + 24u * static_cast<uint32_t>(u);
 #pragma unroll
-                    for (int ka = 0; ka < 2; ++ka) {
-                        tmem_cp_32x128b_x4(sf_col + 4u * ka, sdesc_sf(sfa + 512u * ka));
-#pragma unroll
-                        for (int rb = 0; rb < 2; ++rb)
-                            tmem_cp_32x128b_x4(sf_col + 8u + 8u * ka + 4u * rb,
-                                               sdesc_sf(sfb + 1024u * rb + 512u * ka));
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t ka = static_cast<uint32_t>(j / 2);
+                            mma_mxf4_pair(tmem + kAccCol, sdesc_sw128(sa + 32u * j),
+                                          sdesc_sw128(sb + 32u * j), (j & 1) ? idesc2 : idesc0,
+                                          sf + 4u * ka, sf + 8u + 8u * ka,
+                                          (ks > 0 || u > 0 || j > 0) ? 1u : 0u);
+                        }
                     }
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int ka = j / 2, sf_id = (j % 2) * 2;
-                        mma_mxf4(tmem + kAccCol, sdesc_sw128(sa + 32u * j),
-                                 sdesc_sw128(sb + 32u * j), idesc_mxf4(kBM, kBN, sf_id, sf_id),
-                                 sf_col + 4u * ka, sf_col + 8u + 8u * ka,
-                                 (kt > it.k0 || j > 0) ? 1u : 0u);
-                    }
-                    tc_commit(&ctl->empty[stage]);
+                    tc_commit_pair(&ctl->empty[stage], 0x3);
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
-                tc_commit(&ctl->acc_full);
+                tc_commit_pair(&ctl->acc_full, 0x3);
                 acc_phase ^= 1u;
             }
-            // Make sure every tensor-core operation issued here has finished
-            // before tensor memory is released.
-            tc_commit(&ctl->drain);
-            mbar_wait(&ctl->drain, 0, g.status, nullptr, 100ull * 1000ull * 1000ull);
+            // Every tensor-core operation issued here has finished before
+            // either CTA releases its tensor memory.
+            tc_commit_pair(&ctl->drain, 0x1);
+            mbar_wait_inl(&ctl->drain, 0, g.status, nullptr, 100ull * 1000ull * 1000ull);
+        }
+    } else if (warp < kEpiWarp0) {
+        // ------------------------------------------------------------ scale writers
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow) : "memory");
+        // Tensor-memory scale layout of one K sub-tile (24 columns, as the
+        // tcgen05.mma block-scale path reads it), the same in every lane
+        // quarter q: for k-atom ka (4 blocks of 32), A row 32*c + r of this
+        // CTA at lane 32q + r, column 4*ka + c (the quarter's own rows are at
+        // c = q); B row 128*rb + 32*c + r (all 256 rows) at lane 32q + r,
+        // column 8 + 8*ka + 4*rb + c; byte b of a column is block 4*ka + b.
+        // A lane reads its 16-byte row of each 512-byte scale atom, which
+        // holds exactly those four rows.
+        const int q = warp & 3;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int tile = pair; tile < g.num_tiles; tile += npairs) {
+            bool ok = true;
+            for (int ks = 0; ks < g.k_stages; ++ks) {
+                int okw = 1;
+                if (lane == 0)
+                    okw = mbar_wait_inl(&ctl->sf_full[stage], phase, g.status, abort) ? 1 : 0;
+                okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+                if (!okw) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int kt0 = ks * kKSub;
+                const int nsub = g.k_tiles - kt0 < kKSub ? g.k_tiles - kt0 : kKSub;
+                const uint8_t *st = smem + stage * kStageBytes;
+                const uint32_t slot =
+                    lane_base + kSFCol + kSFSlot * static_cast<uint32_t>(stage);
+                for (int u = 0; u < nsub; ++u) {
+                    const uint8_t *sfa = st + kOffSFA + u * kSFSub;
+                    const uint8_t *sfb = st + kOffSFB + u * kSFSub;
+                    uint32_t a[8], b[16];
+#pragma unroll
+                    for (int ka = 0; ka < 2; ++ka) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(sfa + ka * 512 + lane * 16);
+                        a[4 * ka + 0] = v.x;
+                        a[4 * ka + 1] = v.y;
+                        a[4 * ka + 2] = v.z;
+                        a[4 * ka + 3] = v.w;
+                    }
+#pragma unroll
+                    for (int ka = 0; ka < 2; ++ka)
+#pragma unroll
+                        for (int rb = 0; rb < 2; ++rb) {
+                            const uint4 v = *reinterpret_cast<const uint4 *>(
+                                sfb + rb * kKSub * kSFSub + ka * 512 + lane * 16);
+                            b[8 * ka + 4 * rb + 0] = v.x;
+                            b[8 * ka + 4 * rb + 1] = v.y;
+                            b[8 * ka + 4 * rb + 2] = v.z;
+                            b[8 * ka + 4 * rb + 3] = v.w;
+                        }
+                    const uint32_t col = slot + 24u * static_cast<uint32_t>(u);
+                    tmem_st_32x32b_x8(col, a);
+                    tmem_st_32x32b_x16(col + 8u, b);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) arrive_even(&ctl->sf_ready[stage]);
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int q = warp & 3;           // TMEM lane quarter this warp may access
-        const int half = (warp - 2) / 4;  // column half of the 256-wide tile
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh) : "memory");
+        const int q = warp & 3;                   // TMEM lane quarter this warp may access
+        const int half = (warp - kEpiWarp0) / 4;  // column half of the 256-wide tile
         uint32_t acc_phase = 0;
-        const int ht = ((warp - 2) & 3) * 32 + lane;  // thread index within its column half
-        for (int w = blockIdx.x; w < g.num_items; w += gridDim.x) {
-            const Item it = item_of(g, w);
-            const int mb = it.tile / g.n_tiles, nb = it.tile % g.n_tiles;
+        int done = 0;                             // tiles of this pair finished
+        for (int tile = pair; tile < g.num_tiles; tile += npairs, ++done) {
+            const int mb = tile / g.n_tiles, nb = tile % g.n_tiles;
             // One lane waits; the verdict is broadcast so the warp stays
             // converged for the .sync.aligned tensor-memory loads.
             int ok = 1;
-            if (lane == 0) ok = mbar_wait(&ctl->acc_full, acc_phase, g.status, abort) ? 1 : 0;
+            if (lane == 0) ok = mbar_wait_inl(&ctl->acc_full, acc_phase, g.status, abort) ? 1 : 0;
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             if (!ok) break;
             tc_fence_after();
-            uint32_t v[4][32];
+            acc_phase ^= 1u;
             const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + kAccCol +
-                                   128u * half;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(tbase + 32u * c, v[c]);
+                                   128u * static_cast<uint32_t>(half);
+            uint32_t v0[32], v1[32], v2[32], v3[32];
+            tmem_ld_32x32b_x32(tbase, v0);
+            tmem_ld_32x32b_x32(tbase + 32u, v1);
+            tmem_ld_32x32b_x32(tbase + 64u, v2);
+            tmem_ld_32x32b_x32(tbase + 96u, v3);
             tmem_ld_wait();
+            // The accumulator is in registers: the next tile may start.
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->acc_empty);
-            acc_phase ^= 1u;
+            if (lane == 0) arrive_even(&ctl->acc_empty);
 
-            if (it.khalf >= 0) {
-                // Split tile: CTA rank r (= it.khalf) stores column half r.
-                if (half != it.khalf) {
-                    // Leave this half's partial for the partner and signal it.
+            const int64_t row =
+                static_cast<int64_t>(mb) * kTile + kHalf * rank + 32 * q + lane;
+            float *crow = g.C + row * g.N;
+            const int64_t col0 = static_cast<int64_t>(nb) * kTile + 128 * half;
+            const bool more = tile + npairs < g.num_tiles;
+            if (more && g.c_v8 && col0 + 127 < g.N) {
+                // Store chunk j (8 values) once the producer has issued stage
+                // 1 + j * k_stages / 16 of the next tile.
+                const int base = (done + 1) * g.k_stages;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            uint4 *dst = reinterpret_cast<uint4 *>(
-                                smem + (static_cast<uint32_t>((8 * c + j) * kHalfThreads + ht) << 4));
-                            *dst = make_uint4(v[c][4 * j], v[c][4 * j + 1], v[c][4 * j + 2],
-                                              v[c][4 * j + 3]);
-                        }
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->part_ready), 1u - it.khalf));
-                    continue;
+                for (int j = 0; j < 16; ++j) {
+                    const int need = 1 + (j * g.k_stages) / 16;
+                    if (j == 0 || need != 1 + ((j - 1) * g.k_stages) / 16)
+                        if (!wait_issued(ctl, base + need, g.status, abort)) break;
+                    const uint32_t *src = j < 4    ? &v0[8 * j]
+                                          : j < 8  ? &v1[8 * (j - 4)]
+                                          : j < 12 ? &v2[8 * (j - 8)]
+                                                   : &v3[8 * (j - 12)];
+                    if (row < g.M && MX_STORE_OK(crow + col0 + 8 * j, 32, g.C, g.c_bytes, g.status))
+                        st_global_v8(crow + col0 + 8 * j, src);
                 }
-                int okp = 1;
-                if (lane == 0) okp = mbar_wait_cluster(&ctl->part_ready, 0, g.status, abort) ? 1 : 0;
-                okp = __shfl_sync(0xFFFFFFFFu, okp, 0);
-                if (!okp) break;
-                // Every lane takes the acquire itself (the phase is complete).
-                mbar_wait_cluster(&ctl->part_ready, 0, g.status, abort);
-                const uint32_t peer = mapa_shared(smem_u32(smem), 1u - it.khalf);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint4 p[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        p[j] = ld_shared_cluster_v4(
-                            peer + (static_cast<uint32_t>((8 * c + j) * kHalfThreads + ht) << 4));
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        v[c][4 * j] = __float_as_uint(__uint_as_float(v[c][4 * j]) + __uint_as_float(p[j].x));
-                        v[c][4 * j + 1] =
-                            __float_as_uint(__uint_as_float(v[c][4 * j + 1]) + __uint_as_float(p[j].y));
-                        v[c][4 * j + 2] =
-                            __float_as_uint(__uint_as_float(v[c][4 * j + 2]) + __uint_as_float(p[j].z));
-                        v[c][4 * j + 3] =
-                            __float_as_uint(__uint_as_float(v[c][4 * j + 3]) + __uint_as_float(p[j].w));
-                    }
-                }
-            }
-
-            if (g.c_tma && w + static_cast<int>(gridDim.x) >= g.num_items) {
-                // Last item: stage this warp's 32 rows x 128 columns as four
-                // swizzled boxes and store them with TMA (rows and columns
-                // outside C are not written).
-                uint8_t *stg = smem + kPartialBytes + static_cast<uint32_t>(warp - 2) * kStageOutBytes;
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(
-                            stg + c * 4096 + lane * 128 + (((j ^ (lane & 7)) & 7) << 4));
-                        *dst = make_uint4(v[c][4 * j], v[c][4 * j + 1], v[c][4 * j + 2],
-                                          v[c][4 * j + 3]);
-                    }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    const int32_t r0 = mb * kBM + 32 * q;
-                    const int32_t cb = nb * kBN + 128 * half;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        if (cb + 32 * c < g.N && r0 < g.M)  // boxes that start inside C only
-                            tma_store_2d(&map_c, stg + c * 4096, cb + 32 * c, r0);
-                    bulk_commit_group();
-                    bulk_wait_group_0();
-                }
-                __syncwarp();
-                continue;
-            }
-            const int64_t row = static_cast<int64_t>(mb) * kBM + 32 * q + lane;
-            if (row < g.M) {
-                float *crow = g.C + row * g.N;
-                const int64_t col0 = static_cast<int64_t>(nb) * kBN + 128 * half;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    if (g.c_v8 && col0 + 32 * c + 31 < g.N) {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            if (MX_STORE_OK(crow + col0 + 32 * c + 8 * j, 32, g.C, g.c_bytes, g.status))
-                                st_global_v8(crow + col0 + 32 * c + 8 * j, &v[c][8 * j]);
-                        continue;
-                    }
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int64_t col = col0 + 32 * c + 4 * j;
-                        if (col + 3 < g.N) {
-                            if (MX_STORE_OK(crow + col, 16, g.C, g.c_bytes, g.status))
-                                st_global_v4f(crow + col, v[c][4 * j], v[c][4 * j + 1],
-                                              v[c][4 * j + 2], v[c][4 * j + 3]);
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                if (col + e < g.N &&
-                                    MX_STORE_OK(crow + col + e, 4, g.C, g.c_bytes, g.status))
-                                    crow[col + e] = __uint_as_float(v[c][4 * j + e]);
-                        }
-                    }
-                }
+            } else if (row < g.M) {
+                store_row32(g, crow, col0, v0);
+                store_row32(g, crow, col0 + 32, v1);
+                store_row32(g, crow, col0 + 64, v2);
+                store_row32(g, crow, col0 + 96, v3);
             }
         }
     }
@@ -399,13 +461,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    // Neither CTA of a cluster leaves while the other may still read its
-    // shared memory.
+    // Neither CTA of the pair releases tensor memory (or leaves) while the
+    // other's operations may still touch it.
     __syncwarp();
     cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc_pair(tmem, kTmemCols);
     }
 }
 
@@ -434,12 +496,12 @@ int gemm_clusters(const DeviceInfo &dev) {
 cudaError_t launch_gemm(const void *Aq, const void *As, const void *Bq, const void *Bs, float *C,
                         int64_t M, int64_t N, int64_t K, const DeviceInfo &dev,
                         cudaStream_t stream) {
-    CUtensorMap map_a, map_b, map_c;
-    if (!encode_tmap_2d(&map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, Aq, K / 2, M, K / 2, kBKBytes, kBM,
-                        CU_TENSOR_MAP_SWIZZLE_128B))
+    CUtensorMap map_a, map_b;
+    if (!encode_tmap_2d(&map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, Aq, K / 2, M, K / 2, kBKBytes,
+                        kHalf, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    if (!encode_tmap_2d(&map_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, Bq, K / 2, N, K / 2, kBKBytes, kBN,
-                        CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!encode_tmap_2d(&map_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, Bq, K / 2, N, K / 2, kBKBytes,
+                        kHalf, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     GemmArgs g{};
     g.As = static_cast<const uint8_t *>(As);
@@ -449,41 +511,26 @@ cudaError_t launch_gemm(const void *Aq, const void *As, const void *Bq, const vo
     g.N = N;
     g.K = K;
     g.katoms = scale_katoms(K);
+    g.a_groups = scale_groups(M);
     g.b_groups = scale_groups(N);
     g.k_tiles = static_cast<int>((K + 255) / 256);
-    const int64_t m_tiles = (M + kBM - 1) / kBM;
-    const int64_t n_tiles = (N + kBN - 1) / kBN;
+    g.k_stages = (g.k_tiles + kKSub - 1) / kKSub;
+    const int64_t m_tiles = (M + kTile - 1) / kTile;
+    const int64_t n_tiles = (N + kTile - 1) / kTile;
     if (m_tiles * n_tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
     g.n_tiles = static_cast<int>(n_tiles);
     g.num_tiles = static_cast<int>(m_tiles * n_tiles);
     g.c_v8 = (N % 8 == 0 && (reinterpret_cast<uintptr_t>(C) & 31) == 0) ? 1 : 0;
-    std::memset(&map_c, 0, sizeof(map_c));
-    g.c_tma = (N % 4 == 0 && (reinterpret_cast<uintptr_t>(C) & 15) == 0 &&
-               encode_tmap_2d(&map_c, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M,
-                              static_cast<uint64_t>(N) * sizeof(float), 32, 32,
-                              CU_TENSOR_MAP_SWIZZLE_128B))
-                  ? 1
-                  : 0;
     g.c_bytes = static_cast<size_t>(M) * static_cast<size_t>(N) * sizeof(float);
     g.status = dev.status;
     cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kGemmSmem));
     if (e != cudaSuccess) return e;
-    // Resident CTAs: as many 2-CTA clusters as fit at once.
-    const int slots = 2 * gemm_clusters(dev);
-    if (slots < 2) return cudaErrorLaunchOutOfResources;
-    const int rem = g.num_tiles % slots;
-    g.dp_tiles = g.num_tiles;
-    g.num_items = g.num_tiles;
-    g.k_split = g.k_tiles;
-    if (rem > 0 && 2 * rem <= slots && g.k_tiles >= 2) {
-        g.dp_tiles = g.num_tiles - rem;
-        g.num_items = g.dp_tiles + 2 * rem;
-        g.k_split = g.k_tiles / 2;
-    }
-    int grid = g.num_items < slots ? g.num_items : slots;
-    grid += grid & 1;
-    mx_gemm_kernel<<<grid, kThreads, kGemmSmem, stream>>>(map_a, map_b, map_c, g);
+    // Resident CTAs: as many 2-CTA clusters as fit at once, one tile per pair.
+    const int pairs_max = gemm_clusters(dev);
+    if (pairs_max < 1) return cudaErrorLaunchOutOfResources;
+    const int pairs = g.num_tiles < pairs_max ? g.num_tiles : pairs_max;
+    mx_gemm_kernel<<<2 * pairs, kThreads, kGemmSmem, stream>>>(map_a, map_b, g);
     return cudaGetLastError();
 }
 
