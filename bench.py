@@ -2,11 +2,13 @@
 """Benchmark of the MXFP4 Wgrad hot path on one GB300.
 
 Metric: MXFP4 Wgrad TFLOP/s including the Hadamard rotation and quantisation,
-2*N*K*T / step time, on the Llama-3.1-8B attention o_proj shape (T = 8192
-tokens, dY [8192, 4096], X [8192, 4096] -> dW [4096, 4096] fp32), deterministic
-block Hadamard of 32 along T, round-to-nearest-even.  Inputs are synthetic
-(seeded; Student-t(3) gradients with std 1e-3, N(0,1) activations with 1% x20
-outlier channels) and resident in HBM when the timed region starts.
+2*N*K*T / step time, on the largest single-GPU Llama-3.1-8B Wgrad shape, the
+FFN down_proj (T = 8192 tokens, dY [8192, 4096], X [8192, 14336] -> dW
+[4096, 14336] fp32), deterministic block Hadamard of 32 along T,
+round-to-nearest-even.  The attention o_proj shape (N = K = 4096) is timed
+beside it.  Inputs are synthetic (seeded; Student-t(3) gradients with std
+1e-3; SiLU(g)*u activations for down_proj, N(0,1) with 1% x20 outlier
+channels for o_proj) and resident in HBM when the timed region starts.
 
 One step = the two launches of the hot path through the C ABI:
 mx_quantize_pair(dY, X) (both operands rotated and encoded in one launch) and
@@ -185,26 +187,47 @@ def mode_text():
     return f"{rot} along T, {MODE['round'].upper()}, seed {MODE['seed']}"
 
 
-def oracle_sample(d, T, N, K, s_lines, seed=0):
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def oracle_sample(d, T, N, K, s_lines, seed=0, cores=1):
     """One bounded oracle sample: encode s_lines lines of each operand over the
-    full T and contract them (s_lines^2 outputs).  Returns (seconds, flops)."""
+    full T and contract them (s_lines^2 outputs).  With cores > 1 the oracle's
+    calls are partitioned over threads (its C code releases the GIL): the
+    encode by lines, the double GEMM by output rows; the arithmetic is the
+    oracle's own.  Returns (seconds, flops)."""
     import numpy as np
+    from concurrent.futures import ThreadPoolExecutor
     import oracle
     rng = np.random.default_rng(seed)
     la = np.sort(rng.choice(N, s_lines, replace=False))
     lb = np.sort(rng.choice(K, s_lines, replace=False))
-    t0 = time.perf_counter()
     rot, nb, rnd, qseed = mode_args()
-    Aq, As = oracle.quantize(d["dY"], oracle.CONTRACT_ROWS, rot, nb, rnd, qseed, 1, lines=la)
-    Bq, Bs = oracle.quantize(d["X"], oracle.CONTRACT_ROWS, rot, nb, rnd, qseed, 2, lines=lb)
-    oracle.gemm(Aq, As, Bq, Bs)
+    parts = max(1, min(cores, s_lines))
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(parts) as ex:
+        qa = list(ex.map(lambda ln: oracle.quantize(d["dY"], oracle.CONTRACT_ROWS, rot, nb, rnd,
+                                                    qseed, 1, lines=ln),
+                         np.array_split(la, parts)))
+        qb = list(ex.map(lambda ln: oracle.quantize(d["X"], oracle.CONTRACT_ROWS, rot, nb, rnd,
+                                                    qseed, 2, lines=ln),
+                         np.array_split(lb, parts)))
+        Aq, As = np.concatenate([a[0] for a in qa]), np.concatenate([a[1] for a in qa])
+        Bq, Bs = np.concatenate([b[0] for b in qb]), np.concatenate([b[1] for b in qb])
+        edges = np.linspace(0, s_lines, parts + 1).astype(int)
+        list(ex.map(lambda i: oracle.gemm_rows(Aq, As, Bq, Bs, int(edges[i]), int(edges[i + 1])),
+                    range(parts)))
     return time.perf_counter() - t0, 2.0 * s_lines * s_lines * T
 
 
-def calibrate_sample(d, T, N, K, budget_s):
+def calibrate_sample(d, T, N, K, budget_s, cores=1):
     """Lines per operand so that one oracle sample takes about budget_s
     (the contraction, quadratic in the lines, dominates the cost)."""
-    dt, _ = oracle_sample(d, T, N, K, 64)
+    dt, _ = oracle_sample(d, T, N, K, 64, cores=cores)
     s = int(64 * (budget_s / max(dt, 1e-6)) ** 0.5) // 16 * 16
     return max(16, min(s, N, K))
 
@@ -217,26 +240,29 @@ def run_reference(args, world, rank):
     d = config_inputs(cfg, seed=0, only=("dY", "X"))
     total_budget = args.ref_budget_s
     per_step = max(0.01, total_budget / max(1, args.steps + args.warmup))
-    s = calibrate_sample(d, T, N, K, per_step)
+    cores = host_cores()
+    s = calibrate_sample(d, T, N, K, per_step, cores)
     for i in range(args.warmup):
-        oracle_sample(d, T, N, K, s, seed=100 + i)
+        oracle_sample(d, T, N, K, s, seed=100 + i, cores=cores)
     times, flops = [], 0.0
     for i in range(args.steps):
-        dt, f = oracle_sample(d, T, N, K, s, seed=i)
+        dt, f = oracle_sample(d, T, N, K, s, seed=i, cores=cores)
         times.append(dt)
         flops += f
     tot = sum(times)
     value = flops / tot / 1e12
     sample = (f"per step: {s} lines of dY and {s} lines of X (full T={T}) encoded with "
-              f"{mode_text()}, then their {s}x{s} block of dW contracted in double")
+              f"{mode_text()}, then their {s}x{s} block of dW contracted in double; the "
+              f"oracle's calls partitioned over {cores} host threads (encode by lines, "
+              f"GEMM by output rows)")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
             "data": "synthetic",
             "config": workload_config(args, T, N, K),
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -330,11 +356,13 @@ def run_mine(args, world, rank, local):
     # input copy and step i-1's output copy overlap step i's compute, as in a
     # training loop that streams its layers.  The serial time (one step at a
     # time on one stream) is reported beside it.
-    ws = torch.empty(mx.linear_workspace_bytes(mx.OP_WGRAD, T, N, K), dtype=torch.uint8, device=dev)
-    dW_h = [torch.empty((N, K), dtype=torch.float32).pin_memory() for _ in range(2)]
-    dY_d = [torch.empty_like(dY) for _ in range(2)]
-    X_d = [torch.empty_like(X) for _ in range(2)]
-    dW_d = [dW, torch.empty_like(dW)]
+    if not args.no_e2e:
+        ws = torch.empty(mx.linear_workspace_bytes(mx.OP_WGRAD, T, N, K), dtype=torch.uint8,
+                         device=dev)
+        dW_h = [torch.empty((N, K), dtype=torch.float32).pin_memory() for _ in range(2)]
+        dY_d = [torch.empty_like(dY) for _ in range(2)]
+        X_d = [torch.empty_like(X) for _ in range(2)]
+        dW_d = [dW, torch.empty_like(dW)]
     n_e2e = max(3, min(n, args.e2e_steps))
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     s_cmp = stream
@@ -378,17 +406,27 @@ def run_mine(args, world, rank, local):
         torch.cuda.synchronize(dev)
         return t0.elapsed_time(t1)
 
-    e2e_run(2, True)                                 # warm-up
-    e2e_ms = reduce_max(e2e_run(n_e2e, True), world, dev)
-    serial_ms = e2e_run(n_e2e, False)
-    mx.check_status()
-    e2e_value = world * n_e2e * flops_step / (e2e_ms * 1e-3) / 1e12
+    e2e_value = e2e_ms = serial_ms = None
+    if not args.no_e2e:
+        e2e_run(2, True)                                 # warm-up
+        e2e_ms = reduce_max(e2e_run(n_e2e, True), world, dev)
+        serial_ms = e2e_run(n_e2e, False)
+        mx.check_status()
+        e2e_value = world * n_e2e * flops_step / (e2e_ms * 1e-3) / 1e12
 
     # side measurement: the dual-output encode of dY (both backward encodings
     # from one read) against the two single-direction encodes it replaces
     dual = None
     if rank == 0 and not args.no_extras:
         dual = measure_dual(L, mx, dY, T, N, flush, stream, dev, hbm_gbs=load_peaks()[0]["hbm_gbs"])
+
+    # the tensor cores' own MXFP4 rate on this GPU (issue-rate microbenchmark)
+    # and the o_proj shape beside the headline workload
+    fp4_meas = measure_fp4_peak(mx) if rank == 0 else None
+    side = None
+    if rank == 0 and not args.no_extras and args.workload != "o_proj":
+        side = measure_side_workload(L, mx, "o_proj", dev, stream, flush, min(n, 300),
+                                     args.warmup, fp4_meas)
 
     # parity spot check of the timed output (oracle entries, rank 0 only)
     parity = None
@@ -413,13 +451,16 @@ def run_mine(args, world, rank, local):
             return hit[1]
         return None
 
+    g_ach = flops_step / (t_g * 1e-3) / 1e12
     gemm_rf = {"kernel": "mx_gemm_kernel", "bound": "tensor",
-               "achieved": flops_step / (t_g * 1e-3) / 1e12,
+               "achieved": g_ach,
                "peak": fp4_peak, "unit": "TFLOP/s",
-               "frac": flops_step / (t_g * 1e-3) / 1e12 / fp4_peak,
+               "frac": g_ach / fp4_peak,
                "traffic": tr("mx_gemm_kernel", "mx_gemm.cu"),
                "peak_basis": f"{peak_src} bf16 burst {peaks['bf16_tflops']} TFLOP/s x nominal "
                              f"fp4/bf16 ratio {NOMINAL_FP4_OVER_BF16:g}",
+               "peak_fp4_measured": fp4_meas["tflops"],
+               "frac_fp4_measured": g_ach / fp4_meas["tflops"],
                "ms_per_launch": t_g}
     quant_rf = {"kernel": "mxq_colwise_kernel", "bound": "hbm",
                 "achieved": (q_bytes_n + q_bytes_k) / (t_q * 1e-3) / 1e9,
@@ -432,31 +473,38 @@ def run_mine(args, world, rank, local):
     clk = clocks.summary()
     cpu = None
     if not args.no_cpu_baseline:
-        s = calibrate_sample(d, T, N, K, args.cpu_budget_s)
-        dt, f = oracle_sample(d, T, N, K, s)
-        cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+        cores = host_cores()
+        s = calibrate_sample(d, T, N, K, args.cpu_budget_s, cores)
+        dt, f = oracle_sample(d, T, N, K, s, cores=cores)
+        cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                "sample": f"{s} lines of dY and {s} lines of X (full T={T}) encoded "
                          f"({mode_text()}), then their {s}x{s} block of dW contracted "
-                         f"in double; {dt:.1f} s single-threaded"}
+                         f"in double; the oracle's calls partitioned over {cores} host "
+                         f"threads (encode by lines, GEMM by output rows); {dt:.1f} s"}
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": n, "warmup": args.warmup, "ms_per_step": total_ms / n,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "mxfp4 (e2m1 x e8m0, fp32 accumulate)", "data": "synthetic",
             "config": workload_config(args, T, N, K),
             "roofline": {k: dominant[k] for k in ("bound", "achieved", "peak", "unit", "frac",
-                                                   "traffic")},
+                                                   "traffic", "peak_fp4_measured",
+                                                   "frac_fp4_measured") if k in dominant},
             "roofline_kernels": [gemm_rf, quant_rf],
             "fp4_peak_fraction": value / fp4_peak,
+            "fp4_peak_measured": fp4_meas,
+            "fp4_measured_fraction": value / fp4_meas["tflops"],
+            "o_proj": side,
             "breakdown_ms": {"quantize_pair": t_q, "gemm": t_g},
             "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": dY_h.numel() * 2 + X_h.numel() * 2,
-                    "d2h_bytes_per_step": dW_h[0].numel() * 4,
-                    "ms_per_step": e2e_ms / n_e2e, "call": "mx_linear_wgrad",
-                    "schedule": "steps pipelined over input-copy / compute / output-copy "
-                                "streams, two device buffer sets",
-                    "serial_ms_per_step": serial_ms / n_e2e,
-                    "serial_value": world * n_e2e * flops_step / (serial_ms * 1e-3) / 1e12},
+            "e2e": None if e2e_ms is None else {
+                "value": e2e_value, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": dY_h.numel() * 2 + X_h.numel() * 2,
+                "d2h_bytes_per_step": dW_h[0].numel() * 4,
+                "ms_per_step": e2e_ms / n_e2e, "call": "mx_linear_wgrad",
+                "schedule": "steps pipelined over input-copy / compute / output-copy "
+                            "streams, two device buffer sets",
+                "serial_ms_per_step": serial_ms / n_e2e,
+                "serial_value": world * n_e2e * flops_step / (serial_ms * 1e-3) / 1e12},
             "gpu_launches": 2 * n,
             "dual_quantiser": dual,
             "clocks": clk,
@@ -466,6 +514,76 @@ def run_mine(args, world, rank, local):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def measure_fp4_peak(mx, reps=3):
+    """All-SM issue rate of the GEMM's own instruction,
+    tcgen05.mma.cta_group::2.kind::mxf4.block_scale (M=256, N=256, K=64), on
+    operands resident in shared memory (mx_bench_mma); best of `reps`."""
+    best = None
+    for _ in range(reps):
+        r = mx.bench_mma(kind=0, cta_group=2, n=256, mmas_per_iter=4, iters=20000)
+        if best is None or r["tflops"] > best["tflops"]:
+            best = r
+    return {"tflops": best["tflops"], "ns_per_mma": best["ns_per_mma"], "ctas": best["ctas"],
+            "instruction": "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X "
+                           "M=256 N=256 K=64, operands in shared memory, no copies",
+            "call": "mx_bench_mma", "best_of": reps}
+
+
+def measure_side_workload(L, mx, name, dev, stream, flush, steps, warmup, fp4_meas):
+    """Quantise-pair + GEMM of another Wgrad shape, timed like the headline
+    (L2 flushed before every step, CUDA events on the launching stream)."""
+    import numpy as np
+    import torch
+    from workloads import config_inputs
+    cfg, T, N, K = WORKLOADS[name]
+    d = config_inputs(cfg, seed=0, only=("dY", "X"))
+    dY = torch.from_numpy(d["dY"].view(np.int16)).to(dev)
+    X = torch.from_numpy(d["X"].view(np.int16)).to(dev)
+    sp = stream.cuda_stream
+    rot, nb, rnd, seed = mode_args()
+    aq = torch.empty(mx.codes_bytes(N, T), dtype=torch.uint8, device=dev)
+    as_ = torch.empty(mx.scales_bytes(N, T), dtype=torch.uint8, device=dev)
+    bq = torch.empty(mx.codes_bytes(K, T), dtype=torch.uint8, device=dev)
+    bs = torch.empty(mx.scales_bytes(K, T), dtype=torch.uint8, device=dev)
+    dW = torch.empty((N, K), dtype=torch.float32, device=dev)
+    ptr = lambda t: t.data_ptr()
+
+    def parts():
+        yield L.mx_quantize_pair(ptr(dY), T, N, ptr(X), T, K, rot, nb, rnd, seed, ptr(aq),
+                                 ptr(as_), ptr(bq), ptr(bs), sp)
+        yield L.mx_gemm(ptr(aq), ptr(as_), ptr(bq), ptr(bs), ptr(dW), N, K, T, sp)
+
+    for _ in range(warmup):
+        flush.zero_()
+        if any(parts()):
+            raise RuntimeError(f"{name}: launch failed")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        for j, st in enumerate(parts()):
+            if st != 0:
+                raise RuntimeError(f"{name}: launch failed")
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    mx.check_status()
+    t_q = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(steps)) / steps
+    t_g = sum(ev[i][1].elapsed_time(ev[i][2]) for i in range(steps)) / steps
+    flops = 2.0 * N * K * T
+    hbm = load_peaks()[0]["hbm_gbs"]
+    qbytes = (N + K) * T * (2 + 0.5 + 1 / 32)
+    return {"workload": f"{name} Wgrad: dY [{T},{N}] x X [{T},{K}] -> dW [{N},{K}] fp32, "
+                        f"{mode_text()}",
+            "steps": steps, "ms_per_step": t_q + t_g,
+            "value": flops / ((t_q + t_g) * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "breakdown_ms": {"quantize_pair": t_q, "gemm": t_g},
+            "gemm_tflops": flops / (t_g * 1e-3) / 1e12,
+            "gemm_frac_fp4_measured": flops / (t_g * 1e-3) / 1e12 / fp4_meas["tflops"],
+            "quantizer_gbs": qbytes / (t_q * 1e-3) / 1e9,
+            "quantizer_frac_hbm": qbytes / (t_q * 1e-3) / 1e9 / hbm}
 
 
 def measure_dual(L, mx, dY, T, N, flush, stream, dev, hbm_gbs, reps=30):
@@ -697,9 +815,9 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="o_proj")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="down_proj")
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--cpu-budget-s", type=float, default=8.0)
     ap.add_argument("--ref-budget-s", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-parity-check", action="store_true")
@@ -713,7 +831,10 @@ def main():
                          "measurements instead of the headline line (one GPU)")
     ap.add_argument("--sweep-reps", type=int, default=10)
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip the dual-output encode side measurement")
+                    help="skip the side measurements (o_proj shape, dual-output encode)")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end host-buffer leg (for profiler captures of the "
+                         "hot path only; the line then has no e2e number)")
     args = ap.parse_args()
     MODE.update(rot=args.rot, rot_block=args.rot_block, round=args.round, seed=args.seed)
     if args.warmup < 3:

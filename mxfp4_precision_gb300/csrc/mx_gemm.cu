@@ -38,6 +38,7 @@
 //   (setmaxnreg) so that the epilogue can hold 128 values per thread.
 // Every wait is bounded (see mx_ptx.cuh); a timeout records an error and the
 // CTA unwinds without faulting.
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -87,8 +88,12 @@ struct GemmArgs {
     int64_t b_groups;    // ... and for B
     int k_tiles;         // 256-wide K sub-tiles
     int k_stages;        // stages per tile (ceil(k_tiles / kKSub))
+    int m_tiles;
     int n_tiles;
     int num_tiles;
+    int num_items;       // whole tiles [0, dp_tiles), then two K halves per remaining tile
+    int dp_tiles;
+    int k_split;         // first stage of a second K half
     int c_v8;            // C rows allow 32-byte stores (N % 8 == 0, C 32-byte aligned)
     size_t c_bytes;      // extent of C (store guards)
     int *status;
@@ -106,6 +111,38 @@ struct SharedCtl {
     int abort_flag;
     int issued;                  // stages whose operand loads this CTA has issued (monotonic)
 };
+
+// Tile order: bands of kBand tile rows, column by column within a band, so
+// that the tiles in flight at once share few A and B panels (L2 reuse).
+constexpr int kBand = 8;
+__device__ __forceinline__ void tile_coords(const GemmArgs &g, int t, int &mb, int &nb) {
+    const int per_band = kBand * g.n_tiles;
+    const int band = t / per_band, r = t % per_band;
+    const int first = band * kBand;
+    const int rows = g.m_tiles - first < kBand ? g.m_tiles - first : kBand;
+    mb = first + r % rows;
+    nb = r / rows;
+}
+
+// Work item w: tile t, K stages [ks0, ks1), and which K half it is (-1: the
+// whole range).  A last round that would leave at least half of the pairs
+// idle runs as two K halves per tile; the halves are summed into C with
+// fp32 reduction-adds on a zeroed tile (a + b = b + a: deterministic).
+struct Item {
+    int tile, ks0, ks1, khalf;
+};
+__device__ __forceinline__ Item item_of(const GemmArgs &g, int w) {
+    if (w < g.dp_tiles) return Item{w, 0, g.k_stages, -1};
+    const int j = w - g.dp_tiles, h = j & 1;
+    return Item{g.dp_tiles + (j >> 1), h == 0 ? 0 : g.k_split, h == 0 ? g.k_split : g.k_stages, h};
+}
+
+__device__ __forceinline__ void red_global_v4f(float *p, uint32_t a, uint32_t b, uint32_t c,
+                                               uint32_t d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(__uint_as_float(a)),
+                 "f"(__uint_as_float(b)), "f"(__uint_as_float(c)), "f"(__uint_as_float(d))
+                 : "memory");
+}
 
 __device__ __forceinline__ void st_global_v4f(float *p, uint32_t a, uint32_t b, uint32_t c,
                                               uint32_t d) {
@@ -229,10 +266,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int stage = 0, n_issued = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int tile = pair; ok && tile < g.num_tiles; tile += npairs) {
-                const int mb = tile / g.n_tiles, nb = tile % g.n_tiles;
+            for (int w = pair; ok && w < g.num_items; w += npairs) {
+                const Item it = item_of(g, w);
+                int mb, nb;
+                tile_coords(g, it.tile, mb, nb);
                 const int64_t ga = 2 * static_cast<int64_t>(mb) + rank;  // this CTA's A scale group
-                for (int ks = 0; ks < g.k_stages; ++ks) {
+                for (int ks = it.ks0; ks < it.ks1; ++ks) {
                     if (!mbar_wait_inl(&ctl->empty[stage], phase ^ 1u, g.status, abort)) {
                         ok = false;
                         break;
@@ -287,10 +326,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             bool ok = true;
             const uint32_t idesc0 = idesc_mxf4(2 * kHalf, kTile, 0, 0);
             const uint32_t idesc2 = idesc_mxf4(2 * kHalf, kTile, 2, 2);
-            for (int tile = pair; ok && tile < g.num_tiles; tile += npairs) {
+            for (int w = pair; ok && w < g.num_items; w += npairs) {
+                const Item it = item_of(g, w);
                 if (!mbar_wait_inl(&ctl->acc_empty, acc_phase ^ 1u, g.status, abort)) break;
                 tc_fence_after();
-                for (int ks = 0; ks < g.k_stages; ++ks) {
+                for (int ks = it.ks0; ks < it.ks1; ++ks) {
                     if (!mbar_wait_inl(&ctl->sf_ready[stage], phase, g.status, abort) ||
                         !mbar_wait_inl(&ctl->full[stage], phase, g.status, abort)) {
                         ok = false;
@@ -311,7 +351,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             mma_mxf4_pair(tmem + kAccCol, sdesc_sw128(sa + 32u * j),
                                           sdesc_sw128(sb + 32u * j), (j & 1) ? idesc2 : idesc0,
                                           sf + 4u * ka, sf + 8u + 8u * ka,
-                                          (ks > 0 || u > 0 || j > 0) ? 1u : 0u);
+                                          (ks > it.ks0 || u > 0 || j > 0) ? 1u : 0u);
                         }
                     }
                     tc_commit_pair(&ctl->empty[stage], 0x3);
@@ -343,9 +383,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
         int stage = 0;
         uint32_t phase = 0;
-        for (int tile = pair; tile < g.num_tiles; tile += npairs) {
+        for (int w = pair; w < g.num_items; w += npairs) {
+            const Item it = item_of(g, w);
             bool ok = true;
-            for (int ks = 0; ks < g.k_stages; ++ks) {
+            for (int ks = it.ks0; ks < it.ks1; ++ks) {
                 int okw = 1;
                 if (lane == 0)
                     okw = mbar_wait_inl(&ctl->sf_full[stage], phase, g.status, abort) ? 1 : 0;
@@ -404,9 +445,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int q = warp & 3;                   // TMEM lane quarter this warp may access
         const int half = (warp - kEpiWarp0) / 4;  // column half of the 256-wide tile
         uint32_t acc_phase = 0;
-        int done = 0;                             // tiles of this pair finished
-        for (int tile = pair; tile < g.num_tiles; tile += npairs, ++done) {
-            const int mb = tile / g.n_tiles, nb = tile % g.n_tiles;
+        int staged = 0;                           // stages of this pair's items so far
+        for (int w = pair; w < g.num_items; w += npairs) {
+            const Item it = item_of(g, w);
+            int mb, nb;
+            tile_coords(g, it.tile, mb, nb);
+            staged += it.ks1 - it.ks0;
             // One lane waits; the verdict is broadcast so the warp stays
             // converged for the .sync.aligned tensor-memory loads.
             int ok = 1;
@@ -423,7 +467,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tmem_ld_32x32b_x32(tbase + 64u, v2);
             tmem_ld_32x32b_x32(tbase + 96u, v3);
             tmem_ld_wait();
-            // The accumulator is in registers: the next tile may start.
+            // The accumulator is in registers: the next item may start.
             tc_fence_before();
             __syncwarp();
             if (lane == 0) arrive_even(&ctl->acc_empty);
@@ -432,16 +476,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 static_cast<int64_t>(mb) * kTile + kHalf * rank + 32 * q + lane;
             float *crow = g.C + row * g.N;
             const int64_t col0 = static_cast<int64_t>(nb) * kTile + 128 * half;
-            const bool more = tile + npairs < g.num_tiles;
-            if (more && g.c_v8 && col0 + 127 < g.N) {
+            const int next = w + npairs;
+            if (it.khalf >= 0) {
+                // One K half of a tile: add into the zeroed tile.
+                if (row < g.M) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t *vc = c == 0 ? v0 : c == 1 ? v1 : c == 2 ? v2 : v3;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int64_t col = col0 + 32 * c + 4 * j;
+                            if (col < g.N &&
+                                MX_STORE_OK(crow + col, 16, g.C, g.c_bytes, g.status))
+                                red_global_v4f(crow + col, vc[4 * j], vc[4 * j + 1],
+                                               vc[4 * j + 2], vc[4 * j + 3]);
+                        }
+                    }
+                }
+            } else if (next < g.num_items && g.c_v8 && col0 + 127 < g.N) {
                 // Store chunk j (8 values) once the producer has issued stage
-                // 1 + j * k_stages / 16 of the next tile.
-                const int base = (done + 1) * g.k_stages;
+                // 1 + j * s / 16 of the next item (s stages).
+                const Item nx = item_of(g, next);
+                const int ns = nx.ks1 - nx.ks0;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    const int need = 1 + (j * g.k_stages) / 16;
-                    if (j == 0 || need != 1 + ((j - 1) * g.k_stages) / 16)
-                        if (!wait_issued(ctl, base + need, g.status, abort)) break;
+                    const int need = 1 + (j * ns) / 16;
+                    if (j == 0 || need != 1 + ((j - 1) * ns) / 16)
+                        if (!wait_issued(ctl, staged + need, g.status, abort)) break;
                     const uint32_t *src = j < 4    ? &v0[8 * j]
                                           : j < 8  ? &v1[8 * (j - 4)]
                                           : j < 12 ? &v2[8 * (j - 8)]
@@ -517,7 +578,8 @@ cudaError_t launch_gemm(const void *Aq, const void *As, const void *Bq, const vo
     g.k_stages = (g.k_tiles + kKSub - 1) / kKSub;
     const int64_t m_tiles = (M + kTile - 1) / kTile;
     const int64_t n_tiles = (N + kTile - 1) / kTile;
-    if (m_tiles * n_tiles > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    if (m_tiles * n_tiles > 0x3FFFFFFF) return cudaErrorInvalidValue;
+    g.m_tiles = static_cast<int>(m_tiles);
     g.n_tiles = static_cast<int>(n_tiles);
     g.num_tiles = static_cast<int>(m_tiles * n_tiles);
     g.c_v8 = (N % 8 == 0 && (reinterpret_cast<uintptr_t>(C) & 31) == 0) ? 1 : 0;
@@ -526,10 +588,38 @@ cudaError_t launch_gemm(const void *Aq, const void *As, const void *Bq, const vo
     cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kGemmSmem));
     if (e != cudaSuccess) return e;
-    // Resident CTAs: as many 2-CTA clusters as fit at once, one tile per pair.
+    // Resident CTAs: as many 2-CTA clusters as fit at once, one item per pair.
     const int pairs_max = gemm_clusters(dev);
     if (pairs_max < 1) return cudaErrorLaunchOutOfResources;
-    const int pairs = g.num_tiles < pairs_max ? g.num_tiles : pairs_max;
+    const int rem = g.num_tiles % pairs_max;
+    g.dp_tiles = g.num_tiles;
+    g.num_items = g.num_tiles;
+    g.k_split = g.k_stages;
+    if (g.num_tiles > pairs_max && rem > 0 && 2 * rem <= pairs_max && g.k_stages >= 2) {
+        // The last round's tiles are the last `rem` in the tile order: the
+        // tail of one band from some column on, plus any later (shorter) band
+        // whole.  Zero those regions (tiles there that are stored whole are
+        // written after the memsets, in stream order).
+        g.dp_tiles = g.num_tiles - rem;
+        g.num_items = g.dp_tiles + 2 * rem;
+        g.k_split = g.k_stages / 2;
+        const int per_band = kBand * g.n_tiles;
+        const int band = g.dp_tiles / per_band;
+        const int first = band * kBand;
+        const int rows = g.m_tiles - first < kBand ? g.m_tiles - first : kBand;
+        const int nb0 = (g.dp_tiles % per_band) / rows;
+        const int64_t r0 = static_cast<int64_t>(first) * kTile;
+        const int64_t r1 = std::min<int64_t>(M, r0 + static_cast<int64_t>(rows) * kTile);
+        const int64_t c0 = static_cast<int64_t>(nb0) * kTile;
+        e = cudaMemset2DAsync(C + r0 * N + c0, static_cast<size_t>(N) * sizeof(float), 0,
+                              static_cast<size_t>(N - c0) * sizeof(float),
+                              static_cast<size_t>(r1 - r0), stream);
+        if (e == cudaSuccess && r1 < M)
+            e = cudaMemsetAsync(C + r1 * N, 0, static_cast<size_t>(M - r1) * N * sizeof(float),
+                                stream);
+        if (e != cudaSuccess) return e;
+    }
+    const int pairs = g.num_items < pairs_max ? g.num_items : pairs_max;
     mx_gemm_kernel<<<2 * pairs, kThreads, kGemmSmem, stream>>>(map_a, map_b, g);
     return cudaGetLastError();
 }

@@ -51,16 +51,19 @@ def test_gemm_parity(M, N, K):
     assert worst < 1e-5
 
 
-def _sm_count():
-    return torch.cuda.get_device_properties(0).multi_processor_count
+def _pairs():
+    # the GEMM runs one 256 x 256 tile per 2-CTA pair at a time
+    return torch.cuda.get_device_properties(0).multi_processor_count // 2
 
 
 @pytest.mark.parametrize("N", [2048, 2048 - 100, 1792 + 100])
 def test_gemm_small_last_round(N):
-    """More 128 x 256 tiles than SMs, with a last round of at most 8 tiles.
-    N = 1948 and N = 1892 leave the last column tile 156 and 100 wide."""
-    m_tiles = _sm_count() // 8 + 1
-    M, K = 128 * m_tiles - 37, 512
+    """A few more 256 x 256 tiles than pairs: the last round runs as K halves
+    added into a zeroed tile.  N = 1948 and N = 1892 leave the last column
+    tile 156 and 100 wide; M is ragged too."""
+    n_tiles = (N + 255) // 256
+    m_tiles = (_pairs() + 4 + n_tiles - 1) // n_tiles
+    M, K = 256 * m_tiles - 37, 1024
     Aq, As = _operand(M, K, 11, 1e-3)
     Bq, Bs = _operand(N, K, 12)
     C = run_gemm(Aq, As, Bq, Bs, M, N, K)
@@ -68,10 +71,37 @@ def test_gemm_small_last_round(N):
     assert assert_gemm_close(C, Cref, Cabs, f"small last round {M}x{N}x{K}") < 1e-5
 
 
+@pytest.mark.parametrize("K", [1536, 1312])
+def test_gemm_split_odd_stage_count(K):
+    """K halves of unequal length (3 stages of 512: 1 + 2), with and without a
+    ragged contraction tail."""
+    n_tiles = 8
+    m_tiles = (_pairs() + 6 + n_tiles - 1) // n_tiles
+    M, N = 256 * m_tiles, 256 * n_tiles
+    Aq, As = _operand(M, K, 15, 1e-3)
+    Bq, Bs = _operand(N, K, 16)
+    C = run_gemm(Aq, As, Bq, Bs, M, N, K)
+    Cref, Cabs = oracle.gemm(Aq, As, Bq, Bs)
+    assert assert_gemm_close(C, Cref, Cabs, f"odd split {M}x{N}x{K}") < 1e-5
+
+
+def test_gemm_split_tail_across_bands():
+    """The last round's tiles span the end of one 8-row band of tiles and a
+    whole later band (17 x 5 tiles)."""
+    M, N, K = 17 * 256, 5 * 256, 1024
+    Aq, As = _operand(M, K, 17, 1e-3)
+    Bq, Bs = _operand(N, K, 18)
+    C = run_gemm(Aq, As, Bq, Bs, M, N, K)
+    Cref, Cabs = oracle.gemm(Aq, As, Bq, Bs)
+    assert assert_gemm_close(C, Cref, Cabs, f"tail across bands {M}x{N}x{K}") < 1e-5
+
+
 def test_gemm_large_last_round():
-    """More tiles than SMs, with a last round of more than 100 tiles."""
-    m_tiles = (_sm_count() + 100) // 8 + 1
-    M, N, K = 128 * m_tiles, 2048, 256
+    """More tiles than pairs, with a last round of more than half the pairs
+    (whole tiles, no K split)."""
+    n_tiles = 8
+    m_tiles = (_pairs() + _pairs() // 2 + 10 + n_tiles - 1) // n_tiles
+    M, N, K = 256 * m_tiles, 256 * n_tiles, 512
     Aq, As = _operand(M, K, 13, 1e-3)
     Bq, Bs = _operand(N, K, 14)
     C = run_gemm(Aq, As, Bq, Bs, M, N, K)
@@ -81,9 +111,10 @@ def test_gemm_large_last_round():
 
 def test_gemm_split_rounds_deterministic():
     """Runs whose last round is split along K give the same bits every time:
-    the two halves are summed in a fixed order."""
-    m_tiles = _sm_count() // 8 + 1
-    M, N, K = 128 * m_tiles, 2048, 1024
+    two partial sums added into zero commute."""
+    n_tiles = 8
+    m_tiles = (_pairs() + 4 + n_tiles - 1) // n_tiles
+    M, N, K = 256 * m_tiles, 256 * n_tiles, 1024
     Aq, As = _operand(M, K, 21, 1e-3)
     Bq, Bs = _operand(N, K, 22)
     args = (_dev(Aq), _dev(tile_scales(As, M, K)), _dev(Bq), _dev(tile_scales(Bs, N, K)), M, N, K)
