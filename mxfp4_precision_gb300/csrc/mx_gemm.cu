@@ -91,9 +91,7 @@ struct GemmArgs {
     int m_tiles;
     int n_tiles;
     int num_tiles;
-    int num_items;       // whole tiles [0, dp_tiles), then two K halves per remaining tile
-    int dp_tiles;
-    int k_split;         // first stage of a second K half
+    int num_items;       // one item per tile
     int c_v8;            // C rows allow 32-byte stores (N % 8 == 0, C 32-byte aligned)
     size_t c_bytes;      // extent of C (store guards)
     int *status;
@@ -124,24 +122,12 @@ __device__ __forceinline__ void tile_coords(const GemmArgs &g, int t, int &mb, i
     nb = r / rows;
 }
 
-// Work item w: tile t, K stages [ks0, ks1), and which K half it is (-1: the
-// whole range).  A last round that would leave at least half of the pairs
-// idle runs as two K halves per tile; the halves are summed into C with
-// fp32 reduction-adds on a zeroed tile (a + b = b + a: deterministic).
+// Work item w: tile t over K stages [ks0, ks1).
 struct Item {
-    int tile, ks0, ks1, khalf;
+    int tile, ks0, ks1;
 };
 __device__ __forceinline__ Item item_of(const GemmArgs &g, int w) {
-    if (w < g.dp_tiles) return Item{w, 0, g.k_stages, -1};
-    const int j = w - g.dp_tiles, h = j & 1;
-    return Item{g.dp_tiles + (j >> 1), h == 0 ? 0 : g.k_split, h == 0 ? g.k_split : g.k_stages, h};
-}
-
-__device__ __forceinline__ void red_global_v4f(float *p, uint32_t a, uint32_t b, uint32_t c,
-                                               uint32_t d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(__uint_as_float(a)),
-                 "f"(__uint_as_float(b)), "f"(__uint_as_float(c)), "f"(__uint_as_float(d))
-                 : "memory");
+    return Item{w, 0, g.k_stages};
 }
 
 __device__ __forceinline__ void st_global_v4f(float *p, uint32_t a, uint32_t b, uint32_t c,
@@ -256,6 +242,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
     volatile int *abort = &ctl->abort_flag;
+    // Barriers and tensor memory are set up; global memory is touched only
+    // once the stream's previous kernel (the encoder) has completed.
+    griddep_wait();
+    griddep_launch_dependents();
 
     if (warp < kWriterWarp0) {
         // Warpgroup 0: producers and the MMA issuer need few registers.
@@ -477,23 +467,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             float *crow = g.C + row * g.N;
             const int64_t col0 = static_cast<int64_t>(nb) * kTile + 128 * half;
             const int next = w + npairs;
-            if (it.khalf >= 0) {
-                // One K half of a tile: add into the zeroed tile.
-                if (row < g.M) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const uint32_t *vc = c == 0 ? v0 : c == 1 ? v1 : c == 2 ? v2 : v3;
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const int64_t col = col0 + 32 * c + 4 * j;
-                            if (col < g.N &&
-                                MX_STORE_OK(crow + col, 16, g.C, g.c_bytes, g.status))
-                                red_global_v4f(crow + col, vc[4 * j], vc[4 * j + 1],
-                                               vc[4 * j + 2], vc[4 * j + 3]);
-                        }
-                    }
-                }
-            } else if (next < g.num_items && g.c_v8 && col0 + 127 < g.N) {
+            if (next < g.num_items && g.c_v8 && col0 + 127 < g.N) {
                 // Store chunk j (8 values) once the producer has issued stage
                 // 1 + j * s / 16 of the next item (s stages).
                 const Item nx = item_of(g, next);
@@ -591,36 +565,20 @@ cudaError_t launch_gemm(const void *Aq, const void *As, const void *Bq, const vo
     // Resident CTAs: as many 2-CTA clusters as fit at once, one item per pair.
     const int pairs_max = gemm_clusters(dev);
     if (pairs_max < 1) return cudaErrorLaunchOutOfResources;
-    const int rem = g.num_tiles % pairs_max;
-    g.dp_tiles = g.num_tiles;
     g.num_items = g.num_tiles;
-    g.k_split = g.k_stages;
-    if (g.num_tiles > pairs_max && rem > 0 && 2 * rem <= pairs_max && g.k_stages >= 2) {
-        // The last round's tiles are the last `rem` in the tile order: the
-        // tail of one band from some column on, plus any later (shorter) band
-        // whole.  Zero those regions (tiles there that are stored whole are
-        // written after the memsets, in stream order).
-        g.dp_tiles = g.num_tiles - rem;
-        g.num_items = g.dp_tiles + 2 * rem;
-        g.k_split = g.k_stages / 2;
-        const int per_band = kBand * g.n_tiles;
-        const int band = g.dp_tiles / per_band;
-        const int first = band * kBand;
-        const int rows = g.m_tiles - first < kBand ? g.m_tiles - first : kBand;
-        const int nb0 = (g.dp_tiles % per_band) / rows;
-        const int64_t r0 = static_cast<int64_t>(first) * kTile;
-        const int64_t r1 = std::min<int64_t>(M, r0 + static_cast<int64_t>(rows) * kTile);
-        const int64_t c0 = static_cast<int64_t>(nb0) * kTile;
-        e = cudaMemset2DAsync(C + r0 * N + c0, static_cast<size_t>(N) * sizeof(float), 0,
-                              static_cast<size_t>(N - c0) * sizeof(float),
-                              static_cast<size_t>(r1 - r0), stream);
-        if (e == cudaSuccess && r1 < M)
-            e = cudaMemsetAsync(C + r1 * N, 0, static_cast<size_t>(M - r1) * N * sizeof(float),
-                                stream);
-        if (e != cudaSuccess) return e;
-    }
     const int pairs = g.num_items < pairs_max ? g.num_items : pairs_max;
-    mx_gemm_kernel<<<2 * pairs, kThreads, kGemmSmem, stream>>>(map_a, map_b, g);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2 * pairs, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kGemmSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, mx_gemm_kernel, map_a, map_b, g);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

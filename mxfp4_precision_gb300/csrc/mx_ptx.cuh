@@ -43,6 +43,20 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// ---------------------------------------------------------------- launch order
+// Programmatic dependent launch.  The library's kernels are launched so that
+// each may start while the previous kernel of its stream is still finishing:
+// every thread first waits here until that kernel has completed and its
+// memory is visible (a no-op for a kernel launched without the attribute),
+// touching no global memory before.  Then it allows its own successor to
+// launch early under the same rule.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)

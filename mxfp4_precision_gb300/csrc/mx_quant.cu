@@ -525,6 +525,8 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads, SR ? 1 
         if (a1.num_tiles > 0) prefetch_tmap(&map1);
     }
     __syncthreads();
+    griddep_wait();
+    griddep_launch_dependents();
 
     auto issue = [&](int tile, int s) {
         const bool second = tile >= a0.num_tiles;
@@ -694,6 +696,8 @@ __global__ void __launch_bounds__(kThreads, SR ? 1 : kColMinBlocks) mxq_colwise_
         if (a1.num_tiles > 0) prefetch_tmap(&map1);
     }
     __syncthreads();
+    griddep_wait();
+    griddep_launch_dependents();
 
     auto issue = [&](int tile, int s) {
         const bool second = tile >= a0.num_tiles;
@@ -845,6 +849,8 @@ __global__ void __launch_bounds__(kThreads) mxq_rowwise_kernel(const __grid_cons
         prefetch_tmap(&src_map);
     }
     __syncthreads();
+    griddep_wait();
+    griddep_launch_dependents();
 
     auto issue = [&](int tile, int s) {
         const int rt = tile / p.tiles_inner, ct = tile % p.tiles_inner;
@@ -977,7 +983,21 @@ cudaError_t launch_persistent_n(Kern kernel, int threads, int num_tiles, size_t 
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
     const int grid = num_tiles < dev.sm_count * per_sm ? num_tiles : dev.sm_count * per_sm;
-    kernel<<<grid, threads, smem, stream>>>(args...);
+    // Programmatic dependent launch: the kernel may start while the stream's
+    // previous kernel finishes; it waits for it (griddep_wait) before touching
+    // global memory.
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -58,9 +58,9 @@ def _pairs():
 
 @pytest.mark.parametrize("N", [2048, 2048 - 100, 1792 + 100])
 def test_gemm_small_last_round(N):
-    """A few more 256 x 256 tiles than pairs: the last round runs as K halves
-    added into a zeroed tile.  N = 1948 and N = 1892 leave the last column
-    tile 156 and 100 wide; M is ragged too."""
+    """A few more 256 x 256 tiles than pairs (a short last round).  N = 1948
+    and N = 1892 leave the last column tile 156 and 100 wide; M is ragged
+    too."""
     n_tiles = (N + 255) // 256
     m_tiles = (_pairs() + 4 + n_tiles - 1) // n_tiles
     M, K = 256 * m_tiles - 37, 1024
@@ -72,9 +72,9 @@ def test_gemm_small_last_round(N):
 
 
 @pytest.mark.parametrize("K", [1536, 1312])
-def test_gemm_split_odd_stage_count(K):
-    """K halves of unequal length (3 stages of 512: 1 + 2), with and without a
-    ragged contraction tail."""
+def test_gemm_odd_stage_count(K):
+    """Three 512-wide K stages per tile (the last one half full for K = 1536's
+    neighbour 1312, whose contraction tail is ragged too)."""
     n_tiles = 8
     m_tiles = (_pairs() + 6 + n_tiles - 1) // n_tiles
     M, N = 256 * m_tiles, 256 * n_tiles
@@ -85,9 +85,9 @@ def test_gemm_split_odd_stage_count(K):
     assert assert_gemm_close(C, Cref, Cabs, f"odd split {M}x{N}x{K}") < 1e-5
 
 
-def test_gemm_split_tail_across_bands():
-    """The last round's tiles span the end of one 8-row band of tiles and a
-    whole later band (17 x 5 tiles)."""
+def test_gemm_last_round_across_bands():
+    """Tiles run in bands of 8 tile rows; here the last round spans the end of
+    one band and a whole later band of one row (17 x 5 tiles)."""
     M, N, K = 17 * 256, 5 * 256, 1024
     Aq, As = _operand(M, K, 17, 1e-3)
     Bq, Bs = _operand(N, K, 18)
@@ -97,8 +97,7 @@ def test_gemm_split_tail_across_bands():
 
 
 def test_gemm_large_last_round():
-    """More tiles than pairs, with a last round of more than half the pairs
-    (whole tiles, no K split)."""
+    """More tiles than pairs, with a last round of more than half the pairs."""
     n_tiles = 8
     m_tiles = (_pairs() + _pairs() // 2 + 10 + n_tiles - 1) // n_tiles
     M, N, K = 256 * m_tiles, 256 * n_tiles, 512
@@ -109,9 +108,9 @@ def test_gemm_large_last_round():
     assert assert_gemm_close(C, Cref, Cabs, f"large last round {M}x{N}x{K}") < 1e-5
 
 
-def test_gemm_split_rounds_deterministic():
-    """Runs whose last round is split along K give the same bits every time:
-    two partial sums added into zero commute."""
+def test_gemm_deterministic():
+    """Repeated runs give the same bits: every output element is accumulated
+    in one fixed order."""
     n_tiles = 8
     m_tiles = (_pairs() + 4 + n_tiles - 1) // n_tiles
     M, N, K = 256 * m_tiles, 256 * n_tiles, 1024
