@@ -53,11 +53,17 @@ extern "C" mx_status mx_linear_wgrad_noalloc(const void *d_dY, const void *d_X, 
                                              int64_t T, int64_t N, int64_t K, int rot,
                                              int rot_block, int rnd, uint64_t seed,
                                              void *stream) {
-    if (T < 0 || N < 0 || K < 0) return MX_ERR_SHAPE;
+    // Argument checks first, with mx_linear_wgrad's own rules and status
+    // codes: without a workspace it either rejects the arguments, finishes a
+    // call that needs no scratch (empty shapes), or reports MX_ERR_WORKSPACE
+    // -- all before launching anything that needs one.
+    mx_status st = mx_linear_wgrad(d_dY, d_X, d_dW, T, N, K, rot, rot_block, rnd, seed, nullptr,
+                                   0, stream);
+    if (st != MX_ERR_WORKSPACE) return st;
     const size_t need = mx_linear_workspace_bytes(MX_OP_WGRAD, T, N, K);
     if (need > kScratchBytes) return MX_ERR_WORKSPACE;  // beyond the fixed scratch area
     void *scratch = nullptr;
-    const mx_status st = scratch_for_current_device(&scratch);
+    st = scratch_for_current_device(&scratch);
     if (st != MX_OK) return st;
     // The encoded operands are fully rewritten on every call (padding
     // included), so nothing in the shared area needs clearing first.

@@ -146,3 +146,24 @@ def test_linear_rejects_bad_arguments_before_launch(L):
     assert w(dW=0) == 1
     assert w(K=250) == 3
     assert w(N=0) == 0
+
+
+def test_noalloc_checks_arguments_before_the_scratch_limit(L):
+    """The no-allocation Wgrad entry point reports the same status codes as
+    mx_linear_wgrad for bad arguments, even when the request is also larger
+    than its fixed scratch area; only otherwise-valid oversize requests get
+    MX_ERR_WORKSPACE.  None of these calls reaches the GPU."""
+    big = dict(T=16384, N=4096, K=4096)            # needs 71.3 MB > 64 MiB of scratch
+
+    def na(T, N, K, rot=1, nb=32, rnd=0, dW=0x5000, dY=0x1000):
+        return L.mx_linear_wgrad_noalloc(V(dY), V(0x2000), V(dW), T, N, K, rot, nb, rnd, 0, None)
+    assert na(**big) == 4                          # valid, too large: MX_ERR_WORKSPACE
+    assert na(**{**big, "T": 16384 - 16}) == 2     # T % 32 != 0: MX_ERR_SHAPE
+    assert na(**{**big, "K": 4094}) == 3           # K % 8 != 0 (TMA rows): MX_ERR_ALIGN
+    assert na(**big, rot=5) == 1                   # bad enum: MX_ERR_INVALID_ARG
+    assert na(**big, nb=48) == 1
+    assert na(**big, rnd=2) == 1
+    assert na(**big, dW=0) == 1
+    assert na(**big, dY=0x1008) == 3               # misaligned input
+    assert na(T=256, N=0, K=256) == 0              # empty: nothing to do
+    assert na(T=-1, N=128, K=256) == 2

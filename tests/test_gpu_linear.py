@@ -170,12 +170,41 @@ def test_o_proj_full_size():
     assert worst < 1e-5
 
 
+def _par_oracle_quantize(bits, contract, rot, nb, rnd, seed, tag):
+    """oracle.quantize of every line, partitioned by lines over the host cores
+    (the oracle's C code releases the GIL); its arithmetic is unchanged."""
+    from concurrent.futures import ThreadPoolExecutor
+    n = bits.shape[1] if contract == mx.CONTRACT_ROWS else bits.shape[0]
+    parts = max(1, min(os.cpu_count() or 1, n // 64))
+    chunks = np.array_split(np.arange(n), parts)
+    with ThreadPoolExecutor(parts) as ex:
+        res = list(ex.map(lambda ln: oracle.quantize(bits, OC[contract], rot, nb, rnd, seed, tag,
+                                                     lines=ln), chunks))
+    return np.concatenate([r[0] for r in res]), np.concatenate([r[1] for r in res])
+
+
+def _compare_pair_all_lines(dY_bits, X_bits, rot, nb, rnd, seed):
+    """Every code and scale byte of both Wgrad operands from the one-launch
+    encode (mx_quantize_pair, SR tags 1 and 2) against the oracle."""
+    (ca, sa), (cb, sb) = mx.quantize_pair(_dev(dY_bits), _dev(X_bits), rot, nb, rnd, seed)
+    mx.check_status()
+    T = dY_bits.shape[0]
+    for bits, codes, scales, tag in ((dY_bits, ca, sa, 1), (X_bits, cb, sb, 2)):
+        n = bits.shape[1]
+        oc, os_ = _par_oracle_quantize(bits, mx.CONTRACT_ROWS, rot, nb, rnd, seed, tag)
+        got_c = codes.cpu().numpy()
+        got_s = untile_scales(scales.cpu().numpy(), n, T)
+        bad = np.argwhere((got_c != oc).any(axis=1) | (got_s != os_).any(axis=1))
+        assert bad.size == 0, f"rot {rot}/{nb} rnd {rnd}: {bad.size} of {n} lines differ, " \
+                              f"first {bad[:5].ravel().tolist()}"
+
+
 @pytest.mark.slow
 def test_down_proj_rotation_sweep():
+    # every line of both operands at every Hadamard size, plus sampled GEMM entries
     d = config_inputs("down_proj", seed=0)
     for nb in (16, 32, 64, 128, 256):
-        lines = sample_lines(14336, 96, nb)
-        _compare_codes(d["X"], mx.CONTRACT_ROWS, mx.ROT_HADAMARD_DET, nb, mx.ROUND_RNE, 0, lines)
+        _compare_pair_all_lines(d["dY"], d["X"], mx.ROT_HADAMARD_DET, nb, mx.ROUND_RNE, 0)
         check_op(mx.OP_WGRAD, d["dY"], d["X"], mx.ROT_HADAMARD_DET, nb, sample=24)
 
 
@@ -185,8 +214,7 @@ def test_ablation_modes_full_size():
     for rot, nb, rnd, seed in [(mx.ROT_NONE, 32, mx.ROUND_RNE, 0),
                                (mx.ROT_HADAMARD_RAND, 32, mx.ROUND_RNE, 1),
                                (mx.ROT_NONE, 32, mx.ROUND_SR, 1)]:
-        lines = sample_lines(4096, 64, 7)
-        _compare_codes(d["dY"], mx.CONTRACT_ROWS, rot, nb, rnd, seed, lines)
+        _compare_pair_all_lines(d["dY"], d["X"], rot, nb, rnd, seed)
         check_op(mx.OP_WGRAD, d["dY"], d["X"], rot, nb, rnd, seed, sample=24)
 
 

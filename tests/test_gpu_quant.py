@@ -215,3 +215,35 @@ def test_scales_to_canonical_of_an_encode_equals_the_oracle_scales():
     mx.check_status()
     _, os_ = oracle.quantize(bits, oracle.CONTRACT_ROWS, oracle.ROT_HADAMARD_DET, 32)
     assert np.array_equal(got.cpu().numpy(), os_)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("rot,nb,rnd", [(mx.ROT_HADAMARD_DET, 32, mx.ROUND_RNE),
+                                        (mx.ROT_HADAMARD_DET, 128, mx.ROUND_RNE),
+                                        (mx.ROT_NONE, 32, mx.ROUND_SR)])
+def test_dual_o_proj_full_size(rot, nb, rnd):
+    """Every byte of both encodings of the o_proj output gradient (8192 x 4096),
+    padding included, against the oracle encodes (partitioned over the host
+    cores by lines; the oracle's arithmetic is unchanged)."""
+    from concurrent.futures import ThreadPoolExecutor
+    import os
+    bits = config_inputs("o_proj", seed=0, only=("dY",))["dY"]
+    T, N = bits.shape
+    (ct, st), (cn, sn) = mx.quantize_dual(
+        torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda(), rot, nb, rnd, 0)
+    mx.check_status()
+    cores = os.cpu_count() or 1
+
+    def par(contract, r, b, n):
+        chunks = np.array_split(np.arange(n), cores)
+        with ThreadPoolExecutor(cores) as ex:
+            res = list(ex.map(lambda ln: oracle.quantize(bits, contract, r, b, rnd, 0, 1, lines=ln),
+                              chunks))
+        return np.concatenate([x[0] for x in res]), np.concatenate([x[1] for x in res])
+
+    oc, os_ = par(oracle.CONTRACT_ROWS, rot, nb, N)
+    assert np.array_equal(ct.cpu().numpy(), oc)
+    assert np.array_equal(st.cpu().numpy(), tile_scales(os_, N, T))
+    oc, os_ = par(oracle.CONTRACT_COLS, oracle.ROT_NONE, 32, T)
+    assert np.array_equal(cn.cpu().numpy(), oc)
+    assert np.array_equal(sn.cpu().numpy(), tile_scales(os_, T, N))

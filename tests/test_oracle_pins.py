@@ -282,6 +282,14 @@ def test_sr_outputs_neighbours_and_is_unbiased():
         assert set(np.unique(np.abs(vals))) <= {lo, hi}
         # exact expectation over the even sweep is within one step of the sweep's grain
         assert abs(vals.mean() - float(v)) <= (hi - lo) * 2.0 ** -20 + 1e-12
+        # variance: a draw that lands on lo or hi with probability 1 - p, p
+        # (p = (|v| - lo) / (hi - lo)) has E[(SR - v)^2] = p (1 - p) (hi - lo)^2,
+        # never below the squared error of rounding to the nearest neighbour
+        p = (a - lo) / (hi - lo)
+        mse_sr = float(((np.abs(vals) - a) ** 2).mean())
+        assert abs(mse_sr - p * (1 - p) * (hi - lo) ** 2) <= (hi - lo) ** 2 * 2.0 ** -19
+        rne = oracle.e2m1_value(int(oracle.e2m1_rne(np.array([a], dtype=np.float32))[0]))
+        assert mse_sr >= (rne - a) ** 2 - 1e-12
 
 
 def test_sr_representable_unchanged_and_saturates():
