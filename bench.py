@@ -309,6 +309,16 @@ def run_mine(args, world, rank, local):
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     ptr = lambda t: t.data_ptr()
 
+    # One step = the public Wgrad call on resident inputs: the encode of both
+    # operands (one launch) and the GEMM.
+    ws_step = torch.empty(mx.linear_workspace_bytes(mx.OP_WGRAD, T, N, K), dtype=torch.uint8,
+                          device=dev)
+
+    def step_call():
+        yield L.mx_linear_wgrad(ptr(dY), ptr(X), ptr(dW), T, N, K, rot, nb, rnd, seed,
+                                ptr(ws_step), ws_step.numel(), sp)
+
+    # The two stand-alone launches, timed separately for the per-kernel rooflines.
     def step_parts():
         s1 = L.mx_quantize_pair(ptr(dY), T, N, ptr(X), T, K, rot, nb, rnd, seed, ptr(aq), ptr(as_),
                                 ptr(bq), ptr(bs), sp)
@@ -323,14 +333,15 @@ def run_mine(args, world, rank, local):
     # warm-up
     for _ in range(args.warmup):
         flush.zero_()
+        for st in step_call():
+            check(st, "warm-up")
         for st in step_parts():
             check(st, "warm-up")
     torch.cuda.synchronize(dev)
     mx.check_status()
 
     # Timed region: K steps, one pair of events per step (the flush between
-    # steps stays outside them).  The two launches of a step follow each other
-    # with programmatic dependent launch, as in any use of the library.
+    # steps stays outside them).
     n = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
     barrier(world)
@@ -339,7 +350,7 @@ def run_mine(args, world, rank, local):
         for i in range(n):
             flush.zero_()
             ev[i][0].record(stream)
-            for st in step_parts():
+            for st in step_call():
                 check(st, "step")
             ev[i][1].record(stream)
         torch.cuda.synchronize(dev)
@@ -350,8 +361,8 @@ def run_mine(args, world, rank, local):
     flops_per_s, total_ms = job_throughput(sum(step_ms), n, flops_step, world, dev)
     value = flops_per_s / 1e12
 
-    # Per-kernel breakdown (for the rooflines), in separate steps with an event
-    # between the two launches.
+    # The stand-alone encode and GEMM launches (per-kernel rooflines), in
+    # separate steps with an event between the two launches.
     nb_steps = min(n, 200)
     evb = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nb_steps)]
     for i in range(nb_steps):
@@ -439,6 +450,10 @@ def run_mine(args, world, rank, local):
     # the tensor cores' own MXFP4 rate on this GPU (issue-rate microbenchmark)
     # and the o_proj shape beside the headline workload
     fp4_meas = measure_fp4_peak(mx) if rank == 0 else None
+    fused_side = None
+    if rank == 0 and not args.no_extras:
+        fused_side = measure_fused(L, mx, dY, X, dW, T, N, K, flush, stream, dev, step_ms,
+                                   fp4_meas)
     side = None
     if rank == 0 and not args.no_extras and args.workload != "o_proj":
         side = measure_side_workload(L, mx, "o_proj", dev, stream, flush, min(n, 300),
@@ -485,6 +500,7 @@ def run_mine(args, world, rank, local):
                 "traffic": tr("mxq_colwise_kernel", "mx_quant.cu"),
                 "peak_basis": f"{peak_src} HBM copy bandwidth",
                 "ms_per_launch": t_q}
+    kernels = [gemm_rf, quant_rf]
     dominant = gemm_rf if t_g >= t_q else quant_rf
     clk = clocks.summary()
     cpu = None
@@ -505,14 +521,17 @@ def run_mine(args, world, rank, local):
             "roofline": {k: dominant[k] for k in ("bound", "achieved", "peak", "unit", "frac",
                                                    "traffic", "peak_fp4_measured",
                                                    "frac_fp4_measured") if k in dominant},
-            "roofline_kernels": [gemm_rf, quant_rf],
+            "roofline_kernels": kernels,
+            "step_launches": 2,
+            "fused_wgrad": fused_side,
             "fp4_peak_fraction": value / fp4_peak,
             "fp4_peak_measured": fp4_meas,
             "fp4_measured_fraction": value / fp4_meas["tflops"],
             "o_proj": side,
             "breakdown_ms": {"quantize_pair": t_q, "gemm": t_g,
-                             "note": f"separate {nb_steps} steps with an event between the "
-                                     "two launches (the headline times whole steps)"},
+                             "note": f"the stand-alone encode and GEMM launches, in separate "
+                                     f"{nb_steps} steps with an event between them (the "
+                                     f"headline step is mx_linear_wgrad: the same two launches)"},
             "cpu_baseline": cpu,
             "e2e": None if e2e_ms is None else {
                 "value": e2e_value, "unit": "TFLOP/s",
@@ -580,10 +599,20 @@ def measure_side_workload(L, mx, name, dev, stream, flush, steps, warmup, fp4_me
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     whole = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
     torch.cuda.synchronize(dev)
+    ws = torch.empty(mx.linear_workspace_bytes(mx.OP_WGRAD, T, N, K), dtype=torch.uint8, device=dev)
+
+    def call():
+        return L.mx_linear_wgrad(ptr(dY), ptr(X), ptr(dW), T, N, K, rot, nb, rnd, seed, ptr(ws),
+                                 ws.numel(), sp)
+
+    for _ in range(warmup):
+        flush.zero_()
+        if call():
+            raise RuntimeError(f"{name}: launch failed")
     for i in range(steps):
         flush.zero_()
         whole[i][0].record(stream)
-        if any(parts()):
+        if call():
             raise RuntimeError(f"{name}: launch failed")
         whole[i][1].record(stream)
     for i in range(steps):
@@ -605,11 +634,52 @@ def measure_side_workload(L, mx, name, dev, stream, flush, steps, warmup, fp4_me
                         f"{mode_text()}",
             "steps": steps, "ms_per_step": t_step,
             "value": flops / (t_step * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "step_launches": 2,
             "breakdown_ms": {"quantize_pair": t_q, "gemm": t_g},
             "gemm_tflops": flops / (t_g * 1e-3) / 1e12,
             "gemm_frac_fp4_measured": flops / (t_g * 1e-3) / 1e12 / fp4_meas["tflops"],
             "quantizer_gbs": qbytes / (t_q * 1e-3) / 1e9,
             "quantizer_frac_hbm": qbytes / (t_q * 1e-3) / 1e9 / hbm}
+
+
+def measure_fused(L, mx, dY, X, dW, T, N, K, flush, stream, dev, step_ms, fp4_meas, reps=50):
+    """mx_linear_wgrad_fused (the encode inside the GEMM's launch) on the
+    headline workload: time per call (L2 flushed before each) beside the
+    two-launch step, and whether its output has the same bits."""
+    import torch
+    rot, nb, rnd, seed = mode_args()
+    if not L.mx_linear_wgrad_fused_supported(T, N, K, rot, nb, rnd):
+        return {"call": "mx_linear_wgrad_fused", "supported": False}
+    sp = stream.cuda_stream
+    ptr = lambda t: t.data_ptr()
+    ws = torch.empty(mx.linear_workspace_bytes(mx.OP_WGRAD, T, N, K), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(dW)
+
+    def call():
+        st = L.mx_linear_wgrad_fused(ptr(dY), ptr(X), ptr(out), T, N, K, rot, nb, rnd, seed,
+                                     ptr(ws), ws.numel(), sp)
+        if st != 0:
+            raise RuntimeError(f"mx_linear_wgrad_fused: {mx.status_string(st)}")
+    for _ in range(3):
+        flush.zero_()
+        call()
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ts.append(e0.elapsed_time(e1))
+    mx.check_status()
+    t = sorted(ts)[len(ts) // 2]
+    same = bool(torch.equal(out.view(torch.int32), dW.view(torch.int32)))
+    two = sorted(step_ms)[len(step_ms) // 2]
+    return {"call": "mx_linear_wgrad_fused", "supported": True, "ms": t, "median_of": reps,
+            "tflops": 2.0 * N * K * T / (t * 1e-3) / 1e12,
+            "two_launch_step_ms_median": two,
+            "bitwise_equal_to_two_launch_step": same}
 
 
 def measure_dual(L, mx, dY, T, N, flush, stream, dev, hbm_gbs, reps=30):

@@ -199,6 +199,29 @@ mx_status mx_linear_wgrad(const void *d_dY, const void *d_X, float *d_dW, int64_
                           int64_t N, int64_t K, int rot, int rot_block, int rnd, uint64_t seed,
                           void *d_ws, size_t ws_bytes, void *stream);
 
+/*
+ * mx_linear_wgrad_fused -- mx_linear_wgrad as ONE launch: encoder warps in
+ * the GEMM's own CTAs encode dY and X into the workspace chunk by chunk
+ * (in the order the GEMM first needs them) while the tensor cores consume
+ * what is ready; per (256-line panel, 512-token chunk) counters in the
+ * workspace, zeroed by a small memset before the launch, tell the GEMM's
+ * producers when a stage's operands are stored.  Same arguments, workspace
+ * size and results (the same bits) as mx_linear_wgrad.  Covers
+ * round-to-nearest with no rotation or the deterministic Hadamard of 16 or
+ * 32, T a multiple of 512 and N, K multiples of 256; other arguments get
+ * MX_ERR_UNSUPPORTED (nothing launched).  On GB300 it is SLOWER than
+ * mx_linear_wgrad's two launches (the encoder warps and the GEMM compete
+ * for the same memory path, and shared memory is full with GEMM stages), so
+ * mx_linear_wgrad does not use it.  No counterpart in the pages (the fusion
+ * of the encode into the GEMM is a scheduling choice).
+ * mx_linear_wgrad_fused_supported() returns 1 for arguments it covers.
+ */
+mx_status mx_linear_wgrad_fused(const void *d_dY, const void *d_X, float *d_dW, int64_t T,
+                                int64_t N, int64_t K, int rot, int rot_block, int rnd,
+                                uint64_t seed, void *d_ws, size_t ws_bytes, void *stream);
+int mx_linear_wgrad_fused_supported(int64_t T, int64_t N, int64_t K, int rot, int rot_block,
+                                    int rnd);
+
 /* mx_linear_fprop -- Y[T][N] = X W^T, contraction K (K % 32 == 0, N % 4 == 0). */
 mx_status mx_linear_fprop(const void *d_X, const void *d_W, float *d_Y, int64_t T, int64_t N,
                           int64_t K, int rot, int rot_block, int rnd, uint64_t seed,

@@ -10,7 +10,7 @@ from ._binding import (CONTRACT_COLS, CONTRACT_ROWS, OP_DGRAD, OP_FPROP, OP_WGRA
                        ROT_HADAMARD_RAND, ROT_NONE, ROUND_RNE, ROUND_SR, MMA_KINDS, MXError, bench_mma,
                        check_status,
                        codes_bytes, debug_timeout_probe, gemm, gemm_into, lib, library_path,
-                       linear_dgrad, linear_fprop, linear_wgrad, linear_wgrad_noalloc,
+                       linear_dgrad, linear_fprop, linear_wgrad, linear_wgrad_fused, linear_wgrad_noalloc,
                        linear_workspace_bytes, NOALLOC_SCRATCH_BYTES, quantize, quantize_dual,
                        quantize_pair, quantize_into, scales_bytes, scales_to_canonical,
                        status_string)
@@ -20,7 +20,7 @@ __all__ = [
     "ROT_HADAMARD_RAND", "ROT_NONE", "ROUND_RNE", "ROUND_SR", "MMA_KINDS", "MXError", "bench_mma",
     "check_status",
     "codes_bytes", "debug_timeout_probe", "gemm", "gemm_into", "lib", "library_path",
-    "linear_dgrad", "linear_fprop", "linear_wgrad", "linear_wgrad_noalloc", "linear_workspace_bytes",
+    "linear_dgrad", "linear_fprop", "linear_wgrad", "linear_wgrad_fused", "linear_wgrad_noalloc", "linear_workspace_bytes",
     "NOALLOC_SCRATCH_BYTES", "quantize", "quantize_dual", "quantize_pair",
     "quantize_into", "scales_bytes", "scales_to_canonical", "status_string",
 ]

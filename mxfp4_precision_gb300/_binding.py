@@ -24,6 +24,7 @@ EXPORTED = [
     "mx_codes_bytes", "mx_scales_bytes", "mx_scales_to_canonical", "mx_quantize", "mx_quantize_pair", "mx_quantize_dual",
     "mx_gemm", "mx_linear_workspace_bytes",
     "mx_linear_wgrad", "mx_linear_fprop", "mx_linear_dgrad", "mx_linear_wgrad_noalloc",
+    "mx_linear_wgrad_fused", "mx_linear_wgrad_fused_supported",
     "mx_check_status",
     "mx_debug_timeout_probe", "mx_bench_mma", "mx_status_string", "mx_version",
 ]
@@ -77,6 +78,10 @@ def lib() -> ctypes.CDLL:
                 fn.restype = i32
             L.mx_linear_wgrad_noalloc.argtypes = [P, P, P, i64, i64, i64, i32, i32, i32, u64, P]
             L.mx_linear_wgrad_noalloc.restype = i32
+            L.mx_linear_wgrad_fused.argtypes = [P, P, P, i64, i64, i64, i32, i32, i32, u64, P, sz, P]
+            L.mx_linear_wgrad_fused.restype = i32
+            L.mx_linear_wgrad_fused_supported.argtypes = [i64, i64, i64, i32, i32, i32]
+            L.mx_linear_wgrad_fused_supported.restype = i32
             L.mx_check_status.argtypes = [P]
             L.mx_check_status.restype = i32
             L.mx_debug_timeout_probe.argtypes = [i64, P]
@@ -239,6 +244,16 @@ def linear_wgrad(dY, X, rot=ROT_HADAMARD_DET, rot_block=32, rnd=ROUND_RNE, seed=
 
 
 NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def linear_wgrad_fused(dY, X, rot=ROT_HADAMARD_DET, rot_block=32, rnd=ROUND_RNE, seed=0, ws=None,
+                       out=None, stream=None) -> torch.Tensor:
+    """mx_linear_wgrad as one launch (encoder warps inside the GEMM); same
+    result bits.  Raises MXError(MX_ERR_UNSUPPORTED) outside its modes."""
+    T, N = dY.shape
+    K = X.shape[1]
+    return _linear("mx_linear_wgrad_fused", OP_WGRAD, dY, X, (N, K), T, N, K, rot, rot_block, rnd,
+                   seed, ws, out, stream)
 
 
 def linear_wgrad_noalloc(dY, X, rot=ROT_HADAMARD_DET, rot_block=32, rnd=ROUND_RNE, seed=0,

@@ -231,7 +231,8 @@ mx_status gemm_impl(const void *Aq, const void *As, const void *Bq, const void *
 mx_status linear_impl(int op, const void *a_src, int64_t a_rows, int64_t a_cols, int a_contract,
                       const void *b_src, int64_t b_rows, int64_t b_cols, int b_contract, float *out,
                       int64_t T, int64_t N, int64_t K, int rot, int rot_block, int rnd,
-                      uint64_t seed, void *ws, size_t ws_bytes, cudaStream_t stream) {
+                      uint64_t seed, void *ws, size_t ws_bytes, cudaStream_t stream,
+                      bool fused = false) {
     OpShape s;
     if (!op_shape(op, T, N, K, &s)) return MX_ERR_INVALID_ARG;
     if (T < 0 || N < 0 || K < 0) return MX_ERR_SHAPE;
@@ -256,6 +257,18 @@ mx_status linear_impl(int op, const void *a_src, int64_t a_rows, int64_t a_cols,
     uint8_t *bq = p;
     p += align256(mx_codes_bytes(s.b_lines, s.k));
     uint8_t *bs = p;
+    if (fused) {
+        // One launch: the GEMM's own encoder warps encode both operands while
+        // it runs (its chunk counters, after the operands in the workspace,
+        // are zeroed first).
+        if (op != MX_OP_WGRAD || !wgrad_fusable(T, N, K, rot, rot_block, rnd))
+            return MX_ERR_UNSUPPORTED;
+        const DeviceInfo *dev = nullptr;
+        if ((st = device_or_error(&dev)) != MX_OK) return st;
+        uint8_t *counters = bs + align256(mx_scales_bytes(s.b_lines, s.k));
+        return from_cuda(launch_wgrad_fused(a_src, b_src, out, T, N, K, rot, rot_block, aq, as, bq,
+                                            bs, counters, *dev, stream));
+    }
     if (a_contract == MX_CONTRACT_ROWS && b_contract == MX_CONTRACT_ROWS) {
         // Wgrad: both operands encoded down their rows in a single launch.
         st = quantize_pair_impl(a_src, a_rows, a_cols, b_src, b_rows, b_cols, rot, rot_block, rnd,
@@ -343,8 +356,11 @@ mx_status mx_gemm(const void *d_Aq, const void *d_As, const void *d_Bq, const vo
 size_t mx_linear_workspace_bytes(int op, int64_t T, int64_t N, int64_t K) {
     OpShape s;
     if (!op_shape(op, T, N, K, &s)) return 0;
-    return align256(mx_codes_bytes(s.a_lines, s.k)) + align256(mx_scales_bytes(s.a_lines, s.k)) +
-           align256(mx_codes_bytes(s.b_lines, s.k)) + align256(mx_scales_bytes(s.b_lines, s.k));
+    size_t bytes = align256(mx_codes_bytes(s.a_lines, s.k)) + align256(mx_scales_bytes(s.a_lines, s.k)) +
+                   align256(mx_codes_bytes(s.b_lines, s.k)) + align256(mx_scales_bytes(s.b_lines, s.k));
+    // Wgrad: room for the fused launch's (panel, chunk) counters.
+    if (op == MX_OP_WGRAD && T > 0 && N > 0 && K > 0) bytes += align256(wgrad_fused_counter_bytes(T, N, K));
+    return bytes;
 }
 
 mx_status mx_linear_wgrad(const void *d_dY, const void *d_X, float *d_dW, int64_t T, int64_t N,
@@ -375,6 +391,20 @@ mx_status mx_linear_dgrad(const void *d_dY, const void *d_W, float *d_dX, int64_
     return linear_impl(MX_OP_DGRAD, d_dY, T, N, MX_CONTRACT_COLS, d_W, N, K, MX_CONTRACT_ROWS,
                        d_dX, T, N, K, rot, rot_block, rnd, seed, d_ws, ws_bytes,
                        static_cast<cudaStream_t>(stream));
+}
+
+int mx_linear_wgrad_fused_supported(int64_t T, int64_t N, int64_t K, int rot, int rot_block,
+                                    int rnd) {
+    return wgrad_fusable(T, N, K, rot, rot_block, rnd) ? 1 : 0;
+}
+
+mx_status mx_linear_wgrad_fused(const void *d_dY, const void *d_X, float *d_dW, int64_t T,
+                                int64_t N, int64_t K, int rot, int rot_block, int rnd,
+                                uint64_t seed, void *d_ws, size_t ws_bytes, void *stream) {
+    TraceRange trace("mx_linear_wgrad_fused");
+    return linear_impl(MX_OP_WGRAD, d_dY, T, N, MX_CONTRACT_ROWS, d_X, T, K, MX_CONTRACT_ROWS,
+                       d_dW, T, N, K, rot, rot_block, rnd, seed, d_ws, ws_bytes,
+                       static_cast<cudaStream_t>(stream), true);
 }
 
 mx_status mx_check_status(void *stream) {

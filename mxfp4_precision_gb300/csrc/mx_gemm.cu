@@ -44,7 +44,9 @@
 #include <cstring>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <vector>
 
+#include "mx_encode.cuh"
 #include "mx_internal.h"
 #include "mx_ptx.cuh"
 
@@ -56,15 +58,26 @@ constexpr int kHalf = 128;                        // rows of A / of B per CTA
 constexpr int kBKBytes = 128;                     // 256 FP4 per row per K sub-tile
 constexpr int kKSub = 2;                          // K sub-tiles per stage (K = 512)
 constexpr int kStages = 3;
-constexpr int kThreads = 512;                     // 16 warps
 constexpr int kWriterWarp0 = 4;                   // warps 4..7: scale writers
 constexpr int kEpiWarp0 = 8;                      // warps 8..15: epilogue
 constexpr int kEpiWarps = 8;
-// Register split (setmaxnreg): 512 threads x 128 launch registers =
-// 256 threads x kRegsLow (producers, MMA, scale writers) + 256 x kRegsHigh.
-constexpr int kRegsLow = 56;
-constexpr int kRegsHigh = 200;
-static_assert(256 * kRegsLow + 256 * kRegsHigh <= kThreads * 128, "register split fits the launch");
+constexpr int kEncWarp0 = 16;                     // fused launch: warps 16..23 encode
+constexpr int kEncWarps = 8;
+// Threads and register split (setmaxnreg) of the two variants.  GEMM alone:
+// 512 threads x 128 launch registers = 256 x kRegsLow (producers, MMA, scale
+// writers) + 256 x kRegsHigh (epilogue, whole accumulator half in registers).
+// Fused Wgrad: 768 x 80 = 256 x 48 + 256 x 96 (epilogue, two passes of 64
+// columns) + 256 x 96 (encoder warps).
+template <bool FUSED>
+struct Variant {
+    static constexpr int kThreads = FUSED ? 768 : 512;
+    static constexpr int kLaunchRegs = FUSED ? 80 : 128;
+    static constexpr int kRegsLow = FUSED ? 48 : 56;
+    static constexpr int kRegsHigh = FUSED ? 96 : 200;
+    static_assert(256 * kRegsLow + (kThreads - 256) * kRegsHigh <= kThreads * kLaunchRegs,
+                  "register split fits the launch");
+    static_assert(kThreads * kLaunchRegs <= 65536, "launch registers fit the SM");
+};
 constexpr uint32_t kSubBytes = kHalf * kBKBytes;  // 16 KB: 128 rows x one K sub-tile
 constexpr uint32_t kSFSub = 1024;                 // scales of 128 rows x one K sub-tile
 constexpr uint32_t kOffA = 0;
@@ -77,6 +90,37 @@ constexpr uint32_t kAccCol = 0;                    // accumulator: columns [0, 2
 constexpr uint32_t kSFCol = 256;                   // scale slots: 24 columns per K sub-tile
 constexpr uint32_t kSFSlot = 24 * kKSub;
 static_assert(kSFCol + kStages * kSFSlot <= kTmemCols, "scale slots fit in tensor memory");
+
+// Fused Wgrad: the encoder warps of every CTA encode both operands (dY
+// [T][N], X [T][K], contraction T) into the workspace while the GEMM runs.
+// Units of work: (panel of 256 lines, chunk of 512 tokens, quarter of 64
+// lines, slice of 64 tokens).  Units run in the order the GEMM first needs
+// them: the panels a round of tiles touches for the first time form a group,
+// encoded chunk by chunk, and consecutive units go to warps of different
+// CTAs, so a chunk is spread over the whole GPU and done early.  A (panel,
+// chunk) counter in the workspace (zeroed before the launch) reaches
+// kUnitsPerChunk when all its units are stored; the GEMM's producers wait
+// for it before loading that stage.
+constexpr int kMaxPanels = 512;
+constexpr int kMaxGroups = 128;
+constexpr int kSlices = 8;                        // 64-token slices of a 512-token chunk
+constexpr int kUnitsPerChunk = 4 * kSlices;       // quarters x slices
+struct FusedArgs {
+    const uint32_t *src[2];     // dY, X as 32-bit words (two bf16 channels each)
+    uint8_t *codes[2];          // [lines][T/2]
+    uint8_t *scales[2];         // tiled layout
+    int64_t words_per_row[2];   // N / 2, K / 2
+    int64_t T;
+    int64_t katoms;             // scale k-atoms per 128-line group (contraction T)
+    unsigned int *counters;     // [panel][chunk], zero at launch
+    int rot_block;              // 0 (no rotation), 16 or 32
+    int chunks;                 // T / 512
+    int panels_a;               // A panels come first in the global panel index
+    int groups;
+    int units;                  // kUnitsPerChunk * chunks * panels
+    uint16_t group_start[kMaxGroups + 1];
+    uint16_t panel[kMaxPanels]; // global panel indices in first-use order
+};
 
 struct GemmArgs {
     const uint8_t *As;
@@ -201,9 +245,90 @@ __device__ __forceinline__ bool wait_issued(const SharedCtl *ctl, int target, in
     return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+// Bounded wait until (panel, chunk) counter `ctr` reaches `want` (acquire
+// at GPU scope), then a proxy fence so that the TMA reads see what the
+// encoder warps (generic stores on other SMs) wrote.
+__device__ __forceinline__ bool wait_encoded(const unsigned int *ctr, unsigned int want,
+                                             int *status, volatile int *abort) {
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        unsigned int v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+        if (v >= want) break;
+        if (*abort) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            atomicExch(status, kDevTimeout);
+            *abort = 1;
+            return false;
+        }
+        __nanosleep(64);
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
+}
+
+// Encoder warp of the fused Wgrad launch: units gw, gw + W, ... .  Each lane
+// owns two adjacent lines (channels) and 32 tokens per step: 32 coalesced
+// 128-byte warp loads straight from global memory (the transpose is the
+// lane's own column read), then the same rotation and encode as the
+// stand-alone column encoder (enc::fwht_pairs, enc::encode_pair_rne).
+template <int ROTN>
+__device__ __forceinline__ void encode_units(const FusedArgs &f, int gw, int W, int *status,
+                                             volatile int *abort) {
+    const int lane = threadIdx.x & 31;
+    const float cn = ROTN > 0 ? enc::hadamard_norm<ROTN>() : 1.0f;
+    for (int u = gw; u < f.units; u += W) {
+        if (__shfl_sync(0xFFFFFFFFu, *abort, 0)) return;
+        int gi = 0;
+        while (gi + 1 < f.groups && kUnitsPerChunk * f.chunks * f.group_start[gi + 1] <= u) ++gi;
+        const int gp = f.group_start[gi + 1] - f.group_start[gi];
+        const int r = u - kUnitsPerChunk * f.chunks * f.group_start[gi];
+        const int chunk = r / (kUnitsPerChunk * gp);
+        const int rem = r % (kUnitsPerChunk * gp);
+        const int gpanel = f.panel[f.group_start[gi] + rem / kUnitsPerChunk];
+        const int quarter = (rem % kUnitsPerChunk) / kSlices;
+        const int slice = rem % kSlices;
+        const int o = gpanel >= f.panels_a ? 1 : 0;
+        const int64_t pn = gpanel - (o ? f.panels_a : 0);
+        const int64_t c = pn * 256 + quarter * 64 + 2 * lane;   // first of the lane's two lines
+        const int64_t wpr = f.words_per_row[o];
+        const uint32_t *src = f.src[o] + c / 2;
+        uint8_t *codes = f.codes[o];
+        uint8_t *scales = f.scales[o];
+#pragma unroll 1
+        for (int step = 0; step < 2; ++step) {
+            const int64_t t0 = static_cast<int64_t>(chunk) * 512 + 64 * slice + 32 * step;
+            uint64_t x[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const uint32_t v = __ldg(src + (t0 + i) * wpr);
+                x[i] = enc::pack2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+            }
+            if (ROTN > 0) enc::fwht_pairs<ROTN>(x);
+            uint4 q0, q1;
+            uint32_t s0, s1;
+            enc::encode_pair_rne<(ROTN > 0)>(x, cn, q0, q1, s0, s1);
+            enc::st_global_16(codes + c * (f.T / 2) + t0 / 2, q0);
+            enc::st_global_16(codes + (c + 1) * (f.T / 2) + t0 / 2, q1);
+            scales[enc::scale_offset(c, t0 / 32, f.katoms)] = static_cast<uint8_t>(s0);
+            scales[enc::scale_offset(c + 1, t0 / 32, f.katoms)] = static_cast<uint8_t>(s1);
+        }
+        // Every lane makes its stores visible at GPU scope, then lane 0
+        // counts the unit once all lanes are past their fence (a shuffle as
+        // the convergence point: bar.warp.sync here defeats ptxas's register
+        // split).
+        __threadfence();
+        if (__shfl_sync(0xFFFFFFFFu, lane, 0) == 0 && lane == 0)
+            atomicAdd(f.counters + static_cast<int64_t>(gpanel) * f.chunks + chunk, 1u);
+    }
+}
+
+template <bool FUSED>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
-                   const __grid_constant__ CUtensorMap map_b, const GemmArgs g) {
+                   const __grid_constant__ CUtensorMap map_b, const GemmArgs g,
+                   const __grid_constant__ FusedArgs f) {
+    using V = Variant<FUSED>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned base, kept as a shared-space pointer (offset arithmetic
     // only) so that the compiler emits shared-memory loads.  The offset is the
@@ -249,7 +374,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     if (warp < kWriterWarp0) {
         // Warpgroup 0: producers and the MMA issuer need few registers.
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow) : "memory");
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(V::kRegsLow) : "memory");
         if ((warp == 0 || warp == 2) && lane == 0) {
             // ------------------------------------------------------------ producers
             const bool scales = warp == 2;
@@ -269,6 +394,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const int kt0 = ks * kKSub;
                     const int nsub = g.k_tiles - kt0 < kKSub ? g.k_tiles - kt0 : kKSub;
                     uint8_t *st = smem + stage * kStageBytes;
+                    if constexpr (FUSED) {
+                        // This stage's 512 tokens of both panels are encoded.
+                        const unsigned int want = kUnitsPerChunk;
+                        if (!wait_encoded(f.counters + static_cast<int64_t>(mb) * f.chunks + ks,
+                                          want, g.status, abort) ||
+                            !wait_encoded(f.counters +
+                                              static_cast<int64_t>(f.panels_a + nb) * f.chunks + ks,
+                                          want, g.status, abort)) {
+                            ok = false;
+                            break;
+                        }
+                    }
                     if (scales) {
                         uint32_t bytes = 0;
                         if (ga < g.a_groups) bytes += static_cast<uint32_t>(nsub) * kSFSub;
@@ -360,7 +497,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
     } else if (warp < kEpiWarp0) {
         // ------------------------------------------------------------ scale writers
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow) : "memory");
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(V::kRegsLow) : "memory");
         // Tensor-memory scale layout of one K sub-tile (24 columns, as the
         // tcgen05.mma block-scale path reads it), the same in every lane
         // quarter q: for k-atom ka (4 blocks of 32), A row 32*c + r of this
@@ -429,9 +566,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
         }
-    } else {
+    } else if (!FUSED || warp < kEncWarp0) {
         // ------------------------------------------------------------ epilogue
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh) : "memory");
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(V::kRegsHigh) : "memory");
         const int q = warp & 3;                   // TMEM lane quarter this warp may access
         const int half = (warp - kEpiWarp0) / 4;  // column half of the 256-wide tile
         uint32_t acc_phase = 0;
@@ -451,6 +588,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             acc_phase ^= 1u;
             const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + kAccCol +
                                    128u * static_cast<uint32_t>(half);
+            if constexpr (FUSED) {
+                // Two passes of 64 columns (the encoder warps need the
+                // registers): the first pass is stored at once, the second
+                // after tensor memory is released, paced like below.
+                const int64_t row =
+                    static_cast<int64_t>(mb) * kTile + kHalf * rank + 32 * q + lane;
+                float *crow = g.C + row * g.N;
+                const int64_t col0 = static_cast<int64_t>(nb) * kTile + 128 * half;
+                const int next = w + npairs;
+                uint32_t v0[32], v1[32];
+                tmem_ld_32x32b_x32(tbase, v0);
+                tmem_ld_32x32b_x32(tbase + 32u, v1);
+                tmem_ld_wait();
+                if (row < g.M) {
+                    store_row32(g, crow, col0, v0);
+                    store_row32(g, crow, col0 + 32, v1);
+                }
+                tmem_ld_32x32b_x32(tbase + 64u, v0);
+                tmem_ld_32x32b_x32(tbase + 96u, v1);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) arrive_even(&ctl->acc_empty);
+                if (next < g.num_items && g.c_v8 && col0 + 127 < g.N) {
+                    const Item nx = item_of(g, next);
+                    const int ns = nx.ks1 - nx.ks0;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int need = 1 + (j * ns) / 8;
+                        if (j == 0 || need != 1 + ((j - 1) * ns) / 8)
+                            if (!wait_issued(ctl, staged + need, g.status, abort)) break;
+                        const uint32_t *src = j < 4 ? &v0[8 * j] : &v1[8 * (j - 4)];
+                        if (row < g.M &&
+                            MX_STORE_OK(crow + col0 + 64 + 8 * j, 32, g.C, g.c_bytes, g.status))
+                            st_global_v8(crow + col0 + 64 + 8 * j, src);
+                    }
+                } else if (row < g.M) {
+                    store_row32(g, crow, col0 + 64, v0);
+                    store_row32(g, crow, col0 + 96, v1);
+                }
+                continue;
+            }
             uint32_t v0[32], v1[32], v2[32], v3[32];
             tmem_ld_32x32b_x32(tbase, v0);
             tmem_ld_32x32b_x32(tbase + 32u, v1);
@@ -491,6 +670,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 store_row32(g, crow, col0 + 96, v3);
             }
         }
+    } else if constexpr (FUSED) {
+        // ------------------------------------------------------------ encoder
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(V::kRegsHigh) : "memory");
+        const int gw = (warp - kEncWarp0) * gridDim.x + blockIdx.x;
+        const int W = gridDim.x * kEncWarps;
+        if (f.rot_block == 32)
+            encode_units<32>(f, gw, W, g.status, abort);
+        else if (f.rot_block == 16)
+            encode_units<16>(f, gw, W, g.status, abort);
+        else
+            encode_units<0>(f, gw, W, g.status, abort);
     }
 
     __syncwarp();
@@ -508,22 +698,82 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 constexpr size_t kGemmSmem = kStages * kStageBytes + sizeof(SharedCtl) + 1024;
 
-// Co-resident 2-CTA clusters of mx_gemm_kernel on a device, measured once.
+// Co-resident 2-CTA clusters of a mx_gemm_kernel variant on a device,
+// measured once.
+template <bool FUSED>
 int gemm_clusters(const DeviceInfo &dev) {
     static std::atomic<int> cache[64];
     const int idx = dev.ordinal >= 0 && dev.ordinal < 64 ? dev.ordinal : 0;
     int n = cache[idx].load(std::memory_order_relaxed);
     if (n > 0) return n;
-    if (cudaFuncSetAttribute(mx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(mx_gemm_kernel<FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kGemmSmem)) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(Variant<FUSED>::kThreads, 1, 1);
     cfg.dynamicSmemBytes = kGemmSmem;
-    if (cudaOccupancyMaxActiveClusters(&n, mx_gemm_kernel, &cfg) != cudaSuccess || n < 1) return 0;
+    if (cudaOccupancyMaxActiveClusters(&n, mx_gemm_kernel<FUSED>, &cfg) != cudaSuccess || n < 1)
+        return 0;
     cache[idx].store(n, std::memory_order_relaxed);
     return n;
+}
+
+// Common set-up of both variants: tensor maps and the GEMM arguments.
+bool gemm_setup(const void *Aq, const void *As, const void *Bq, const void *Bs, float *C,
+                int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, CUtensorMap *map_a,
+                CUtensorMap *map_b, GemmArgs *g) {
+    if (!encode_tmap_2d(map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, Aq, K / 2, M, K / 2, kBKBytes, kHalf,
+                        CU_TENSOR_MAP_SWIZZLE_128B))
+        return false;
+    if (!encode_tmap_2d(map_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, Bq, K / 2, N, K / 2, kBKBytes, kHalf,
+                        CU_TENSOR_MAP_SWIZZLE_128B))
+        return false;
+    *g = GemmArgs{};
+    g->As = static_cast<const uint8_t *>(As);
+    g->Bs = static_cast<const uint8_t *>(Bs);
+    g->C = C;
+    g->M = M;
+    g->N = N;
+    g->K = K;
+    g->katoms = scale_katoms(K);
+    g->a_groups = scale_groups(M);
+    g->b_groups = scale_groups(N);
+    g->k_tiles = static_cast<int>((K + 255) / 256);
+    g->k_stages = (g->k_tiles + kKSub - 1) / kKSub;
+    const int64_t m_tiles = (M + kTile - 1) / kTile;
+    const int64_t n_tiles = (N + kTile - 1) / kTile;
+    if (m_tiles * n_tiles > 0x3FFFFFFF) return false;
+    g->m_tiles = static_cast<int>(m_tiles);
+    g->n_tiles = static_cast<int>(n_tiles);
+    g->num_tiles = static_cast<int>(m_tiles * n_tiles);
+    g->num_items = g->num_tiles;
+    g->c_v8 = (N % 8 == 0 && (reinterpret_cast<uintptr_t>(C) & 31) == 0) ? 1 : 0;
+    g->c_bytes = static_cast<size_t>(M) * static_cast<size_t>(N) * sizeof(float);
+    g->status = dev.status;
+    return true;
+}
+
+template <bool FUSED>
+cudaError_t gemm_launch(const CUtensorMap &map_a, const CUtensorMap &map_b, const GemmArgs &g,
+                        const FusedArgs &f, int pairs, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel<FUSED>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kGemmSmem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2 * pairs, 1, 1);
+    cfg.blockDim = dim3(Variant<FUSED>::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kGemmSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, mx_gemm_kernel<FUSED>, map_a, map_b, g, f);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -532,54 +782,92 @@ cudaError_t launch_gemm(const void *Aq, const void *As, const void *Bq, const vo
                         int64_t M, int64_t N, int64_t K, const DeviceInfo &dev,
                         cudaStream_t stream) {
     CUtensorMap map_a, map_b;
-    if (!encode_tmap_2d(&map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, Aq, K / 2, M, K / 2, kBKBytes,
-                        kHalf, CU_TENSOR_MAP_SWIZZLE_128B))
+    GemmArgs g;
+    if (!gemm_setup(Aq, As, Bq, Bs, C, M, N, K, dev, &map_a, &map_b, &g))
         return cudaErrorInvalidValue;
-    if (!encode_tmap_2d(&map_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, Bq, K / 2, N, K / 2, kBKBytes,
-                        kHalf, CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
-    GemmArgs g{};
-    g.As = static_cast<const uint8_t *>(As);
-    g.Bs = static_cast<const uint8_t *>(Bs);
-    g.C = C;
-    g.M = M;
-    g.N = N;
-    g.K = K;
-    g.katoms = scale_katoms(K);
-    g.a_groups = scale_groups(M);
-    g.b_groups = scale_groups(N);
-    g.k_tiles = static_cast<int>((K + 255) / 256);
-    g.k_stages = (g.k_tiles + kKSub - 1) / kKSub;
-    const int64_t m_tiles = (M + kTile - 1) / kTile;
-    const int64_t n_tiles = (N + kTile - 1) / kTile;
-    if (m_tiles * n_tiles > 0x3FFFFFFF) return cudaErrorInvalidValue;
-    g.m_tiles = static_cast<int>(m_tiles);
-    g.n_tiles = static_cast<int>(n_tiles);
-    g.num_tiles = static_cast<int>(m_tiles * n_tiles);
-    g.c_v8 = (N % 8 == 0 && (reinterpret_cast<uintptr_t>(C) & 31) == 0) ? 1 : 0;
-    g.c_bytes = static_cast<size_t>(M) * static_cast<size_t>(N) * sizeof(float);
-    g.status = dev.status;
-    cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kGemmSmem));
-    if (e != cudaSuccess) return e;
-    // Resident CTAs: as many 2-CTA clusters as fit at once, one item per pair.
-    const int pairs_max = gemm_clusters(dev);
+    // Resident CTAs: as many 2-CTA clusters as fit at once, one tile per pair.
+    const int pairs_max = gemm_clusters<false>(dev);
     if (pairs_max < 1) return cudaErrorLaunchOutOfResources;
-    g.num_items = g.num_tiles;
     const int pairs = g.num_items < pairs_max ? g.num_items : pairs_max;
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(2 * pairs, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kGemmSmem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, mx_gemm_kernel, map_a, map_b, g);
+    FusedArgs f;
+    std::memset(&f, 0, sizeof(f));
+    return gemm_launch<false>(map_a, map_b, g, f, pairs, stream);
+}
+
+size_t wgrad_fused_counter_bytes(int64_t T, int64_t N, int64_t K) {
+    return static_cast<size_t>(4) * static_cast<size_t>((N + 255) / 256 + (K + 255) / 256) *
+           static_cast<size_t>((T + 511) / 512);
+}
+
+bool wgrad_fusable(int64_t T, int64_t N, int64_t K, int rot, int rot_block, int rnd) {
+    if (rnd != 0) return false;                               // round to nearest only
+    if (rot == 2) return false;                               // no random signs
+    if (rot == 1 && rot_block != 16 && rot_block != 32) return false;
+    if (T < 512 || T % 512 != 0 || N < 256 || N % 256 != 0 || K < 256 || K % 256 != 0)
+        return false;
+    if (N / 256 + K / 256 > kMaxPanels) return false;
+    return true;
+}
+
+cudaError_t launch_wgrad_fused(const void *dY, const void *X, float *dW, int64_t T, int64_t N,
+                               int64_t K, int rot, int rot_block, void *Aq, void *As, void *Bq,
+                               void *Bs, void *counters, const DeviceInfo &dev,
+                               cudaStream_t stream) {
+    CUtensorMap map_a, map_b;
+    GemmArgs g;
+    // dW[N][K] = A . B^T with A = dY^T (N lines), B = X^T (K lines), contraction T.
+    if (!gemm_setup(Aq, As, Bq, Bs, dW, N, K, T, dev, &map_a, &map_b, &g))
+        return cudaErrorInvalidValue;
+    const int pairs_max = gemm_clusters<true>(dev);
+    if (pairs_max < 1) return cudaErrorLaunchOutOfResources;
+    const int pairs = g.num_items < pairs_max ? g.num_items : pairs_max;
+
+    FusedArgs f;
+    std::memset(&f, 0, sizeof(f));
+    f.src[0] = static_cast<const uint32_t *>(dY);
+    f.src[1] = static_cast<const uint32_t *>(X);
+    f.codes[0] = static_cast<uint8_t *>(Aq);
+    f.codes[1] = static_cast<uint8_t *>(Bq);
+    f.scales[0] = static_cast<uint8_t *>(As);
+    f.scales[1] = static_cast<uint8_t *>(Bs);
+    f.words_per_row[0] = N / 2;
+    f.words_per_row[1] = K / 2;
+    f.T = T;
+    f.katoms = scale_katoms(T);
+    f.counters = static_cast<unsigned int *>(counters);
+    f.rot_block = rot == 0 ? 0 : rot_block;
+    f.chunks = static_cast<int>(T / 512);
+    f.panels_a = g.m_tiles;
+    // First-use order of the panels: walk the tiles round by round (one tile
+    // per pair per round, in the kernel's banded order).
+    std::vector<char> seen(static_cast<size_t>(g.m_tiles + g.n_tiles), 0);
+    int np = 0, ng = 0;
+    for (int r0 = 0; r0 < g.num_tiles; r0 += pairs) {
+        const int start = np;
+        for (int pass = 0; pass < 2; ++pass)
+            for (int t = r0; t < g.num_tiles && t < r0 + pairs; ++t) {
+                const int per_band = kBand * g.n_tiles;
+                const int band = t / per_band, rr = t % per_band;
+                const int first = band * kBand;
+                const int rows = g.m_tiles - first < kBand ? g.m_tiles - first : kBand;
+                const int p = pass == 0 ? first + rr % rows : g.m_tiles + rr / rows;
+                if (!seen[p]) {
+                    seen[p] = 1;
+                    if (np >= kMaxPanels) return cudaErrorNotSupported;
+                    f.panel[np++] = static_cast<uint16_t>(p);
+                }
+            }
+        if (np > start) {
+            if (ng >= kMaxGroups) return cudaErrorNotSupported;
+            f.group_start[ng++] = static_cast<uint16_t>(start);
+        }
+    }
+    f.group_start[ng] = static_cast<uint16_t>(np);
+    f.groups = ng;
+    f.units = kUnitsPerChunk * f.chunks * np;
+    cudaError_t e = cudaMemsetAsync(counters, 0, wgrad_fused_counter_bytes(T, N, K), stream);
     if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    return gemm_launch<true>(map_a, map_b, g, f, pairs, stream);
 }
 
 }  // namespace mx

@@ -54,4 +54,15 @@ cudaError_t launch_gemm(const void *Aq, const void *As, const void *Bq, const vo
                         int64_t M, int64_t N, int64_t K, const DeviceInfo &dev,
                         cudaStream_t stream);
 
+// Fused Wgrad: one launch whose encoder warps encode dY and X (contraction
+// T) into Aq/As/Bq/Bs while the GEMM consumes them; `counters` is
+// wgrad_fused_counter_bytes(T, N, K) of workspace (any contents).  Only for
+// the shapes and modes wgrad_fusable() accepts.
+bool wgrad_fusable(int64_t T, int64_t N, int64_t K, int rot, int rot_block, int rnd);
+size_t wgrad_fused_counter_bytes(int64_t T, int64_t N, int64_t K);
+cudaError_t launch_wgrad_fused(const void *dY, const void *X, float *dW, int64_t T, int64_t N,
+                               int64_t K, int rot, int rot_block, void *Aq, void *As, void *Bq,
+                               void *Bs, void *counters, const DeviceInfo &dev,
+                               cudaStream_t stream);
+
 }  // namespace mx

@@ -36,11 +36,13 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "mx_encode.cuh"
 #include "mx_internal.h"
 #include "mx_ptx.cuh"
 
 namespace mx {
 namespace {
+using namespace enc;
 
 #ifndef MXQ_STAGES
 #define MXQ_STAGES 2
@@ -69,299 +71,6 @@ struct QuantArgs {
     int tiles_inner;   // tiles along the fast tile axis
     int num_tiles;
 };
-
-// ---------------------------------------------------------------- Philox4x64-10
-// Salmon et al., "Parallel Random Numbers: As Easy as 1, 2, 3" (SC'11).
-__device__ __forceinline__ void philox4x64_10(uint64_t c0, uint64_t k0, uint64_t k1,
-                                              uint64_t (&o)[4]) {
-    const uint64_t mul_a = 0xD2E7470EE14C6C93ull, mul_b = 0xCA5A826395121157ull;
-    const uint64_t weyl_a = 0x9E3779B97F4A7C15ull, weyl_b = 0xBB67AE8584CAA73Bull;
-    uint64_t x0 = c0, x1 = 0, x2 = 0, x3 = 0;
-#pragma unroll
-    for (int r = 0; r < 10; ++r) {
-        if (r > 0) {
-            k0 += weyl_a;
-            k1 += weyl_b;
-        }
-        const uint64_t lo_a = mul_a * x0, hi_a = __umul64hi(mul_a, x0);
-        const uint64_t lo_b = mul_b * x2, hi_b = __umul64hi(mul_b, x2);
-        const uint64_t n0 = hi_b ^ x1 ^ k0, n2 = hi_a ^ x3 ^ k1;
-        x0 = n0;
-        x1 = lo_b;
-        x2 = n2;
-        x3 = lo_a;
-    }
-    o[0] = x0;
-    o[1] = x1;
-    o[2] = x2;
-    o[3] = x3;
-}
-
-// 32 consecutive 24-bit SR draws for flat indices e0 .. e0+31 (e0 % 8 == 0).
-__device__ __forceinline__ void sr_draws32(uint64_t seed, uint64_t tag, uint64_t e0,
-                                           uint32_t (&u)[32]) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint64_t o[4];
-        philox4x64_10(e0 / 8 + q, seed, tag, o);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            u[8 * q + j] = static_cast<uint32_t>(o[j / 2] >> (32 * (j % 2))) >> 8;
-    }
-}
-
-// 32 random sign bits for positions 32*chunk .. 32*chunk+31 of the 256-block
-// `blk256` (bit i set -> d = -1).
-__device__ __forceinline__ uint32_t sign_bits32(uint64_t seed, uint64_t blk256, int chunk) {
-    uint64_t o[4];
-    philox4x64_10(blk256, seed, 0, o);
-    return static_cast<uint32_t>(o[chunk / 2] >> (32 * (chunk % 2)));
-}
-
-__device__ __forceinline__ void apply_signs(float (&x)[32], uint32_t bits) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-        x[i] = __uint_as_float(__float_as_uint(x[i]) ^ (((bits >> i) & 1u) << 31));
-}
-
-// ---------------------------------------------------------------- Hadamard
-// In-register butterfly stages of stride 1 .. min(N,32)/2 on 32 values.
-template <int N>
-__device__ __forceinline__ void fwht_in_thread(float (&x)[32]) {
-    constexpr int H = N < 32 ? N : 32;
-#pragma unroll
-    for (int h = 1; h < H; h <<= 1) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            if ((i & h) == 0) {
-                const float a = x[i], b = x[i + h];
-                x[i] = __fadd_rn(a, b);
-                x[i + h] = __fsub_rn(a, b);
-            }
-        }
-    }
-}
-
-// fp32 value nearest to 1/sqrt(N).
-template <int N>
-__device__ __forceinline__ float hadamard_norm() {
-    if (N == 16) return 0.25f;
-    if (N == 32) return __uint_as_float(0x3E3504F3u);
-    if (N == 64) return 0.125f;
-    if (N == 128) return __uint_as_float(0x3DB504F3u);
-    return 0.0625f;
-}
-
-template <int N>
-__device__ __forceinline__ void scale_by_norm(float (&x)[32]) {
-    const float c = hadamard_norm<N>();
-#pragma unroll
-    for (int i = 0; i < 32; ++i) x[i] = __fmul_rn(x[i], c);
-}
-
-// ---------------------------------------------------------------- encoding
-// E2M1 with stochastic rounding: lower grid neighbour lo, step to the next;
-// round up iff u24 < (|v| - lo) / step * 2^24 (exact in fp32).
-__device__ __forceinline__ uint32_t e2m1_sr_code(float v, uint32_t u24) {
-    const uint32_t sign = (__float_as_uint(v) >> 28) & 8u;
-    const float a = fabsf(v);
-    if (a >= 6.0f) return sign | 7u;
-    const uint32_t lo = (a >= 0.5f) + (a >= 1.0f) + (a >= 1.5f) + (a >= 2.0f) + (a >= 3.0f) +
-                        (a >= 4.0f);
-    const float lov = lo <= 4 ? 0.5f * static_cast<float>(lo) : (lo == 5 ? 3.0f : 4.0f);
-    const float inv_step_2p24 = lo < 4 ? 33554432.0f : (lo < 6 ? 16777216.0f : 8388608.0f);
-    const float thr = __fmul_rn(__fsub_rn(a, lov), inv_step_2p24);
-    const uint32_t up = static_cast<float>(u24) < thr ? 1u : 0u;
-    return sign | (lo + up);
-}
-
-// Pack e2m1(v[2j]) into the low nibble and e2m1(v[2j+1]) into the high nibble
-// of byte j; four bytes per call (round to nearest even, saturating).
-__device__ __forceinline__ uint32_t cvt_e2m1x8(float v0, float v1, float v2, float v3, float v4,
-                                               float v5, float v6, float v7) {
-    uint32_t out;
-    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
-        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
-        : "=r"(out)
-        : "f"(v0), "f"(v1), "f"(v2), "f"(v3), "f"(v4), "f"(v5), "f"(v6), "f"(v7));
-    return out;
-}
-
-// ---------------------------------------------------------------- paired lanes
-// Two channels processed in lockstep travel as one 64-bit register pair
-// {channel 2l (low), channel 2l+1 (high)}; the f32x2 instructions round each
-// half exactly like the scalar fp32 instruction would.
-__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ void unpack2(uint64_t r, float &lo, float &hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
-}
-__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-// NaN-propagating maxima of magnitudes: a NaN anywhere in a block survives
-// (max.NaN returns the canonical NaN, whose bits exceed every other magnitude).
-__device__ __forceinline__ float absmax2_nan(float a, float b) {
-    float r;
-    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(fabsf(a)), "f"(fabsf(b)));
-    return r;
-}
-__device__ __forceinline__ float absmax3_nan(float a, float b, float c) {
-    float r;
-    asm("max.NaN.abs.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-    return r;
-}
-
-// max |v_i| over 32 values as a tree of three-input maxima (17 instructions).
-__device__ __forceinline__ float block_amax32(const float (&v)[32]) {
-    float t[11];
-#pragma unroll
-    for (int j = 0; j < 10; ++j) t[j] = absmax3_nan(v[3 * j], v[3 * j + 1], v[3 * j + 2]);
-    t[10] = absmax2_nan(v[30], v[31]);
-    float u[4];
-#pragma unroll
-    for (int j = 0; j < 3; ++j) u[j] = absmax3_nan(t[3 * j], t[3 * j + 1], t[3 * j + 2]);
-    u[3] = absmax2_nan(t[9], t[10]);
-    return absmax2_nan(absmax3_nan(u[0], u[1], u[2]), u[3]);
-}
-
-// Butterfly stages of stride 1 .. min(N,32)/2 on 32 channel pairs.
-template <int N>
-__device__ __forceinline__ void fwht_pairs(uint64_t (&x)[32]) {
-    constexpr int H = N < 32 ? N : 32;
-#pragma unroll
-    for (int h = 1; h < H; h <<= 1) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            if ((i & h) == 0) {
-                const uint64_t a = x[i], b = x[i + h];
-                x[i] = add2(a, b);
-                x[i + h] = sub2(a, b);
-            }
-        }
-    }
-}
-
-// Shared-exponent byte and its exact inverse power of two for a block amax.
-__device__ __forceinline__ uint32_t scale_of(float amax, float &inv) {
-    const uint32_t m = __float_as_uint(amax);
-    const uint32_t e = m >> 23;                 // biased exponent (0: zero/subnormal)
-    const uint32_t sb = e >= 2u ? e - 2u : 0u;  // floor(log2 amax) - 2 + 127, clamped at 0
-    inv = __uint_as_float((254u - (sb > 253u ? 253u : sb)) << 23);  // 2^(127 - sb)
-    return m >= 0x7F800000u ? 0xFFu : sb;       // Inf/NaN in the block: NaN scale
-}
-
-// Round-to-nearest encode of two channels' blocks held as pairs.  x holds the
-// rotation's butterfly sums before the 1/sqrt(n) factor cn (cn = 1: none).
-// Rounding is monotone, so the block amax of fl(x*cn) is fl(amax(x)*cn), and
-// the scale comes out exactly as if every value had been normalised first.
-// The normalised value is then divided by the scale's power of two; when the
-// scale exponent keeps both fl(x*cn) and cn*2^-e away from the subnormal
-// range, fl(fl(x*cn)*2^-e) == fl(x*(cn*2^-e)) (scaling by a power of two
-// commutes with rounding in the normal range, and any value that lands below
-// it encodes to a signed zero either way), so one multiply does both.
-// Outside that range the two multiplies are done one after the other.
-template <bool NORM>
-__device__ __forceinline__ void encode_pair_rne(uint64_t (&x)[32], float cn, uint4 &q0, uint4 &q1,
-                                                uint32_t &s0, uint32_t &s1) {
-    float l[32], h[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) unpack2(x[i], l[i], h[i]);
-    float m0 = block_amax32(l), m1 = block_amax32(h);
-    if (NORM) {
-        m0 = __fmul_rn(m0, cn);
-        m1 = __fmul_rn(m1, cn);
-    }
-    float inv0, inv1;
-    s0 = scale_of(m0, inv0);
-    s1 = scale_of(m1, inv1);
-    uint64_t mult = pack2(inv0, inv1);
-    if (NORM) {
-        // Scale bytes 4 .. 249 (or a NaN scale, whose codes are discarded).
-        const bool fused = (s0 - 4u <= 245u || s0 == 0xFFu) && (s1 - 4u <= 245u || s1 == 0xFFu);
-        if (fused) {
-            mult = pack2(__fmul_rn(inv0, cn), __fmul_rn(inv1, cn));
-        } else {
-            const uint64_t cc = pack2(cn, cn);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) x[i] = mul2(x[i], cc);
-        }
-    }
-    float v0[32], v1[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) unpack2(mul2(x[i], mult), v0[i], v1[i]);
-    uint32_t w0[4], w1[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        w0[j] = cvt_e2m1x8(v0[8 * j], v0[8 * j + 1], v0[8 * j + 2], v0[8 * j + 3], v0[8 * j + 4],
-                           v0[8 * j + 5], v0[8 * j + 6], v0[8 * j + 7]);
-        w1[j] = cvt_e2m1x8(v1[8 * j], v1[8 * j + 1], v1[8 * j + 2], v1[8 * j + 3], v1[8 * j + 4],
-                           v1[8 * j + 5], v1[8 * j + 6], v1[8 * j + 7]);
-    }
-    q0 = s0 == 0xFFu ? make_uint4(0, 0, 0, 0) : make_uint4(w0[0], w0[1], w0[2], w0[3]);
-    q1 = s1 == 0xFFu ? make_uint4(0, 0, 0, 0) : make_uint4(w1[0], w1[1], w1[2], w1[3]);
-}
-
-// Encode one block of 32 rotated values.  Returns the E8M0 byte; codes in q.
-template <bool SR>
-__device__ __forceinline__ uint32_t encode_block32(const float (&r)[32], uint4 &q,
-                                                   const uint32_t *u24) {
-    uint32_t m = 0;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) m = max(m, __float_as_uint(r[i]) & 0x7FFFFFFFu);
-    if (m >= 0x7F800000u) {  // Inf or NaN in the block: NaN scale, zero codes
-        q = make_uint4(0, 0, 0, 0);
-        return 0xFFu;
-    }
-    const uint32_t e = m >> 23;               // biased exponent of amax (0: zero/subnormal)
-    const uint32_t sb = e >= 2u ? e - 2u : 0u;  // floor(log2 amax) - 2 + 127, clamped at 0
-    const float inv = __uint_as_float((254u - sb) << 23);  // 2^(127 - sb), exact
-    float v[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(r[i], inv);
-    uint32_t w[4];
-    if (SR) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint32_t word = 0;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) word |= e2m1_sr_code(v[8 * j + k], u24[8 * j + k]) << (4 * k);
-            w[j] = word;
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            w[j] = cvt_e2m1x8(v[8 * j], v[8 * j + 1], v[8 * j + 2], v[8 * j + 3], v[8 * j + 4],
-                              v[8 * j + 5], v[8 * j + 6], v[8 * j + 7]);
-    }
-    q = make_uint4(w[0], w[1], w[2], w[3]);
-    return sb;
-}
-
-__device__ __forceinline__ void st_global_16(void *p, uint4 v) {
-    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
-                 : "memory");
-}
 
 // Byte offset of scale (line, block) within a tile's 2-atom staging area:
 // staging[a][g][8] holds, for k-atom a of the tile and line group g = line%32,
@@ -421,12 +130,6 @@ __device__ __forceinline__ uint32_t encode_row_block(const uint32_t (&w)[16], ui
 }
 
 // ---------------------------------------------------------------- colwise
-// Byte offset of the scale of (line, block) in the tiled layout.
-__device__ __forceinline__ int64_t scale_offset(int64_t line, int64_t block, int64_t katoms) {
-    return ((line / 128) * katoms + block / 4) * 512 + (line % 32) * 16 + ((line % 128) / 32) * 4 +
-           (block % 4);
-}
-
 // Row direction of a dual encode: each thread encodes two (token, 32-channel)
 // blocks of a staged TT x TC column tile.  The four 16-byte reads of a block
 // start at a row-dependent chunk so that a warp's reads spread over all banks.

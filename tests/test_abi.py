@@ -52,7 +52,12 @@ def test_buffer_sizes(L):
     assert mx.codes_bytes(0, 64) == 0 and mx.scales_bytes(5, 0) == 0
     T, N, K = 8192, 4096, 14336
     ws = mx.linear_workspace_bytes(mx.OP_WGRAD, T, N, K)
-    assert ws == (N * T // 2 + N * T // 32) + (K * T // 2 + K * T // 32)
+    # both encoded operands, plus one 4-byte counter per (256-line panel,
+    # 512-token chunk) for the fused Wgrad launch
+    counters = 4 * (N // 256 + K // 256) * (T // 512)
+    assert ws == (N * T // 2 + N * T // 32) + (K * T // 2 + K * T // 32) + (counters + 255) // 256 * 256
+    assert mx.linear_workspace_bytes(mx.OP_FPROP, T, N, K) == \
+        (T * K // 2 + T * K // 32) + (N * K // 2 + N * K // 32)
     assert mx.linear_workspace_bytes(7, T, N, K) == 0
 
 

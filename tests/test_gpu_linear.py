@@ -228,3 +228,52 @@ def test_qkv_gateup_all_three_gemms():
         check_op_rows_cols(mx.OP_FPROP, X, W, mx.ROT_NONE, 32)
         check_op_rows_cols(mx.OP_DGRAD, dY, W, mx.ROT_NONE, 32)
         check_op_rows_cols(mx.OP_WGRAD, dY, X, mx.ROT_HADAMARD_DET, 32)
+
+
+@pytest.mark.parametrize("T,N,K,rot,nb", [(1024, 512, 768, mx.ROT_HADAMARD_DET, 32),
+                                          (2048, 256, 1280, mx.ROT_HADAMARD_DET, 16),
+                                          (512, 768, 256, mx.ROT_NONE, 32),
+                                          (4096, 2560, 2304, mx.ROT_HADAMARD_DET, 32)])
+def test_wgrad_fused_launch_equals_separate_launches(T, N, K, rot, nb):
+    """mx_linear_wgrad_fused runs these shapes as one launch whose encoder
+    warps feed the GEMM; the result has the bits of mx_linear_wgrad's separate
+    encode + GEMM launches (the same encode and the same accumulation order)
+    and matches the oracle on sampled entries.  The last shape has more tiles
+    than pairs."""
+    assert mx.lib().mx_linear_wgrad_fused_supported(T, N, K, rot, nb, mx.ROUND_RNE) == 1
+    dY_bits = _bits((T, N), 51, 1e-3)
+    X_bits = _bits((T, K), 52)
+    dY, X = _dev(dY_bits), _dev(X_bits)
+    fused = mx.linear_wgrad_fused(dY, X, rot=rot, rot_block=nb, rnd=mx.ROUND_RNE, seed=0)
+    mx.check_status()
+    (aq, as_), (bq, bs) = mx.quantize_pair(dY, X, rot, nb, mx.ROUND_RNE, 0)
+    sep = mx.gemm(aq, as_, bq, bs, N, K, T)
+    mx.check_status()
+    assert torch.equal(fused.view(torch.int32), sep.view(torch.int32))
+    again = mx.linear_wgrad_fused(dY, X, rot=rot, rot_block=nb, rnd=mx.ROUND_RNE, seed=0)
+    mx.check_status()
+    assert torch.equal(fused.view(torch.int32), again.view(torch.int32))
+    ref, ref_abs = _oracle_entries(dY_bits, X_bits, rot, nb)
+    got = fused.cpu().numpy()
+    ii, jj = ref[2], ref[3]
+    assert np.all(np.abs(got[ii, jj].astype(np.float64) - ref[0]) <= 1e-5 * ref_abs)
+
+
+def _oracle_entries(dY_bits, X_bits, rot, nb, n=2048):
+    Aq, As = oracle.quantize(dY_bits, oracle.CONTRACT_ROWS, rot, nb, mx.ROUND_RNE, 0, 1)
+    Bq, Bs = oracle.quantize(X_bits, oracle.CONTRACT_ROWS, rot, nb, mx.ROUND_RNE, 0, 2)
+    rng = np.random.default_rng(9)
+    ii, jj = rng.integers(0, Aq.shape[0], n), rng.integers(0, Bq.shape[0], n)
+    C, Ca = oracle.gemm_entries(Aq, As, Bq, Bs, ii, jj)
+    return (C, Ca, ii, jj), Ca
+
+
+def test_wgrad_fused_rejects_modes_it_does_not_cover():
+    dY = torch.zeros((1024, 256), dtype=torch.int16, device="cuda")
+    X = torch.zeros((1024, 256), dtype=torch.int16, device="cuda")
+    for rot, nb, rnd in [(mx.ROT_HADAMARD_RAND, 32, mx.ROUND_RNE), (mx.ROT_HADAMARD_DET, 64, mx.ROUND_RNE),
+                         (mx.ROT_HADAMARD_DET, 32, mx.ROUND_SR)]:
+        assert mx.lib().mx_linear_wgrad_fused_supported(1024, 256, 256, rot, nb, rnd) == 0
+        with pytest.raises(mx.MXError):
+            mx.linear_wgrad_fused(dY, X, rot=rot, rot_block=nb, rnd=rnd)
+    assert mx.lib().mx_linear_wgrad_fused_supported(1000, 256, 256, 1, 32, 0) == 0   # T % 512
