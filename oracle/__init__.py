@@ -23,6 +23,7 @@ _HDR = os.path.join(_HERE, "mx_oracle.h")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _SO = os.path.join(_BUILD_DIR, "liboracle.so")
 
+FMT_MXFP4, FMT_MXFP8 = 0, 1
 ROT_NONE, ROT_HADAMARD_DET, ROT_HADAMARD_RAND = 0, 1, 2
 ROUND_RNE, ROUND_SR = 0, 1
 CONTRACT_ROWS, CONTRACT_COLS = 0, 1
@@ -79,6 +80,20 @@ def lib() -> ctypes.CDLL:
             L.oracle_dequantize.argtypes = [P, P, i64, i64, P]
             L.oracle_gemm_entries.argtypes = [P, P, P, P, i64, P, P, i64, P, P]
             L.oracle_gemm_rows.argtypes = [P, P, P, P, i64, i64, i64, i64, i64, P, P]
+            L.oracle_scale_byte_e4m3.argtypes = [ctypes.c_float]
+            L.oracle_scale_byte_e4m3.restype = ctypes.c_uint8
+            L.oracle_e4m3_rne.argtypes = [ctypes.c_float]
+            L.oracle_e4m3_rne.restype = ctypes.c_uint8
+            L.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+            L.oracle_e4m3_value.restype = ctypes.c_double
+            L.oracle_scale_bytes_e4m3.argtypes = [P, i64, P]
+            L.oracle_e4m3_rne_vec.argtypes = [P, i64, P]
+            L.oracle_quantize_mxfp8.argtypes = [P, i64, i64, i32, i32, i32, u64, P, i64, i32,
+                                                P, P]
+            L.oracle_quantize_mxfp8.restype = i32
+            L.oracle_dequantize_fmt.argtypes = [i32, P, P, i64, i64, P]
+            L.oracle_gemm_entries_fmt.argtypes = [i32, P, P, P, P, i64, P, P, i64, P, P]
+            L.oracle_gemm_rows_fmt.argtypes = [i32, P, P, P, P, i64, i64, i64, i64, i64, P, P]
             _lib = L
     return _lib
 
@@ -149,6 +164,26 @@ def e2m1_value(code: int) -> float:
     return float(lib().oracle_e2m1_value(code))
 
 
+def scale_bytes_e4m3(amax) -> np.ndarray:
+    shape = np.shape(amax)
+    a = np.ascontiguousarray(np.asarray(amax, dtype=np.float32).reshape(-1))
+    out = np.zeros(a.shape, dtype=np.uint8)
+    lib().oracle_scale_bytes_e4m3(_ptr(a), int(a.size), _ptr(out))
+    return out.reshape(shape)
+
+
+def e4m3_rne(v) -> np.ndarray:
+    shape = np.shape(v)
+    a = np.ascontiguousarray(np.asarray(v, dtype=np.float32).reshape(-1))
+    out = np.zeros(a.shape, dtype=np.uint8)
+    lib().oracle_e4m3_rne_vec(_ptr(a), int(a.size), _ptr(out))
+    return out.reshape(shape)
+
+
+def e4m3_value(code: int) -> float:
+    return float(lib().oracle_e4m3_value(code))
+
+
 # --------------------------------------------------------------------------
 # operand encoding / decoding / contraction
 # --------------------------------------------------------------------------
@@ -190,39 +225,69 @@ def quantize(src_bf16: np.ndarray, contract: int, rot: int = ROT_NONE, rot_block
     return codes, scales
 
 
-def dequantize(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+def quantize_mxfp8(src_bf16: np.ndarray, contract: int, rot: int = ROT_NONE,
+                   rot_block: int = 32, seed: int = 0, lines=None, precise: bool = False):
+    """MXFP8-encode bf16 bits src[rows, cols]; returns (codes, canonical scales).
+
+    contract=CONTRACT_ROWS -> codes [cols, rows], scales [cols, rows/32]
+    contract=CONTRACT_COLS -> codes [rows, cols], scales [rows, cols/32]
+    """
+    src = np.ascontiguousarray(src_bf16, dtype=np.uint16)
+    rows, cols = src.shape
+    L = rows if contract == CONTRACT_ROWS else cols
+    nl = cols if contract == CONTRACT_ROWS else rows
+    if lines is not None:
+        ln = np.ascontiguousarray(np.asarray(lines, dtype=np.int64))
+        count, lp = ln.size, _ptr(ln)
+    else:
+        ln, count, lp = None, nl, None
+    codes = np.zeros((count, L), dtype=np.uint8)
+    scales = np.zeros((count, L // 32), dtype=np.uint8)
+    rc = lib().oracle_quantize_mxfp8(_ptr(src), rows, cols, contract, rot, rot_block, seed, lp,
+                                     count if ln is not None else 0, int(precise), _ptr(codes),
+                                     _ptr(scales))
+    if rc != 0:
+        raise ValueError("oracle_quantize_mxfp8 rejected its arguments")
+    return codes, scales
+
+
+def _k_of(codes: np.ndarray, fmt: int) -> int:
+    return codes.shape[1] * (1 if fmt == FMT_MXFP8 else 2)
+
+
+def dequantize(codes: np.ndarray, scales: np.ndarray, fmt: int = FMT_MXFP4) -> np.ndarray:
     c = np.ascontiguousarray(codes, dtype=np.uint8)
     s = np.ascontiguousarray(scales, dtype=np.uint8)
-    mn, k = c.shape[0], c.shape[1] * 2
+    mn, k = c.shape[0], _k_of(c, fmt)
     out = np.zeros((mn, k), dtype=np.float64)
-    lib().oracle_dequantize(_ptr(c), _ptr(s), mn, k, _ptr(out))
+    lib().oracle_dequantize_fmt(fmt, _ptr(c), _ptr(s), mn, k, _ptr(out))
     return out
 
 
-def gemm_entries(Aq, As, Bq, Bs, ii, jj):
+def gemm_entries(Aq, As, Bq, Bs, ii, jj, fmt: int = FMT_MXFP4):
     """C[i, j] and sum |a||b| for listed pairs (i, j); A, B contraction-major."""
     Aq, As, Bq, Bs = (np.ascontiguousarray(a, dtype=np.uint8) for a in (Aq, As, Bq, Bs))
-    K = Aq.shape[1] * 2
+    K = _k_of(Aq, fmt)
     ii = np.ascontiguousarray(np.asarray(ii, dtype=np.int64))
     jj = np.ascontiguousarray(np.asarray(jj, dtype=np.int64))
     C = np.zeros(ii.size, dtype=np.float64)
     Ca = np.zeros(ii.size, dtype=np.float64)
-    lib().oracle_gemm_entries(_ptr(Aq), _ptr(As), _ptr(Bq), _ptr(Bs), K, _ptr(ii), _ptr(jj),
-                              int(ii.size), _ptr(C), _ptr(Ca))
+    lib().oracle_gemm_entries_fmt(fmt, _ptr(Aq), _ptr(As), _ptr(Bq), _ptr(Bs), K, _ptr(ii),
+                                  _ptr(jj), int(ii.size), _ptr(C), _ptr(Ca))
     return C, Ca
 
 
-def gemm_rows(Aq, As, Bq, Bs, m0: int = 0, m1: int | None = None):
+def gemm_rows(Aq, As, Bq, Bs, m0: int = 0, m1: int | None = None, fmt: int = FMT_MXFP4):
     """Rows [m0, m1) of C = A B^T (double) and of sum |a||b|."""
     Aq, As, Bq, Bs = (np.ascontiguousarray(a, dtype=np.uint8) for a in (Aq, As, Bq, Bs))
-    M, N, K = Aq.shape[0], Bq.shape[0], Aq.shape[1] * 2
+    M, N, K = Aq.shape[0], Bq.shape[0], _k_of(Aq, fmt)
     m1 = M if m1 is None else m1
     C = np.zeros((m1 - m0, N), dtype=np.float64)
     Ca = np.zeros((m1 - m0, N), dtype=np.float64)
-    lib().oracle_gemm_rows(_ptr(Aq), _ptr(As), _ptr(Bq), _ptr(Bs), M, N, K, m0, m1, _ptr(C),
-                           _ptr(Ca))
+    lib().oracle_gemm_rows_fmt(fmt, _ptr(Aq), _ptr(As), _ptr(Bq), _ptr(Bs), M, N, K, m0, m1,
+                               _ptr(C), _ptr(Ca))
     return C, Ca
 
 
-def gemm(Aq, As, Bq, Bs):
-    return gemm_rows(Aq, As, Bq, Bs, 0, None)
+def gemm(Aq, As, Bq, Bs, fmt: int = FMT_MXFP4):
+    return gemm_rows(Aq, As, Bq, Bs, 0, None, fmt)

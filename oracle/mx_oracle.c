@@ -148,7 +148,9 @@ void oracle_hadamard_f64(const double *x, int n, double *y)
 /* ------------------------------------------------------------------------ */
 /* Shared scale and element rounding.                                        */
 /* ------------------------------------------------------------------------ */
-uint8_t oracle_scale_byte(float amax)
+/* E8M0 block exponent: floor(log2 amax) minus the element format's largest
+ * exponent (emax), clamped to the byte's range; 0xFF marks a non-finite block. */
+static uint8_t scale_byte_emax(float amax, int emax)
 {
     if (isnan(amax) || isinf(amax))
         return 0xFF;
@@ -156,12 +158,22 @@ uint8_t oracle_scale_byte(float amax)
         return 0x00;
     int e;
     (void)frexp((double)amax, &e);    /* amax = m * 2^e, m in [0.5, 1) */
-    int s = (e - 1) - 2;              /* floor(log2 amax) - emax(E2M1) */
+    int s = (e - 1) - emax;           /* floor(log2 amax) - emax */
     if (s < -127)
         s = -127;
     if (s > 127)
         s = 127;
     return (uint8_t)(s + 127);
+}
+
+uint8_t oracle_scale_byte(float amax)
+{
+    return scale_byte_emax(amax, 2);  /* E2M1: largest value 6 = 1.5 * 2^2 */
+}
+
+uint8_t oracle_scale_byte_e4m3(float amax)
+{
+    return scale_byte_emax(amax, 8);  /* E4M3: largest value 448 = 1.75 * 2^8 */
 }
 
 /* The eight non-negative E2M1 magnitudes, listed by code 0..7
@@ -206,6 +218,50 @@ double oracle_e2m1_value(uint8_t code)
 {
     double m = E2M1_MAG[code & 7u];
     return (code & 8u) ? -m : m;
+}
+
+/* E4M3 (OCP 8-bit float, the "FP8 (E4M3)" of [show] section 2.2): sign in
+ * bit 7, exponent field bits 6..3 with bias 7, mantissa bits 2..0.  Exponent
+ * field 0 is subnormal (m/8 * 2^-6); S.1111.111 is NaN; there is no infinity,
+ * so the largest finite magnitude is 1.75 * 2^8 = 448. */
+double oracle_e4m3_value(uint8_t code)
+{
+    int e = (code >> 3) & 0xF, m = code & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    double mag = (e == 0) ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return (code & 0x80u) ? -mag : mag;
+}
+
+uint8_t oracle_e4m3_rne(float v)
+{
+    double a = fabs((double)v);
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    if (a >= 448.0)                    /* saturate: beyond the grid, 448 is nearest */
+        return (uint8_t)(sign | 0x7E);
+    int best = 0;
+    double best_d = a;
+    for (int c = 1; c <= 0x7E; ++c) {  /* every non-negative finite code */
+        double d = fabs(a - oracle_e4m3_value((uint8_t)c));
+        /* strictly nearer wins; on an exact tie the even code wins */
+        if (d < best_d || (d == best_d && (c % 2) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+void oracle_scale_bytes_e4m3(const float *amax, int64_t n, uint8_t *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_scale_byte_e4m3(amax[i]);
+}
+
+void oracle_e4m3_rne_vec(const float *v, int64_t n, uint8_t *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_e4m3_rne(v[i]);
 }
 
 void oracle_scale_bytes(const float *amax, int64_t n, uint8_t *out)
@@ -318,10 +374,61 @@ static void encode_line(const float *r, int64_t L, int rnd, uint64_t seed, uint6
     }
 }
 
+/* MXFP8 line: the same blocks of 32 and E8M0 exponent rule as MXFP4 with
+ * E4M3's emax (8), each element rounded to nearest-even E4M3 (saturating),
+ * one byte per element. */
+static void encode_line_e4m3(const float *r, int64_t L, uint8_t *codes, uint8_t *scales)
+{
+    for (int64_t b = 0; b < L / 32; ++b) {
+        const float *blk = r + b * 32;
+        float amax = 0.0f;
+        int nonfinite = 0;
+        for (int i = 0; i < 32; ++i) {
+            float a = fabsf(blk[i]);
+            if (!isfinite(a))
+                nonfinite = 1;
+            else if (a > amax)
+                amax = a;
+        }
+        uint8_t sb = nonfinite ? (uint8_t)0xFF : oracle_scale_byte_e4m3(amax);
+        scales[b] = sb;
+        if (sb == 0xFF) {
+            memset(codes + b * 32, 0, 32);
+            continue;
+        }
+        int s = (int)sb - 127;
+        float inv = ldexpf(1.0f, -s);              /* exact power of two, normal */
+        for (int i = 0; i < 32; ++i)
+            codes[b * 32 + i] = oracle_e4m3_rne(blk[i] * inv);
+    }
+}
+
+static int quantize_impl(int fmt, const uint16_t *src, int64_t rows, int64_t cols,
+                         int contract, int rot, int rot_block, int rnd, uint64_t seed,
+                         uint64_t sr_tag, const int64_t *lines, int64_t nlines, int precise,
+                         uint8_t *codes, uint8_t *scales);
+
 int oracle_quantize(const uint16_t *src, int64_t rows, int64_t cols, int contract,
                     int rot, int rot_block, int rnd, uint64_t seed, uint64_t sr_tag,
                     const int64_t *lines, int64_t nlines, int precise,
                     uint8_t *codes, uint8_t *scales)
+{
+    return quantize_impl(ORACLE_FMT_MXFP4, src, rows, cols, contract, rot, rot_block, rnd,
+                         seed, sr_tag, lines, nlines, precise, codes, scales);
+}
+
+int oracle_quantize_mxfp8(const uint16_t *src, int64_t rows, int64_t cols, int contract,
+                          int rot, int rot_block, uint64_t seed, const int64_t *lines,
+                          int64_t nlines, int precise, uint8_t *codes, uint8_t *scales)
+{
+    return quantize_impl(ORACLE_FMT_MXFP8, src, rows, cols, contract, rot, rot_block,
+                         ORACLE_ROUND_RNE, seed, 0, lines, nlines, precise, codes, scales);
+}
+
+static int quantize_impl(int fmt, const uint16_t *src, int64_t rows, int64_t cols,
+                         int contract, int rot, int rot_block, int rnd, uint64_t seed,
+                         uint64_t sr_tag, const int64_t *lines, int64_t nlines, int precise,
+                         uint8_t *codes, uint8_t *scales)
 {
     if (!src || !codes || !scales || rows <= 0 || cols <= 0)
         return -1;
@@ -358,8 +465,11 @@ int oracle_quantize(const uint16_t *src, int64_t rows, int64_t cols, int contrac
             free(r);
             return -1;
         }
-        encode_line(r, L, rnd, seed, sr_tag, (uint64_t)line, codes + k * (L / 2),
-                    scales + k * (L / 32));
+        if (fmt == ORACLE_FMT_MXFP8)
+            encode_line_e4m3(r, L, codes + k * L, scales + k * (L / 32));
+        else
+            encode_line(r, L, rnd, seed, sr_tag, (uint64_t)line, codes + k * (L / 2),
+                        scales + k * (L / 32));
     }
     free(r);
     return 0;
@@ -370,34 +480,52 @@ int oracle_quantize(const uint16_t *src, int64_t rows, int64_t cols, int contrac
 /* Y = X W^T, Dgrad dX = dY W, Wgrad dW = dY^T X; all three are C = A B^T     */
 /* over operands encoded along the contraction dimension).                   */
 /* ------------------------------------------------------------------------ */
-static double decode(const uint8_t *codes, const uint8_t *scales, int64_t row, int64_t k,
-                     int64_t t)
+/* Bytes of codes per encoded line of k elements. */
+static int64_t code_row_bytes(int fmt, int64_t k)
 {
-    uint8_t byte = codes[row * (k / 2) + t / 2];
-    uint8_t code = (t % 2 == 0) ? (uint8_t)(byte & 0xFu) : (uint8_t)(byte >> 4);
+    return fmt == ORACLE_FMT_MXFP8 ? k : k / 2;
+}
+
+static double decode(int fmt, const uint8_t *codes, const uint8_t *scales, int64_t row,
+                     int64_t k, int64_t t)
+{
     uint8_t sb = scales[row * (k / 32) + t / 32];
     if (sb == 0xFF)
         return NAN;
-    return ldexp(oracle_e2m1_value(code), (int)sb - 127);
+    double v;
+    if (fmt == ORACLE_FMT_MXFP8) {
+        v = oracle_e4m3_value(codes[row * k + t]);
+    } else {
+        uint8_t byte = codes[row * (k / 2) + t / 2];
+        uint8_t code = (t % 2 == 0) ? (uint8_t)(byte & 0xFu) : (uint8_t)(byte >> 4);
+        v = oracle_e2m1_value(code);
+    }
+    return ldexp(v, (int)sb - 127);
+}
+
+void oracle_dequantize_fmt(int fmt, const uint8_t *codes, const uint8_t *scales, int64_t mn,
+                           int64_t k, double *out)
+{
+    for (int64_t i = 0; i < mn; ++i)
+        for (int64_t t = 0; t < k; ++t)
+            out[i * k + t] = decode(fmt, codes, scales, i, k, t);
 }
 
 void oracle_dequantize(const uint8_t *codes, const uint8_t *scales, int64_t mn, int64_t k,
                        double *out)
 {
-    for (int64_t i = 0; i < mn; ++i)
-        for (int64_t t = 0; t < k; ++t)
-            out[i * k + t] = decode(codes, scales, i, k, t);
+    oracle_dequantize_fmt(ORACLE_FMT_MXFP4, codes, scales, mn, k, out);
 }
 
-void oracle_gemm_entries(const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq,
-                         const uint8_t *Bs, int64_t K, const int64_t *ii, const int64_t *jj,
-                         int64_t n, double *C, double *Cabs)
+void oracle_gemm_entries_fmt(int fmt, const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq,
+                             const uint8_t *Bs, int64_t K, const int64_t *ii, const int64_t *jj,
+                             int64_t n, double *C, double *Cabs)
 {
     for (int64_t p = 0; p < n; ++p) {
         double acc = 0.0, acc_abs = 0.0;
         for (int64_t t = 0; t < K; ++t) {
-            double a = decode(Aq, As, ii[p], K, t);
-            double b = decode(Bq, Bs, jj[p], K, t);
+            double a = decode(fmt, Aq, As, ii[p], K, t);
+            double b = decode(fmt, Bq, Bs, jj[p], K, t);
             acc += a * b;
             acc_abs += fabs(a) * fabs(b);
         }
@@ -406,16 +534,23 @@ void oracle_gemm_entries(const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq
     }
 }
 
-void oracle_gemm_rows(const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq,
-                      const uint8_t *Bs, int64_t M, int64_t N, int64_t K, int64_t m0,
-                      int64_t m1, double *C, double *Cabs)
+void oracle_gemm_entries(const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq,
+                         const uint8_t *Bs, int64_t K, const int64_t *ii, const int64_t *jj,
+                         int64_t n, double *C, double *Cabs)
+{
+    oracle_gemm_entries_fmt(ORACLE_FMT_MXFP4, Aq, As, Bq, Bs, K, ii, jj, n, C, Cabs);
+}
+
+void oracle_gemm_rows_fmt(int fmt, const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq,
+                          const uint8_t *Bs, int64_t M, int64_t N, int64_t K, int64_t m0,
+                          int64_t m1, double *C, double *Cabs)
 {
     (void)M;
     double *a = (double *)malloc(sizeof(double) * (size_t)K);
     double *b = (double *)malloc(sizeof(double) * (size_t)N * (size_t)K);
-    oracle_dequantize(Bq, Bs, N, K, b);
+    oracle_dequantize_fmt(fmt, Bq, Bs, N, K, b);
     for (int64_t i = m0; i < m1; ++i) {
-        oracle_dequantize(Aq + i * (K / 2), As + i * (K / 32), 1, K, a);
+        oracle_dequantize_fmt(fmt, Aq + i * code_row_bytes(fmt, K), As + i * (K / 32), 1, K, a);
         for (int64_t j = 0; j < N; ++j) {
             const double *bj = b + j * K;
             double acc = 0.0, acc_abs = 0.0;
@@ -429,4 +564,11 @@ void oracle_gemm_rows(const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq,
     }
     free(a);
     free(b);
+}
+
+void oracle_gemm_rows(const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq,
+                      const uint8_t *Bs, int64_t M, int64_t N, int64_t K, int64_t m0,
+                      int64_t m1, double *C, double *Cabs)
+{
+    oracle_gemm_rows_fmt(ORACLE_FMT_MXFP4, Aq, As, Bq, Bs, M, N, K, m0, m1, C, Cabs);
 }

@@ -16,7 +16,9 @@
  *   [show]  "AMD颠覆认知：FP4不稳定性的真正原因" (showapi.com), section 2.2
  *           (FP4 = 1 sign, 2 exponent, 1 mantissa bit).
  *   OCP Microscaling (MX) standard, named in [36kr] "Fazit": E8M0 scale
- *           (bias 127), E2M1 element (bias 1, max 6, no Inf/NaN).
+ *           (bias 127), E2M1 element (bias 1, max 6, no Inf/NaN); its 8-bit
+ *           member MXFP8 (E4M3 element, bias 7, max 448) is the block-scaled
+ *           form of the FP8 baseline of [36kr] "Ende-zu-Ende-Effizienz".
  *   Philox4x64-10: Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As
  *           Easy as 1, 2, 3", SC'11.
  *
@@ -72,6 +74,7 @@ void oracle_e2m1_rne_vec(const float *v, int64_t n, uint8_t *out);
 void oracle_e2m1_sr_vec(const float *v, const uint32_t *u24, int64_t n, uint8_t *out);
 
 /* Rotation mode / rounding mode / contraction direction. */
+enum { ORACLE_FMT_MXFP4 = 0, ORACLE_FMT_MXFP8 = 1 };
 enum { ORACLE_ROT_NONE = 0, ORACLE_ROT_HADAMARD_DET = 1, ORACLE_ROT_HADAMARD_RAND = 2 };
 enum { ORACLE_ROUND_RNE = 0, ORACLE_ROUND_SR = 1 };
 enum { ORACLE_CONTRACT_ROWS = 0, ORACLE_CONTRACT_COLS = 1 };
@@ -81,6 +84,19 @@ enum { ORACLE_CONTRACT_ROWS = 0, ORACLE_CONTRACT_COLS = 1 };
  * precise == 1: dense double product rounded once to fp32 (diagnostic). */
 int oracle_rotate_line(const uint16_t *line_bf16, int64_t stride, int64_t L, int64_t t0,
                        int rot, int rot_block, uint64_t seed, int precise, float *out);
+
+/* E8M0 byte for a block whose largest magnitude is amax, MXFP8 rule:
+ * floor(log2 amax) - 8 (E4M3's largest exponent), clamped to [-127, 127],
+ * biased by 127; 0 for amax == 0; 0xFF for a non-finite amax. */
+uint8_t oracle_scale_byte_e4m3(float amax);
+
+/* Nearest E4M3 code to v (ties to the even code, |v| >= 448 saturates to
+ * 448, the sign of v kept, zero included).  Value of an E4M3 code (NaN for
+ * S.1111.111). */
+uint8_t oracle_e4m3_rne(float v);
+double oracle_e4m3_value(uint8_t code);
+void oracle_scale_bytes_e4m3(const float *amax, int64_t n, uint8_t *out);
+void oracle_e4m3_rne_vec(const float *v, int64_t n, uint8_t *out);
 
 /* MXFP4-encode a bf16 matrix src[rows][cols] (row-major).
  *  contract == ROWS: blocks of 32 run down each column; line c = column c,
@@ -97,6 +113,26 @@ int oracle_quantize(const uint16_t *src, int64_t rows, int64_t cols, int contrac
                     int rot, int rot_block, int rnd, uint64_t seed, uint64_t sr_tag,
                     const int64_t *lines, int64_t nlines, int precise,
                     uint8_t *codes, uint8_t *scales);
+
+/* MXFP8-encode a bf16 matrix: the line selection, rotation and canonical
+ * scale layout of oracle_quantize, E4M3 elements rounded to nearest-even,
+ * one code byte per element: codes[line][L].  Returns 0, or -1 on bad
+ * arguments. */
+int oracle_quantize_mxfp8(const uint16_t *src, int64_t rows, int64_t cols, int contract,
+                          int rot, int rot_block, uint64_t seed, const int64_t *lines,
+                          int64_t nlines, int precise, uint8_t *codes, uint8_t *scales);
+
+/* Decode, the contraction over listed entries and over a row range, for
+ * either format (fmt = ORACLE_FMT_*): codes are [mn][k/2] for MXFP4 and
+ * [mn][k] for MXFP8; canonical scales [mn][k/32]. */
+void oracle_dequantize_fmt(int fmt, const uint8_t *codes, const uint8_t *scales, int64_t mn,
+                           int64_t k, double *out);
+void oracle_gemm_entries_fmt(int fmt, const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq,
+                             const uint8_t *Bs, int64_t K, const int64_t *ii, const int64_t *jj,
+                             int64_t n, double *C, double *Cabs);
+void oracle_gemm_rows_fmt(int fmt, const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq,
+                          const uint8_t *Bs, int64_t M, int64_t N, int64_t K, int64_t m0,
+                          int64_t m1, double *C, double *Cabs);
 
 /* Decode codes[mn][k/2] + canonical scales[mn][k/32] into double out[mn][k]. */
 void oracle_dequantize(const uint8_t *codes, const uint8_t *scales, int64_t mn, int64_t k,
