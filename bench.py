@@ -454,10 +454,15 @@ def run_mine(args, world, rank, local):
     if rank == 0 and not args.no_extras:
         fused_side = measure_fused(L, mx, dY, X, dW, T, N, K, flush, stream, dev, step_ms,
                                    fp4_meas)
+    fp8_side = None
+    if rank == 0 and not args.no_extras:
+        fp8_meas = measure_fp8_peak(mx)
+        fp8_side = measure_mxfp8(L, mx, dY, X, T, N, K, flush, stream, dev, fp8_meas,
+                                 sorted(step_ms)[len(step_ms) // 2])
     side = None
     if rank == 0 and not args.no_extras and args.workload != "o_proj":
         side = measure_side_workload(L, mx, "o_proj", dev, stream, flush, min(n, 300),
-                                     args.warmup, fp4_meas)
+                                     args.warmup, fp4_meas, fp8_meas)
 
     # parity spot check of the timed output (oracle entries, rank 0 only)
     parity = None
@@ -524,6 +529,7 @@ def run_mine(args, world, rank, local):
             "roofline_kernels": kernels,
             "step_launches": 2,
             "fused_wgrad": fused_side,
+            "fp8_comparator": fp8_side,
             "fp4_peak_fraction": value / fp4_peak,
             "fp4_peak_measured": fp4_meas,
             "fp4_measured_fraction": value / fp4_meas["tflops"],
@@ -568,7 +574,8 @@ def measure_fp4_peak(mx, reps=3):
             "call": "mx_bench_mma", "best_of": reps}
 
 
-def measure_side_workload(L, mx, name, dev, stream, flush, steps, warmup, fp4_meas):
+def measure_side_workload(L, mx, name, dev, stream, flush, steps, warmup, fp4_meas,
+                          fp8_meas=None):
     """Quantise-pair + GEMM of another Wgrad shape, timed like the headline
     (L2 flushed before every step, CUDA events on the launching stream)."""
     import numpy as np
@@ -630,8 +637,12 @@ def measure_side_workload(L, mx, name, dev, stream, flush, steps, warmup, fp4_me
     flops = 2.0 * N * K * T
     hbm = load_peaks()[0]["hbm_gbs"]
     qbytes = (N + K) * T * (2 + 0.5 + 1 / 32)
+    fp8 = None
+    if fp8_meas is not None:
+        fp8 = measure_mxfp8(L, mx, dY, X, T, N, K, flush, stream, dev, fp8_meas, t_step)
     return {"workload": f"{name} Wgrad: dY [{T},{N}] x X [{T},{K}] -> dW [{N},{K}] fp32, "
                         f"{mode_text()}",
+            "fp8_comparator": fp8,
             "steps": steps, "ms_per_step": t_step,
             "value": flops / (t_step * 1e-3) / 1e12, "unit": "TFLOP/s",
             "step_launches": 2,
@@ -680,6 +691,73 @@ def measure_fused(L, mx, dY, X, dW, T, N, K, flush, stream, dev, step_ms, fp4_me
             "tflops": 2.0 * N * K * T / (t * 1e-3) / 1e12,
             "two_launch_step_ms_median": two,
             "bitwise_equal_to_two_launch_step": same}
+
+
+def measure_fp8_peak(mx, reps=3):
+    """All-SM issue rate of the MXFP8 comparator GEMM's instruction,
+    tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X (M=256,
+    N=256, K=32), operands in shared memory; best of `reps`."""
+    best = None
+    for _ in range(reps):
+        r = mx.bench_mma(kind=5, cta_group=2, n=256, mmas_per_iter=4, iters=20000)
+        if best is None or r["tflops"] > best["tflops"]:
+            best = r
+    return {"tflops": best["tflops"], "ns_per_mma": best["ns_per_mma"],
+            "instruction": "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X "
+                           "M=256 N=256 K=32", "call": "mx_bench_mma", "best_of": reps}
+
+
+def measure_mxfp8(L, mx, dY, X, T, N, K, flush, stream, dev, fp8_meas, mxfp4_step_ms,
+                  reps=50):
+    """The FP8 comparator on the same Wgrad shape: mx_linear_wgrad_mxfp8
+    (MXFP8 encode of both operands + the MXFP8 GEMM, no rotation), and its
+    GEMM launch alone; medians over `reps` calls, L2 flushed before each."""
+    import torch
+    sp = stream.cuda_stream
+    ptr = lambda t: t.data_ptr()
+    ws = torch.empty(mx.linear_wgrad_mxfp8_workspace_bytes(T, N, K), dtype=torch.uint8,
+                     device=dev)
+    out = torch.empty((N, K), dtype=torch.float32, device=dev)
+    n_code = mx.mxfp8_codes_bytes(N, T)
+    align = lambda x: (x + 255) // 256 * 256
+    aq = ws[0:]
+    as_ = ws[align(n_code):]
+    bq = ws[align(n_code) + align(mx.scales_bytes(N, T)):]
+    bs = ws[align(n_code) + align(mx.scales_bytes(N, T)) + align(mx.mxfp8_codes_bytes(K, T)):]
+
+    def step():
+        return L.mx_linear_wgrad_mxfp8(ptr(dY), ptr(X), ptr(out), T, N, K, ptr(ws), ws.numel(), sp)
+
+    def gemm():
+        return L.mx_gemm_mxfp8(ptr(aq), ptr(as_), ptr(bq), ptr(bs), ptr(out), N, K, T, sp)
+
+    def timed(fn):
+        for _ in range(3):
+            flush.zero_()
+            if fn():
+                raise RuntimeError("MXFP8 comparator launch failed")
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ts.append(e0.elapsed_time(e1))
+        return sorted(ts)[len(ts) // 2]
+
+    t_step = timed(step)
+    t_gemm = timed(gemm)             # on the operands the last step left in the workspace
+    mx.check_status()
+    flops = 2.0 * N * K * T
+    return {"call": "mx_linear_wgrad_mxfp8", "format": "MXFP8: E4M3 elements, E8M0 scale per "
+            "32 along T, no rotation, round to nearest even",
+            "ms_per_step": t_step, "tflops": flops / (t_step * 1e-3) / 1e12,
+            "gemm_ms": t_gemm, "gemm_tflops": flops / (t_gemm * 1e-3) / 1e12,
+            "fp8_peak_measured": fp8_meas,
+            "gemm_frac_fp8_measured": flops / (t_gemm * 1e-3) / 1e12 / fp8_meas["tflops"],
+            "mxfp4_step_speedup": t_step / mxfp4_step_ms, "median_of": reps, "step_launches": 2}
 
 
 def measure_dual(L, mx, dY, T, N, flush, stream, dev, hbm_gbs, reps=30):

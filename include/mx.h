@@ -222,6 +222,43 @@ mx_status mx_linear_wgrad_fused(const void *d_dY, const void *d_X, float *d_dW, 
 int mx_linear_wgrad_fused_supported(int64_t T, int64_t N, int64_t K, int rot, int rot_block,
                                     int rnd);
 
+/*
+ * MXFP8 comparator -- the FP8 baseline the pages compare MXFP4 against
+ * ("Neue Studie von AMD ...", eu.36kr.com, section "Ende-zu-Ende-Effizienz":
+ * MXFP4 training against an FP8 baseline; E4M3 is the FP8 layout named in
+ * "AMD颠覆认知", showapi.com, section 2.2), run on the same shapes and the
+ * same kernels with 8-bit elements.  Read here as OCP MXFP8: blocks of 32
+ * along the contraction dimension share one E8M0 exponent,
+ * floor(log2 amax) - 8 (E4M3's largest exponent), biased by 127 and clamped
+ * to [0, 254] (0xFF: a block holding Inf/NaN, whose codes are zero); each
+ * element becomes the nearest E4M3 value of x * 2^-exponent (ties to even,
+ * magnitudes beyond 448 saturate to 448, sign kept).  No rotation and no
+ * stochastic rounding (the FP8 baseline uses neither).
+ *
+ * Layouts: codes are one byte per element, row-major [lines][k]
+ * (mx_mxfp8_codes_bytes(lines, k) = lines * k); scales use the same tiled
+ * layout and size as MXFP4 (mx_scales_bytes).
+ *
+ * mx_quantize_mxfp8: contraction down the rows of src[rows][cols] (the
+ *   Wgrad operands): codes [cols][rows].  rows % 32 == 0, cols % 8 == 0,
+ *   16-byte aligned pointers.
+ * mx_gemm_mxfp8: C[M][N] = A . B^T (fp32) over MXFP8 operands, contraction
+ *   K (K % 32 == 0, N % 4 == 0); the arguments of mx_gemm otherwise.
+ * mx_linear_wgrad_mxfp8: dW[N][K] = dY^T X with both operands MXFP8-encoded
+ *   along T (one encode launch, one GEMM launch), workspace of
+ *   mx_linear_wgrad_mxfp8_workspace_bytes(T, N, K) bytes, 256-byte aligned.
+ *   T % 32 == 0; N, K % 8 == 0.
+ * Status codes and asynchrony as for the MXFP4 calls.
+ */
+size_t mx_mxfp8_codes_bytes(int64_t mn, int64_t k);
+mx_status mx_quantize_mxfp8(const void *d_src, int64_t rows, int64_t cols, void *d_codes,
+                            void *d_scales, void *stream);
+mx_status mx_gemm_mxfp8(const void *d_Aq, const void *d_As, const void *d_Bq, const void *d_Bs,
+                        float *d_C, int64_t M, int64_t N, int64_t K, void *stream);
+size_t mx_linear_wgrad_mxfp8_workspace_bytes(int64_t T, int64_t N, int64_t K);
+mx_status mx_linear_wgrad_mxfp8(const void *d_dY, const void *d_X, float *d_dW, int64_t T,
+                                int64_t N, int64_t K, void *d_ws, size_t ws_bytes, void *stream);
+
 /* mx_linear_fprop -- Y[T][N] = X W^T, contraction K (K % 32 == 0, N % 4 == 0). */
 mx_status mx_linear_fprop(const void *d_X, const void *d_W, float *d_Y, int64_t T, int64_t N,
                           int64_t K, int rot, int rot_block, int rnd, uint64_t seed,

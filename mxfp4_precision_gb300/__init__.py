@@ -13,7 +13,8 @@ from ._binding import (CONTRACT_COLS, CONTRACT_ROWS, OP_DGRAD, OP_FPROP, OP_WGRA
                        linear_dgrad, linear_fprop, linear_wgrad, linear_wgrad_fused, linear_wgrad_noalloc,
                        linear_workspace_bytes, NOALLOC_SCRATCH_BYTES, quantize, quantize_dual,
                        quantize_pair, quantize_into, scales_bytes, scales_to_canonical,
-                       status_string)
+                       status_string, mxfp8_codes_bytes, quantize_mxfp8, gemm_mxfp8,
+                       gemm_mxfp8_into, linear_wgrad_mxfp8, linear_wgrad_mxfp8_workspace_bytes)
 
 __all__ = [
     "CONTRACT_COLS", "CONTRACT_ROWS", "OP_DGRAD", "OP_FPROP", "OP_WGRAD", "ROT_HADAMARD_DET",
@@ -23,4 +24,6 @@ __all__ = [
     "linear_dgrad", "linear_fprop", "linear_wgrad", "linear_wgrad_fused", "linear_wgrad_noalloc", "linear_workspace_bytes",
     "NOALLOC_SCRATCH_BYTES", "quantize", "quantize_dual", "quantize_pair",
     "quantize_into", "scales_bytes", "scales_to_canonical", "status_string",
+    "mxfp8_codes_bytes", "quantize_mxfp8", "gemm_mxfp8", "gemm_mxfp8_into", "linear_wgrad_mxfp8",
+    "linear_wgrad_mxfp8_workspace_bytes",
 ]

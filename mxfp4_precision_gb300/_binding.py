@@ -25,6 +25,8 @@ EXPORTED = [
     "mx_gemm", "mx_linear_workspace_bytes",
     "mx_linear_wgrad", "mx_linear_fprop", "mx_linear_dgrad", "mx_linear_wgrad_noalloc",
     "mx_linear_wgrad_fused", "mx_linear_wgrad_fused_supported",
+    "mx_mxfp8_codes_bytes", "mx_quantize_mxfp8", "mx_gemm_mxfp8",
+    "mx_linear_wgrad_mxfp8_workspace_bytes", "mx_linear_wgrad_mxfp8",
     "mx_check_status",
     "mx_debug_timeout_probe", "mx_bench_mma", "mx_status_string", "mx_version",
 ]
@@ -82,6 +84,16 @@ def lib() -> ctypes.CDLL:
             L.mx_linear_wgrad_fused.restype = i32
             L.mx_linear_wgrad_fused_supported.argtypes = [i64, i64, i64, i32, i32, i32]
             L.mx_linear_wgrad_fused_supported.restype = i32
+            L.mx_mxfp8_codes_bytes.argtypes = [i64, i64]
+            L.mx_mxfp8_codes_bytes.restype = sz
+            L.mx_quantize_mxfp8.argtypes = [P, i64, i64, P, P, P]
+            L.mx_quantize_mxfp8.restype = i32
+            L.mx_gemm_mxfp8.argtypes = [P, P, P, P, P, i64, i64, i64, P]
+            L.mx_gemm_mxfp8.restype = i32
+            L.mx_linear_wgrad_mxfp8_workspace_bytes.argtypes = [i64, i64, i64]
+            L.mx_linear_wgrad_mxfp8_workspace_bytes.restype = sz
+            L.mx_linear_wgrad_mxfp8.argtypes = [P, P, P, i64, i64, i64, P, sz, P]
+            L.mx_linear_wgrad_mxfp8.restype = i32
             L.mx_check_status.argtypes = [P]
             L.mx_check_status.restype = i32
             L.mx_debug_timeout_probe.argtypes = [i64, P]
@@ -244,6 +256,57 @@ def linear_wgrad(dY, X, rot=ROT_HADAMARD_DET, rot_block=32, rnd=ROUND_RNE, seed=
 
 
 NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+# --------------------------------------------------------------------------- MXFP8 comparator
+def mxfp8_codes_bytes(mn: int, k: int) -> int:
+    return int(lib().mx_mxfp8_codes_bytes(mn, k))
+
+
+def quantize_mxfp8(src: torch.Tensor, stream=None):
+    """MXFP8 encode down the rows of src [rows, cols] (bf16): returns (codes
+    uint8 [cols, rows], scales uint8 [mx_scales_bytes(cols, rows)], tiled)."""
+    src = _as_bf16_bits(src)
+    rows, cols = src.shape
+    codes = torch.empty((cols, rows), dtype=torch.uint8, device=src.device)
+    scales = torch.empty((max(1, scales_bytes(cols, rows)),), dtype=torch.uint8, device=src.device)
+    st = lib().mx_quantize_mxfp8(_dev_ptr(src, "src"), rows, cols, _dev_ptr(codes, "codes"),
+                                 _dev_ptr(scales, "scales"), _stream(stream))
+    _check(st, "mx_quantize_mxfp8")
+    return codes, scales
+
+
+def gemm_mxfp8_into(Aq, As, Bq, Bs, C: torch.Tensor, M: int, N: int, K: int, stream=None) -> None:
+    st = lib().mx_gemm_mxfp8(_dev_ptr(Aq, "Aq"), _dev_ptr(As, "As"), _dev_ptr(Bq, "Bq"),
+                             _dev_ptr(Bs, "Bs"), _dev_ptr(C, "C"), M, N, K, _stream(stream))
+    _check(st, "mx_gemm_mxfp8")
+
+
+def gemm_mxfp8(Aq, As, Bq, Bs, M: int, N: int, K: int, stream=None) -> torch.Tensor:
+    C = torch.empty((M, N), dtype=torch.float32, device=Aq.device)
+    gemm_mxfp8_into(Aq, As, Bq, Bs, C, M, N, K, stream)
+    return C
+
+
+def linear_wgrad_mxfp8_workspace_bytes(T: int, N: int, K: int) -> int:
+    return int(lib().mx_linear_wgrad_mxfp8_workspace_bytes(T, N, K))
+
+
+def linear_wgrad_mxfp8(dY, X, ws=None, out=None, stream=None) -> torch.Tensor:
+    """dW[N, K] = dY^T X with both operands MXFP8-encoded along T; fp32 output."""
+    dY, X = _as_bf16_bits(dY), _as_bf16_bits(X)
+    T, N = dY.shape
+    K = X.shape[1]
+    if ws is None:
+        need = linear_wgrad_mxfp8_workspace_bytes(T, N, K)
+        ws = torch.empty((max(need, 256),), dtype=torch.uint8, device=dY.device)
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.float32, device=dY.device)
+    st = lib().mx_linear_wgrad_mxfp8(_dev_ptr(dY, "dY"), _dev_ptr(X, "X"), _dev_ptr(out, "out"),
+                                     T, N, K, _dev_ptr(ws, "workspace"),
+                                     ws.numel() * ws.element_size(), _stream(stream))
+    _check(st, "mx_linear_wgrad_mxfp8")
+    return out
 
 
 def linear_wgrad_fused(dY, X, rot=ROT_HADAMARD_DET, rot_block=32, rnd=ROUND_RNE, seed=0, ws=None,

@@ -227,6 +227,41 @@ mx_status gemm_impl(const void *Aq, const void *As, const void *Bq, const void *
     return from_cuda(launch_gemm(Aq, As, Bq, Bs, C, M, N, K, *dev, stream));
 }
 
+// MXFP8 comparator: encode down the rows of one or two operands, contract.
+mx_status quantize_mxfp8_impl(const void *src0, int64_t rows0, int64_t cols0, const void *src1,
+                              int64_t rows1, int64_t cols1, void *codes0, void *scales0,
+                              void *codes1, void *scales1, cudaStream_t stream) {
+    mx_status st = check_encode(src0, rows0, cols0, MX_CONTRACT_ROWS, MX_ROT_NONE, 32,
+                                MX_ROUND_RNE, codes0, scales0);
+    if (st != MX_OK) return st;
+    if (src1 != nullptr) {
+        st = check_encode(src1, rows1, cols1, MX_CONTRACT_ROWS, MX_ROT_NONE, 32, MX_ROUND_RNE,
+                          codes1, scales1);
+        if (st != MX_OK) return st;
+        if (rows1 == 0 || cols1 == 0) src1 = nullptr;
+    }
+    if (rows0 == 0 || cols0 == 0) {
+        if (src1 == nullptr) return MX_OK;
+        src0 = src1, rows0 = rows1, cols0 = cols1, codes0 = codes1, scales0 = scales1;
+        src1 = nullptr;
+    }
+    const DeviceInfo *dev = nullptr;
+    if ((st = device_or_error(&dev)) != MX_OK) return st;
+    return from_cuda(launch_quantize_mxfp8_colwise(src0, rows0, cols0, src1, rows1, cols1, codes0,
+                                                   scales0, codes1, scales1, *dev, stream));
+}
+
+mx_status gemm_mxfp8_impl(const void *Aq, const void *As, const void *Bq, const void *Bs,
+                          float *C, int64_t M, int64_t N, int64_t K, cudaStream_t stream) {
+    mx_status st = check_gemm(Aq, As, Bq, Bs, C, M, N, K);
+    if (st != MX_OK || M == 0 || N == 0) return st;
+    if (K == 0)
+        return from_cuda(cudaMemsetAsync(C, 0, static_cast<size_t>(M) * N * sizeof(float), stream));
+    const DeviceInfo *dev = nullptr;
+    if ((st = device_or_error(&dev)) != MX_OK) return st;
+    return from_cuda(launch_gemm_fmt(true, Aq, As, Bq, Bs, C, M, N, K, *dev, stream));
+}
+
 // Quantise both operands of a linear op into the workspace, then contract.
 mx_status linear_impl(int op, const void *a_src, int64_t a_rows, int64_t a_cols, int a_contract,
                       const void *b_src, int64_t b_rows, int64_t b_cols, int b_contract, float *out,
@@ -391,6 +426,57 @@ mx_status mx_linear_dgrad(const void *d_dY, const void *d_W, float *d_dX, int64_
     return linear_impl(MX_OP_DGRAD, d_dY, T, N, MX_CONTRACT_COLS, d_W, N, K, MX_CONTRACT_ROWS,
                        d_dX, T, N, K, rot, rot_block, rnd, seed, d_ws, ws_bytes,
                        static_cast<cudaStream_t>(stream));
+}
+
+size_t mx_mxfp8_codes_bytes(int64_t mn, int64_t k) {
+    if (mn <= 0 || k <= 0) return 0;
+    return static_cast<size_t>(mn) * static_cast<size_t>(k);
+}
+
+mx_status mx_quantize_mxfp8(const void *d_src, int64_t rows, int64_t cols, void *d_codes,
+                            void *d_scales, void *stream) {
+    TraceRange trace("mx_quantize_mxfp8");
+    return quantize_mxfp8_impl(d_src, rows, cols, nullptr, 0, 0, d_codes, d_scales, nullptr,
+                               nullptr, static_cast<cudaStream_t>(stream));
+}
+
+mx_status mx_gemm_mxfp8(const void *d_Aq, const void *d_As, const void *d_Bq, const void *d_Bs,
+                        float *d_C, int64_t M, int64_t N, int64_t K, void *stream) {
+    TraceRange trace("mx_gemm_mxfp8");
+    return gemm_mxfp8_impl(d_Aq, d_As, d_Bq, d_Bs, d_C, M, N, K,
+                           static_cast<cudaStream_t>(stream));
+}
+
+size_t mx_linear_wgrad_mxfp8_workspace_bytes(int64_t T, int64_t N, int64_t K) {
+    if (T <= 0 || N <= 0 || K <= 0) return 0;
+    return align256(mx_mxfp8_codes_bytes(N, T)) + align256(mx_scales_bytes(N, T)) +
+           align256(mx_mxfp8_codes_bytes(K, T)) + align256(mx_scales_bytes(K, T));
+}
+
+mx_status mx_linear_wgrad_mxfp8(const void *d_dY, const void *d_X, float *d_dW, int64_t T,
+                                int64_t N, int64_t K, void *d_ws, size_t ws_bytes, void *stream) {
+    TraceRange trace("mx_linear_wgrad_mxfp8");
+    const cudaStream_t st_ = static_cast<cudaStream_t>(stream);
+    if (T < 0 || N < 0 || K < 0) return MX_ERR_SHAPE;
+    if (N == 0 || K == 0) return MX_OK;
+    if (d_dW == nullptr) return MX_ERR_INVALID_ARG;
+    if (T == 0) return gemm_mxfp8_impl(nullptr, nullptr, nullptr, nullptr, d_dW, N, K, 0, st_);
+    mx_status st = check_encode(d_dY, T, N, MX_CONTRACT_ROWS, MX_ROT_NONE, 32, MX_ROUND_RNE,
+                                d_dY, d_dY);
+    if (st != MX_OK) return st;
+    st = check_encode(d_X, T, K, MX_CONTRACT_ROWS, MX_ROT_NONE, 32, MX_ROUND_RNE, d_X, d_X);
+    if (st != MX_OK) return st;
+    if (K % 4 != 0 || !aligned16(d_dW)) return MX_ERR_ALIGN;
+    if (d_ws == nullptr || ws_bytes < mx_linear_wgrad_mxfp8_workspace_bytes(T, N, K))
+        return MX_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(d_ws) & 255u) != 0) return MX_ERR_ALIGN;
+    uint8_t *aq = static_cast<uint8_t *>(d_ws);
+    uint8_t *as = aq + align256(mx_mxfp8_codes_bytes(N, T));
+    uint8_t *bq = as + align256(mx_scales_bytes(N, T));
+    uint8_t *bs = bq + align256(mx_mxfp8_codes_bytes(K, T));
+    st = quantize_mxfp8_impl(d_dY, T, N, d_X, T, K, aq, as, bq, bs, st_);
+    if (st != MX_OK) return st;
+    return gemm_mxfp8_impl(aq, as, bq, bs, d_dW, N, K, T, st_);
 }
 
 int mx_linear_wgrad_fused_supported(int64_t T, int64_t N, int64_t K, int rot, int rot_block,

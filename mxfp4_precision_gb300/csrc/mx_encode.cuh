@@ -306,6 +306,63 @@ __device__ __forceinline__ uint32_t encode_block32(const float (&r)[32], uint4 &
     return sb;
 }
 
+// ---------------------------------------------------------------- MXFP8
+// E8M0 byte of an MXFP8 block (E4M3 elements, largest exponent 8) and its
+// exact inverse power of two: floor(log2 amax) - 8 + 127, clamped at 0.
+__device__ __forceinline__ uint32_t scale_of_e4m3(float amax, float &inv) {
+    const uint32_t m = __float_as_uint(amax);
+    const uint32_t e = m >> 23;                 // biased exponent (0: zero/subnormal)
+    const uint32_t sb = e >= 8u ? e - 8u : 0u;  // at most 247, so 2^(127 - sb) is normal
+    inv = __uint_as_float((254u - sb) << 23);   // 2^(127 - sb)
+    return m >= 0x7F800000u ? 0xFFu : sb;       // Inf/NaN in the block: NaN scale
+}
+
+// Four E4M3 codes (round to nearest even, saturating at +-448), v0 in the
+// low byte.  The packed conversion puts its first source in the upper byte.
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float v0, float v1, float v2, float v3) {
+    uint32_t out;
+    asm("{\n\t.reg .b16 h0, h1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 h0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 h1, %4, %3;\n\t"
+        "mov.b32 %0, {h0, h1};\n\t}"
+        : "=r"(out)
+        : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
+    return out;
+}
+
+// MXFP8 encode of two channels' blocks of 32 held as pairs (no rotation):
+// 32 code bytes per channel in q0 / q1.  The scaled value fl(x * 2^-s) is
+// exact for every scale this rule yields unless it is an fp32 subnormal,
+// which lies far below E4M3's smallest subnormal (2^-9) and rounds to a
+// signed zero either way.
+__device__ __forceinline__ void encode_pair_e4m3(const uint64_t (&x)[32], uint4 (&q0)[2],
+                                                 uint4 (&q1)[2], uint32_t &s0, uint32_t &s1) {
+    float l[32], h[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) unpack2(x[i], l[i], h[i]);
+    float inv0, inv1;
+    s0 = scale_of_e4m3(block_amax32(l), inv0);
+    s1 = scale_of_e4m3(block_amax32(h), inv1);
+    const uint64_t mult = pack2(inv0, inv1);
+    float v0[32], v1[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) unpack2(mul2(x[i], mult), v0[i], v1[i]);
+    uint32_t w0[8], w1[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        w0[j] = cvt_e4m3x4(v0[4 * j], v0[4 * j + 1], v0[4 * j + 2], v0[4 * j + 3]);
+        w1[j] = cvt_e4m3x4(v1[4 * j], v1[4 * j + 1], v1[4 * j + 2], v1[4 * j + 3]);
+    }
+    const bool z0 = s0 == 0xFFu, z1 = s1 == 0xFFu;  // NaN scale: zero codes
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        q0[k] = z0 ? make_uint4(0, 0, 0, 0)
+                   : make_uint4(w0[4 * k], w0[4 * k + 1], w0[4 * k + 2], w0[4 * k + 3]);
+        q1[k] = z1 ? make_uint4(0, 0, 0, 0)
+                   : make_uint4(w1[4 * k], w1[4 * k + 1], w1[4 * k + 2], w1[4 * k + 3]);
+    }
+}
+
 __device__ __forceinline__ void st_global_16(void *p, uint4 v) {
     asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
                  "r"(v.z), "r"(v.w)

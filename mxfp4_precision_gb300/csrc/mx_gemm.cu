@@ -79,7 +79,15 @@ struct Variant {
     static_assert(kThreads * kLaunchRegs <= 65536, "launch registers fit the SM");
 };
 constexpr uint32_t kSubBytes = kHalf * kBKBytes;  // 16 KB: 128 rows x one K sub-tile
-constexpr uint32_t kSFSub = 1024;                 // scales of 128 rows x one K sub-tile
+constexpr uint32_t kSFSub = 1024;                 // scale room of 128 rows x one K sub-tile
+// Element formats: a 128-byte K sub-tile row holds 256 E2M1 (MXFP4: two
+// 512-byte scale atoms per 128 rows) or 128 E4M3 (MXFP8: one atom).
+template <bool F8>
+struct Elem {
+    static constexpr int kSubK = F8 ? 128 : 256;          // elements per sub-tile row
+    static constexpr int kAtoms = F8 ? 1 : 2;             // scale atoms per sub-tile
+    static constexpr uint32_t kSFBytes = 512u * kAtoms;   // scale bytes per 128 rows
+};
 constexpr uint32_t kOffA = 0;
 constexpr uint32_t kOffB = kKSub * kSubBytes;
 constexpr uint32_t kOffSFA = 2 * kKSub * kSubBytes;
@@ -323,12 +331,14 @@ __device__ __forceinline__ void encode_units(const FusedArgs &f, int gw, int W, 
     }
 }
 
-template <bool FUSED>
+template <bool FUSED, bool F8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b, const GemmArgs g,
                    const __grid_constant__ FusedArgs f) {
     using V = Variant<FUSED>;
+    using E = Elem<F8>;
+    static_assert(!(FUSED && F8), "the fused launch encodes MXFP4 only");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned base, kept as a shared-space pointer (offset arithmetic
     // only) so that the compiler emits shared-memory loads.  The offset is the
@@ -407,21 +417,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThr
                         }
                     }
                     if (scales) {
+                        const uint32_t sub_bytes = static_cast<uint32_t>(nsub) * E::kSFBytes;
                         uint32_t bytes = 0;
-                        if (ga < g.a_groups) bytes += static_cast<uint32_t>(nsub) * kSFSub;
+                        if (ga < g.a_groups) bytes += sub_bytes;
                         for (int rb = 0; rb < 2; ++rb)
-                            if (2 * static_cast<int64_t>(nb) + rb < g.b_groups)
-                                bytes += static_cast<uint32_t>(nsub) * kSFSub;
+                            if (2 * static_cast<int64_t>(nb) + rb < g.b_groups) bytes += sub_bytes;
                         mbar_arrive_expect_tx(&ctl->sf_full[stage], bytes);
                         if (ga < g.a_groups)
-                            bulk_load(st + kOffSFA, g.As + (ga * g.katoms + 2 * kt0) * 512,
-                                      static_cast<uint32_t>(nsub) * kSFSub, &ctl->sf_full[stage]);
+                            bulk_load(st + kOffSFA, g.As + (ga * g.katoms + E::kAtoms * kt0) * 512,
+                                      sub_bytes, &ctl->sf_full[stage]);
                         for (int rb = 0; rb < 2; ++rb) {
                             const int64_t gb = 2 * static_cast<int64_t>(nb) + rb;
                             if (gb < g.b_groups)
                                 bulk_load(st + kOffSFB + rb * kKSub * kSFSub,
-                                          g.Bs + (gb * g.katoms + 2 * kt0) * 512,
-                                          static_cast<uint32_t>(nsub) * kSFSub, &ctl->sf_full[stage]);
+                                          g.Bs + (gb * g.katoms + E::kAtoms * kt0) * 512,
+                                          sub_bytes, &ctl->sf_full[stage]);
                         }
                     } else {
                         // Both CTAs' operand loads complete on the even CTA's
@@ -453,6 +463,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThr
             bool ok = true;
             const uint32_t idesc0 = idesc_mxf4(2 * kHalf, kTile, 0, 0);
             const uint32_t idesc2 = idesc_mxf4(2 * kHalf, kTile, 2, 2);
+            uint32_t idesc8[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) idesc8[j] = idesc_mxf8(2 * kHalf, kTile, j, j);
             for (int w = pair; ok && w < g.num_items; w += npairs) {
                 const Item it = item_of(g, w);
                 if (!mbar_wait_inl(&ctl->acc_empty, acc_phase ^ 1u, g.status, abort)) break;
@@ -474,11 +487,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThr
                         const uint32_t sf = slot + 24u * static_cast<uint32_t>(u);
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            const uint32_t ka = static_cast<uint32_t>(j / 2);
-                            mma_mxf4_pair(tmem + kAccCol, sdesc_sw128(sa + 32u * j),
-                                          sdesc_sw128(sb + 32u * j), (j & 1) ? idesc2 : idesc0,
-                                          sf + 4u * ka, sf + 8u + 8u * ka,
-                                          (ks > it.ks0 || u > 0 || j > 0) ? 1u : 0u);
+                            const uint32_t acc = (ks > it.ks0 || u > 0 || j > 0) ? 1u : 0u;
+                            if constexpr (F8) {
+                                // K = 32 per MMA: block j of the sub-tile's
+                                // single scale atom (byte j of its columns).
+                                mma_mxf8_pair(tmem + kAccCol, sdesc_sw128(sa + 32u * j),
+                                              sdesc_sw128(sb + 32u * j), idesc8[j], sf, sf + 8u,
+                                              acc);
+                            } else {
+                                const uint32_t ka = static_cast<uint32_t>(j / 2);
+                                mma_mxf4_pair(tmem + kAccCol, sdesc_sw128(sa + 32u * j),
+                                              sdesc_sw128(sb + 32u * j), (j & 1) ? idesc2 : idesc0,
+                                              sf + 4u * ka, sf + 8u + 8u * ka, acc);
+                            }
                         }
                     }
                     tc_commit_pair(&ctl->empty[stage], 0x3);
@@ -529,8 +550,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThr
                 const uint32_t slot =
                     lane_base + kSFCol + kSFSlot * static_cast<uint32_t>(stage);
                 for (int u = 0; u < nsub; ++u) {
-                    const uint8_t *sfa = st + kOffSFA + u * kSFSub;
-                    const uint8_t *sfb = st + kOffSFB + u * kSFSub;
+                    const uint8_t *sfa = st + kOffSFA + u * E::kSFBytes;
+                    const uint8_t *sfb = st + kOffSFB + u * E::kSFBytes;
+                    const uint32_t col = slot + 24u * static_cast<uint32_t>(u);
+                    if constexpr (F8) {
+                        // One atom: A at columns 0..3, B at 8..15 (ka = 0).
+                        uint32_t a4[4], b8[8];
+                        const uint4 va = *reinterpret_cast<const uint4 *>(sfa + lane * 16);
+                        a4[0] = va.x;
+                        a4[1] = va.y;
+                        a4[2] = va.z;
+                        a4[3] = va.w;
+#pragma unroll
+                        for (int rb = 0; rb < 2; ++rb) {
+                            const uint4 v = *reinterpret_cast<const uint4 *>(
+                                sfb + rb * kKSub * kSFSub + lane * 16);
+                            b8[4 * rb + 0] = v.x;
+                            b8[4 * rb + 1] = v.y;
+                            b8[4 * rb + 2] = v.z;
+                            b8[4 * rb + 3] = v.w;
+                        }
+                        tmem_st_32x32b_x4(col, a4);
+                        tmem_st_32x32b_x8(col + 8u, b8);
+                        continue;
+                    }
                     uint32_t a[8], b[16];
 #pragma unroll
                     for (int ka = 0; ka < 2; ++ka) {
@@ -551,7 +594,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThr
                             b[8 * ka + 4 * rb + 2] = v.z;
                             b[8 * ka + 4 * rb + 3] = v.w;
                         }
-                    const uint32_t col = slot + 24u * static_cast<uint32_t>(u);
                     tmem_st_32x32b_x8(col, a);
                     tmem_st_32x32b_x16(col + 8u, b);
                 }
@@ -700,34 +742,37 @@ constexpr size_t kGemmSmem = kStages * kStageBytes + sizeof(SharedCtl) + 1024;
 
 // Co-resident 2-CTA clusters of a mx_gemm_kernel variant on a device,
 // measured once.
-template <bool FUSED>
+template <bool FUSED, bool F8>
 int gemm_clusters(const DeviceInfo &dev) {
     static std::atomic<int> cache[64];
     const int idx = dev.ordinal >= 0 && dev.ordinal < 64 ? dev.ordinal : 0;
     int n = cache[idx].load(std::memory_order_relaxed);
     if (n > 0) return n;
-    if (cudaFuncSetAttribute(mx_gemm_kernel<FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(mx_gemm_kernel<FUSED, F8>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kGemmSmem)) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(2, 1, 1);
     cfg.blockDim = dim3(Variant<FUSED>::kThreads, 1, 1);
     cfg.dynamicSmemBytes = kGemmSmem;
-    if (cudaOccupancyMaxActiveClusters(&n, mx_gemm_kernel<FUSED>, &cfg) != cudaSuccess || n < 1)
+    if (cudaOccupancyMaxActiveClusters(&n, mx_gemm_kernel<FUSED, F8>, &cfg) != cudaSuccess ||
+        n < 1)
         return 0;
     cache[idx].store(n, std::memory_order_relaxed);
     return n;
 }
 
 // Common set-up of both variants: tensor maps and the GEMM arguments.
-bool gemm_setup(const void *Aq, const void *As, const void *Bq, const void *Bs, float *C,
-                int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, CUtensorMap *map_a,
-                CUtensorMap *map_b, GemmArgs *g) {
-    if (!encode_tmap_2d(map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, Aq, K / 2, M, K / 2, kBKBytes, kHalf,
-                        CU_TENSOR_MAP_SWIZZLE_128B))
+bool gemm_setup(bool f8, const void *Aq, const void *As, const void *Bq, const void *Bs,
+                float *C, int64_t M, int64_t N, int64_t K, const DeviceInfo &dev,
+                CUtensorMap *map_a, CUtensorMap *map_b, GemmArgs *g) {
+    const int64_t row_bytes = f8 ? K : K / 2;
+    if (!encode_tmap_2d(map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, Aq, row_bytes, M, row_bytes,
+                        kBKBytes, kHalf, CU_TENSOR_MAP_SWIZZLE_128B))
         return false;
-    if (!encode_tmap_2d(map_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, Bq, K / 2, N, K / 2, kBKBytes, kHalf,
-                        CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!encode_tmap_2d(map_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, Bq, row_bytes, N, row_bytes,
+                        kBKBytes, kHalf, CU_TENSOR_MAP_SWIZZLE_128B))
         return false;
     *g = GemmArgs{};
     g->As = static_cast<const uint8_t *>(As);
@@ -739,7 +784,8 @@ bool gemm_setup(const void *Aq, const void *As, const void *Bq, const void *Bs, 
     g->katoms = scale_katoms(K);
     g->a_groups = scale_groups(M);
     g->b_groups = scale_groups(N);
-    g->k_tiles = static_cast<int>((K + 255) / 256);
+    const int64_t sub_k = f8 ? Elem<true>::kSubK : Elem<false>::kSubK;
+    g->k_tiles = static_cast<int>((K + sub_k - 1) / sub_k);
     g->k_stages = (g->k_tiles + kKSub - 1) / kKSub;
     const int64_t m_tiles = (M + kTile - 1) / kTile;
     const int64_t n_tiles = (N + kTile - 1) / kTile;
@@ -754,10 +800,10 @@ bool gemm_setup(const void *Aq, const void *As, const void *Bq, const void *Bs, 
     return true;
 }
 
-template <bool FUSED>
+template <bool FUSED, bool F8>
 cudaError_t gemm_launch(const CUtensorMap &map_a, const CUtensorMap &map_b, const GemmArgs &g,
                         const FusedArgs &f, int pairs, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel<FUSED>,
+    cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel<FUSED, F8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kGemmSmem));
     if (e != cudaSuccess) return e;
@@ -771,27 +817,43 @@ cudaError_t gemm_launch(const CUtensorMap &map_a, const CUtensorMap &map_b, cons
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, mx_gemm_kernel<FUSED>, map_a, map_b, g, f);
+    e = cudaLaunchKernelEx(&cfg, mx_gemm_kernel<FUSED, F8>, map_a, map_b, g, f);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_gemm(const void *Aq, const void *As, const void *Bq, const void *Bs, float *C,
-                        int64_t M, int64_t N, int64_t K, const DeviceInfo &dev,
-                        cudaStream_t stream) {
+namespace {
+template <bool F8>
+cudaError_t launch_gemm_elem(const void *Aq, const void *As, const void *Bq, const void *Bs,
+                             float *C, int64_t M, int64_t N, int64_t K, const DeviceInfo &dev,
+                             cudaStream_t stream) {
     CUtensorMap map_a, map_b;
     GemmArgs g;
-    if (!gemm_setup(Aq, As, Bq, Bs, C, M, N, K, dev, &map_a, &map_b, &g))
+    if (!gemm_setup(F8, Aq, As, Bq, Bs, C, M, N, K, dev, &map_a, &map_b, &g))
         return cudaErrorInvalidValue;
     // Resident CTAs: as many 2-CTA clusters as fit at once, one tile per pair.
-    const int pairs_max = gemm_clusters<false>(dev);
+    const int pairs_max = gemm_clusters<false, F8>(dev);
     if (pairs_max < 1) return cudaErrorLaunchOutOfResources;
     const int pairs = g.num_items < pairs_max ? g.num_items : pairs_max;
     FusedArgs f;
     std::memset(&f, 0, sizeof(f));
-    return gemm_launch<false>(map_a, map_b, g, f, pairs, stream);
+    return gemm_launch<false, F8>(map_a, map_b, g, f, pairs, stream);
+}
+}  // namespace
+
+cudaError_t launch_gemm(const void *Aq, const void *As, const void *Bq, const void *Bs, float *C,
+                        int64_t M, int64_t N, int64_t K, const DeviceInfo &dev,
+                        cudaStream_t stream) {
+    return launch_gemm_elem<false>(Aq, As, Bq, Bs, C, M, N, K, dev, stream);
+}
+
+cudaError_t launch_gemm_fmt(bool f8, const void *Aq, const void *As, const void *Bq,
+                            const void *Bs, float *C, int64_t M, int64_t N, int64_t K,
+                            const DeviceInfo &dev, cudaStream_t stream) {
+    return f8 ? launch_gemm_elem<true>(Aq, As, Bq, Bs, C, M, N, K, dev, stream)
+              : launch_gemm_elem<false>(Aq, As, Bq, Bs, C, M, N, K, dev, stream);
 }
 
 size_t wgrad_fused_counter_bytes(int64_t T, int64_t N, int64_t K) {
@@ -816,9 +878,9 @@ cudaError_t launch_wgrad_fused(const void *dY, const void *X, float *dW, int64_t
     CUtensorMap map_a, map_b;
     GemmArgs g;
     // dW[N][K] = A . B^T with A = dY^T (N lines), B = X^T (K lines), contraction T.
-    if (!gemm_setup(Aq, As, Bq, Bs, dW, N, K, T, dev, &map_a, &map_b, &g))
+    if (!gemm_setup(false, Aq, As, Bq, Bs, dW, N, K, T, dev, &map_a, &map_b, &g))
         return cudaErrorInvalidValue;
-    const int pairs_max = gemm_clusters<true>(dev);
+    const int pairs_max = gemm_clusters<true, false>(dev);
     if (pairs_max < 1) return cudaErrorLaunchOutOfResources;
     const int pairs = g.num_items < pairs_max ? g.num_items : pairs_max;
 
@@ -867,7 +929,7 @@ cudaError_t launch_wgrad_fused(const void *dY, const void *X, float *dW, int64_t
     f.units = kUnitsPerChunk * f.chunks * np;
     cudaError_t e = cudaMemsetAsync(counters, 0, wgrad_fused_counter_bytes(T, N, K), stream);
     if (e != cudaSuccess) return e;
-    return gemm_launch<true>(map_a, map_b, g, f, pairs, stream);
+    return gemm_launch<true, false>(map_a, map_b, g, f, pairs, stream);
 }
 
 }  // namespace mx

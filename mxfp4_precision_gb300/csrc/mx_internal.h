@@ -50,6 +50,20 @@ cudaError_t launch_quantize_dual(const void *src, int64_t rows, int64_t cols, in
                                  void *scales_t, void *codes_n, void *scales_n,
                                  const DeviceInfo &dev, cudaStream_t stream);
 
+// MXFP8 (E4M3 elements, the FP8 comparator) encode down the rows of one or
+// two operands (src1 == nullptr: one) in one launch; no rotation, round to
+// nearest.  Codes [cols][rows] bytes, scales in the tiled layout.
+cudaError_t launch_quantize_mxfp8_colwise(const void *src0, int64_t rows0, int64_t cols0,
+                                          const void *src1, int64_t rows1, int64_t cols1,
+                                          void *codes0, void *scales0, void *codes1,
+                                          void *scales1, const DeviceInfo &dev,
+                                          cudaStream_t stream);
+
+// Block-scaled GEMM over MXFP4 (f8 false) or MXFP8 (f8 true) operands.
+cudaError_t launch_gemm_fmt(bool f8, const void *Aq, const void *As, const void *Bq,
+                            const void *Bs, float *C, int64_t M, int64_t N, int64_t K,
+                            const DeviceInfo &dev, cudaStream_t stream);
+
 cudaError_t launch_gemm(const void *Aq, const void *As, const void *Bq, const void *Bs, float *C,
                         int64_t M, int64_t N, int64_t K, const DeviceInfo &dev,
                         cudaStream_t stream);

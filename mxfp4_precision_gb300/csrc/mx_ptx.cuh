@@ -388,6 +388,32 @@ __device__ __forceinline__ void mma_mxf4_pair(uint32_t d_tmem, uint64_t a_desc, 
         : "memory");
 }
 
+// Instruction descriptor for kind::mxf8f6f4 with E4M3 x E4M3 operands, E8M0
+// scales (scale_vec::1X: one scale byte per row per MMA, selected by the
+// scale-factor ids), fp32 accumulate, K-major, tile M x N.
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int a_sf_id, int b_sf_id) {
+    return (static_cast<uint32_t>(b_sf_id & 3) << 4)      // B scale-factor id
+           | (0u << 7)                                    // A format: E4M3
+           | (0u << 10)                                   // B format: E4M3
+           | (static_cast<uint32_t>(N >> 3) << 17)        // N / 8
+           | (1u << 23)                                   // scale format: UE8M0
+           | (static_cast<uint32_t>(M >> 4) << 24)        // M / 16
+           | (static_cast<uint32_t>(a_sf_id & 3) << 29);  // A scale-factor id
+}
+
+// The MXFP8 form of mma_mxf4_pair (K = 32 per instruction).
+__device__ __forceinline__ void mma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
+        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive on the barrier at shared offset `bar` of every CTA in `cta_mask`
 // once every pair operation issued so far by this thread has completed.
 __device__ __forceinline__ void tc_commit_pair(uint64_t *bar, uint16_t cta_mask) {
@@ -400,6 +426,11 @@ __device__ __forceinline__ void tc_commit_pair(uint64_t *bar, uint16_t cta_mask)
 
 // Each thread of the warp writes its registers into consecutive 32-bit
 // columns of its own tensor-memory lane.
+__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, const uint32_t (&v)[4]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr),
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3])
+                 : "memory");
+}
 __device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&v)[8]) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(
                      taddr),

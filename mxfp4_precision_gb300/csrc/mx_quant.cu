@@ -198,7 +198,9 @@ struct ColTile {
 // all eight compute warps have released it, so no compute warp waits for the
 // slowest one.  (The dual variant keeps its registers for the row encode and
 // refills from thread 0 instead.)
-template <int ROTN, bool RAND, bool SR, bool DUAL>
+// With F8 (MXFP8, the FP8 comparator: no rotation, round to nearest) each
+// block becomes 32 E4M3 code bytes under the same E8M0 scale layout.
+template <int ROTN, bool RAND, bool SR, bool DUAL, bool F8 = false>
 __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads, SR ? 1 : kColMinBlocks)
     mxq_colwise_kernel(
     const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
@@ -326,6 +328,22 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads, SR ? 1 
         const int64_t c = c0 + 64 * chalf + 2 * lane;  // first of the thread's two channels
         uint4 q0, q1;
         uint32_t s0, s1;
+        if constexpr (F8) {
+            static_assert(ROTN == 0 && !RAND && !SR && !DUAL, "MXFP8: plain encode only");
+            uint4 p0[2], p1[2];
+            encode_pair_e4m3(x, p0, p1, s0, s1);
+            if (tb < L) {
+                uint8_t *d0 = codes + c * L + tb, *d1 = codes + (c + 1) * L + tb;
+                if (c < lines && MX_STORE_OK(d0, 32, codes, codes_bytes, a0.status)) {
+                    st_global_16(d0, p0[0]);
+                    st_global_16(d0 + 16, p0[1]);
+                }
+                if (c + 1 < lines && MX_STORE_OK(d1, 32, codes, codes_bytes, a0.status)) {
+                    st_global_16(d1, p1[0]);
+                    st_global_16(d1 + 16, p1[1]);
+                }
+            }
+        } else {
         if (SR) {
             const uint64_t tag = second ? a1.sr_tag : a0.sr_tag;
             float x0[32], x1[32];
@@ -345,6 +363,7 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads, SR ? 1 
             if (c < lines && MX_STORE_OK(d0, 16, codes, codes_bytes, a0.status)) st_global_16(d0, q0);
             if (c + 1 < lines && MX_STORE_OK(d1, 16, codes, codes_bytes, a0.status))
                 st_global_16(d1, q1);
+        }
         }
         // Scale bytes (padding lines / blocks included: their input is zero).
         const int64_t kb = tb / 32;
@@ -778,14 +797,14 @@ cudaError_t launch_dir(int rot, int rot_block, bool sr, const Operands &o, const
 // Fills the per-operand arguments (and tensor map) of one encode.
 bool prepare_operand(const void *src, int64_t rows, int64_t cols, bool colwise, int col_tt,
                      uint64_t seed, uint64_t sr_tag, void *codes, void *scales,
-                     const DeviceInfo &dev, CUtensorMap *map, QuantArgs *a) {
+                     const DeviceInfo &dev, CUtensorMap *map, QuantArgs *a, bool f8 = false) {
     *a = QuantArgs{};
     a->L = colwise ? rows : cols;
     a->lines = colwise ? cols : rows;
     a->katoms = scale_katoms(a->L);
     a->codes = static_cast<uint8_t *>(codes);
     a->scales = static_cast<uint8_t *>(scales);
-    a->codes_bytes = static_cast<size_t>(a->lines) * static_cast<size_t>(a->L / 2);
+    a->codes_bytes = static_cast<size_t>(a->lines) * static_cast<size_t>(f8 ? a->L : a->L / 2);
     a->scales_bytes = static_cast<size_t>(128 * scale_groups(a->lines)) *
                       static_cast<size_t>(4 * scale_katoms(a->L));
     a->seed = seed;
@@ -872,6 +891,28 @@ cudaError_t launch_quantize_dual(const void *src, int64_t rows, int64_t cols, in
     o.ar.status = dev.status;
     o.dual = true;
     return launch_dir<true>(rot, rot_block, rnd == 1, o, dev, stream);
+}
+
+cudaError_t launch_quantize_mxfp8_colwise(const void *src0, int64_t rows0, int64_t cols0,
+                                          const void *src1, int64_t rows1, int64_t cols1,
+                                          void *codes0, void *scales0, void *codes1,
+                                          void *scales1, const DeviceInfo &dev,
+                                          cudaStream_t stream) {
+    Operands o;
+    if (!prepare_operand(src0, rows0, cols0, true, 128, 0, 1, codes0, scales0, dev, &o.map0,
+                         &o.a0, true))
+        return cudaErrorInvalidValue;
+    o.map1 = o.map0;
+    o.a1 = QuantArgs{};
+    if (src1 != nullptr &&
+        !prepare_operand(src1, rows1, cols1, true, 128, 0, 2, codes1, scales1, dev, &o.map1,
+                         &o.a1, true))
+        return cudaErrorInvalidValue;
+    o.ar = QuantArgs{};
+    const size_t smem = kStages * kTileBytes + 1024 + 1024;
+    return launch_persistent_n(mxq_colwise_kernel<0, false, false, false, true>,
+                               kColProducerThreads, o.a0.num_tiles + o.a1.num_tiles, smem, dev,
+                               stream, o.map0, o.map1, o.a0, o.a1, o.ar);
 }
 
 }  // namespace mx
