@@ -23,7 +23,7 @@ _HDR = os.path.join(_HERE, "mx_oracle.h")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _SO = os.path.join(_BUILD_DIR, "liboracle.so")
 
-FMT_MXFP4, FMT_MXFP8 = 0, 1
+FMT_MXFP4, FMT_MXFP8, FMT_NVFP4 = 0, 1, 2
 ROT_NONE, ROT_HADAMARD_DET, ROT_HADAMARD_RAND = 0, 1, 2
 ROUND_RNE, ROUND_SR = 0, 1
 CONTRACT_ROWS, CONTRACT_COLS = 0, 1
@@ -91,9 +91,18 @@ def lib() -> ctypes.CDLL:
             L.oracle_quantize_mxfp8.argtypes = [P, i64, i64, i32, i32, i32, u64, P, i64, i32,
                                                 P, P]
             L.oracle_quantize_mxfp8.restype = i32
-            L.oracle_dequantize_fmt.argtypes = [i32, P, P, i64, i64, P]
-            L.oracle_gemm_entries_fmt.argtypes = [i32, P, P, P, P, i64, P, P, i64, P, P]
-            L.oracle_gemm_rows_fmt.argtypes = [i32, P, P, P, P, i64, i64, i64, i64, i64, P, P]
+            d = ctypes.c_double
+            L.oracle_dequantize_fmt.argtypes = [i32, P, P, i64, i64, d, P]
+            L.oracle_gemm_entries_fmt.argtypes = [i32, P, P, d, P, P, d, i64, P, P, i64, P, P]
+            L.oracle_gemm_rows_fmt.argtypes = [i32, P, P, d, P, P, d, i64, i64, i64, i64, i64,
+                                               P, P]
+            L.oracle_nvfp4_tensor_scale.argtypes = [ctypes.c_float]
+            L.oracle_nvfp4_tensor_scale.restype = ctypes.c_float
+            L.oracle_nvfp4_block_scale.argtypes = [ctypes.c_float, ctypes.c_float]
+            L.oracle_nvfp4_block_scale.restype = ctypes.c_uint8
+            L.oracle_quantize_nvfp4.argtypes = [P, i64, i64, i32, i32, i32, u64, P, i64, i32,
+                                                P, P, P, P]
+            L.oracle_quantize_nvfp4.restype = i32
             _lib = L
     return _lib
 
@@ -251,20 +260,54 @@ def quantize_mxfp8(src_bf16: np.ndarray, contract: int, rot: int = ROT_NONE,
     return codes, scales
 
 
+def nvfp4_tensor_scale(amax: float) -> float:
+    return float(lib().oracle_nvfp4_tensor_scale(amax))
+
+
+def nvfp4_block_scale(block_amax: float, s_enc: float) -> int:
+    return int(lib().oracle_nvfp4_block_scale(block_amax, s_enc))
+
+
+def quantize_nvfp4(src_bf16: np.ndarray, contract: int, rot: int = ROT_NONE,
+                   rot_block: int = 16, seed: int = 0, lines=None, precise: bool = False):
+    """NVFP4-encode bf16 bits src[rows, cols]: returns (codes [lines, L/2],
+    canonical scales [lines, L/16], tensor amax, s_enc)."""
+    src = np.ascontiguousarray(src_bf16, dtype=np.uint16)
+    rows, cols = src.shape
+    L = rows if contract == CONTRACT_ROWS else cols
+    nl = cols if contract == CONTRACT_ROWS else rows
+    if lines is not None:
+        ln = np.ascontiguousarray(np.asarray(lines, dtype=np.int64))
+        count, lp = ln.size, _ptr(ln)
+    else:
+        ln, count, lp = None, nl, None
+    codes = np.zeros((count, L // 2), dtype=np.uint8)
+    scales = np.zeros((count, L // 16), dtype=np.uint8)
+    amax, senc = ctypes.c_float(0), ctypes.c_float(0)
+    rc = lib().oracle_quantize_nvfp4(_ptr(src), rows, cols, contract, rot, rot_block, seed, lp,
+                                     count if ln is not None else 0, int(precise), _ptr(codes),
+                                     _ptr(scales), ctypes.addressof(amax), ctypes.addressof(senc))
+    if rc != 0:
+        raise ValueError("oracle_quantize_nvfp4 rejected its arguments")
+    return codes, scales, float(amax.value), float(senc.value)
+
+
 def _k_of(codes: np.ndarray, fmt: int) -> int:
     return codes.shape[1] * (1 if fmt == FMT_MXFP8 else 2)
 
 
-def dequantize(codes: np.ndarray, scales: np.ndarray, fmt: int = FMT_MXFP4) -> np.ndarray:
+def dequantize(codes: np.ndarray, scales: np.ndarray, fmt: int = FMT_MXFP4,
+               s_enc: float = 1.0) -> np.ndarray:
     c = np.ascontiguousarray(codes, dtype=np.uint8)
     s = np.ascontiguousarray(scales, dtype=np.uint8)
     mn, k = c.shape[0], _k_of(c, fmt)
     out = np.zeros((mn, k), dtype=np.float64)
-    lib().oracle_dequantize_fmt(fmt, _ptr(c), _ptr(s), mn, k, _ptr(out))
+    lib().oracle_dequantize_fmt(fmt, _ptr(c), _ptr(s), mn, k, float(s_enc), _ptr(out))
     return out
 
 
-def gemm_entries(Aq, As, Bq, Bs, ii, jj, fmt: int = FMT_MXFP4):
+def gemm_entries(Aq, As, Bq, Bs, ii, jj, fmt: int = FMT_MXFP4, a_senc: float = 1.0,
+                 b_senc: float = 1.0):
     """C[i, j] and sum |a||b| for listed pairs (i, j); A, B contraction-major."""
     Aq, As, Bq, Bs = (np.ascontiguousarray(a, dtype=np.uint8) for a in (Aq, As, Bq, Bs))
     K = _k_of(Aq, fmt)
@@ -272,22 +315,24 @@ def gemm_entries(Aq, As, Bq, Bs, ii, jj, fmt: int = FMT_MXFP4):
     jj = np.ascontiguousarray(np.asarray(jj, dtype=np.int64))
     C = np.zeros(ii.size, dtype=np.float64)
     Ca = np.zeros(ii.size, dtype=np.float64)
-    lib().oracle_gemm_entries_fmt(fmt, _ptr(Aq), _ptr(As), _ptr(Bq), _ptr(Bs), K, _ptr(ii),
-                                  _ptr(jj), int(ii.size), _ptr(C), _ptr(Ca))
+    lib().oracle_gemm_entries_fmt(fmt, _ptr(Aq), _ptr(As), float(a_senc), _ptr(Bq), _ptr(Bs),
+                                  float(b_senc), K, _ptr(ii), _ptr(jj), int(ii.size), _ptr(C),
+                                  _ptr(Ca))
     return C, Ca
 
 
-def gemm_rows(Aq, As, Bq, Bs, m0: int = 0, m1: int | None = None, fmt: int = FMT_MXFP4):
+def gemm_rows(Aq, As, Bq, Bs, m0: int = 0, m1: int | None = None, fmt: int = FMT_MXFP4,
+              a_senc: float = 1.0, b_senc: float = 1.0):
     """Rows [m0, m1) of C = A B^T (double) and of sum |a||b|."""
     Aq, As, Bq, Bs = (np.ascontiguousarray(a, dtype=np.uint8) for a in (Aq, As, Bq, Bs))
     M, N, K = Aq.shape[0], Bq.shape[0], _k_of(Aq, fmt)
     m1 = M if m1 is None else m1
     C = np.zeros((m1 - m0, N), dtype=np.float64)
     Ca = np.zeros((m1 - m0, N), dtype=np.float64)
-    lib().oracle_gemm_rows_fmt(fmt, _ptr(Aq), _ptr(As), _ptr(Bq), _ptr(Bs), M, N, K, m0, m1,
-                               _ptr(C), _ptr(Ca))
+    lib().oracle_gemm_rows_fmt(fmt, _ptr(Aq), _ptr(As), float(a_senc), _ptr(Bq), _ptr(Bs),
+                               float(b_senc), M, N, K, m0, m1, _ptr(C), _ptr(Ca))
     return C, Ca
 
 
-def gemm(Aq, As, Bq, Bs, fmt: int = FMT_MXFP4):
-    return gemm_rows(Aq, As, Bq, Bs, 0, None, fmt)
+def gemm(Aq, As, Bq, Bs, fmt: int = FMT_MXFP4, a_senc: float = 1.0, b_senc: float = 1.0):
+    return gemm_rows(Aq, As, Bq, Bs, 0, None, fmt, a_senc, b_senc)

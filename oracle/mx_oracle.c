@@ -24,6 +24,7 @@
  */
 #include "mx_oracle.h"
 
+#include <float.h>
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
@@ -264,6 +265,28 @@ void oracle_e4m3_rne_vec(const float *v, int64_t n, uint8_t *out)
         out[i] = oracle_e4m3_rne(v[i]);
 }
 
+/* NVFP4 (E2M1 elements, blocks of 16, UE4M3 block scale, fp32 tensor
+ * scale): the tensor's encode scale maps its largest magnitude onto the
+ * largest value a block can hold, 448 (E4M3) * 6 (E2M1) = 2688. */
+float oracle_nvfp4_tensor_scale(float amax)
+{
+    if (!(amax > 0.0f) || !isfinite(amax))
+        return 1.0f;
+    float s = 2688.0f / amax;          /* fp32 division, rounded to nearest */
+    if (isinf(s))
+        s = FLT_MAX;
+    return s;
+}
+
+/* Block scale code: the block's decode scale amax/6 in the tensor's encoded
+ * units, rounded to nearest-even E4M3 (saturating at 448; always >= 0). */
+uint8_t oracle_nvfp4_block_scale(float block_amax, float s_enc)
+{
+    float t = block_amax / 6.0f;
+    float u = t * s_enc;
+    return oracle_e4m3_rne(u);
+}
+
 void oracle_scale_bytes(const float *amax, int64_t n, uint8_t *out)
 {
     for (int64_t i = 0; i < n; ++i)
@@ -403,10 +426,71 @@ static void encode_line_e4m3(const float *r, int64_t L, uint8_t *codes, uint8_t 
     }
 }
 
+/* NVFP4 line: blocks of 16; the block scale as above; each element x becomes
+ * the nearest-even E2M1 code of x * q with q = s_enc / sf (fp32, at most
+ * FLT_MAX), so that x ~ e2m1 * sf / s_enc.  A block holding Inf/NaN gets the
+ * E4M3 NaN code 0x7F and zero codes; a block whose scale rounds to zero gets
+ * zero codes. */
+static void encode_line_nvfp4(const float *r, int64_t L, float s_enc, uint8_t *codes,
+                              uint8_t *scales)
+{
+    for (int64_t b = 0; b < L / 16; ++b) {
+        const float *blk = r + b * 16;
+        float amax = 0.0f;
+        int nonfinite = 0;
+        for (int i = 0; i < 16; ++i) {
+            float a = fabsf(blk[i]);
+            if (!isfinite(a))
+                nonfinite = 1;
+            else if (a > amax)
+                amax = a;
+        }
+        uint8_t q[16];
+        memset(q, 0, sizeof q);
+        uint8_t sf = nonfinite ? (uint8_t)0x7F : oracle_nvfp4_block_scale(amax, s_enc);
+        scales[b] = sf;
+        if (!nonfinite && sf != 0) {
+            float m = s_enc / (float)oracle_e4m3_value(sf);
+            if (isinf(m))
+                m = FLT_MAX;
+            for (int i = 0; i < 16; ++i)
+                q[i] = oracle_e2m1_rne(blk[i] * m);
+        }
+        for (int i = 0; i < 8; ++i)
+            codes[b * 8 + i] = (uint8_t)((q[2 * i] & 0xFu) | ((q[2 * i + 1] & 0xFu) << 4));
+    }
+}
+
 static int quantize_impl(int fmt, const uint16_t *src, int64_t rows, int64_t cols,
                          int contract, int rot, int rot_block, int rnd, uint64_t seed,
                          uint64_t sr_tag, const int64_t *lines, int64_t nlines, int precise,
                          uint8_t *codes, uint8_t *scales);
+static int quantize_core(int fmt, const uint16_t *src, int64_t rows, int64_t cols,
+                         int contract, int rot, int rot_block, int rnd, uint64_t seed,
+                         uint64_t sr_tag, const int64_t *lines, int64_t nlines, int precise,
+                         float s_enc, uint8_t *codes, uint8_t *scales, float *amax_out);
+
+int oracle_quantize_nvfp4(const uint16_t *src, int64_t rows, int64_t cols, int contract,
+                          int rot, int rot_block, uint64_t seed, const int64_t *lines,
+                          int64_t nlines, int precise, uint8_t *codes, uint8_t *scales,
+                          float *tensor_amax, float *s_enc)
+{
+    /* Pass 1: the largest finite magnitude of the (rotated) tensor, over
+     * every line; pass 2: the requested lines, encoded with its scale. */
+    float amax = 0.0f;
+    int rc = quantize_core(ORACLE_FMT_NVFP4, src, rows, cols, contract, rot, rot_block,
+                           ORACLE_ROUND_RNE, seed, 0, NULL, 0, precise, 1.0f, NULL, NULL, &amax);
+    if (rc != 0)
+        return rc;
+    float se = oracle_nvfp4_tensor_scale(amax);
+    if (tensor_amax)
+        *tensor_amax = amax;
+    if (s_enc)
+        *s_enc = se;
+    return quantize_core(ORACLE_FMT_NVFP4, src, rows, cols, contract, rot, rot_block,
+                         ORACLE_ROUND_RNE, seed, 0, lines, nlines, precise, se, codes, scales,
+                         NULL);
+}
 
 int oracle_quantize(const uint16_t *src, int64_t rows, int64_t cols, int contract,
                     int rot, int rot_block, int rnd, uint64_t seed, uint64_t sr_tag,
@@ -430,7 +514,23 @@ static int quantize_impl(int fmt, const uint16_t *src, int64_t rows, int64_t col
                          uint64_t sr_tag, const int64_t *lines, int64_t nlines, int precise,
                          uint8_t *codes, uint8_t *scales)
 {
-    if (!src || !codes || !scales || rows <= 0 || cols <= 0)
+    if (!codes || !scales)
+        return -1;
+    return quantize_core(fmt, src, rows, cols, contract, rot, rot_block, rnd, seed, sr_tag,
+                         lines, nlines, precise, 1.0f, codes, scales, NULL);
+}
+
+/* Rotates every requested line and encodes it in format fmt; with amax_out
+ * set (and no outputs) it only records the largest finite magnitude of the
+ * rotated lines. */
+static int quantize_core(int fmt, const uint16_t *src, int64_t rows, int64_t cols,
+                         int contract, int rot, int rot_block, int rnd, uint64_t seed,
+                         uint64_t sr_tag, const int64_t *lines, int64_t nlines, int precise,
+                         float s_enc, uint8_t *codes, uint8_t *scales, float *amax_out)
+{
+    if (!src || rows <= 0 || cols <= 0)
+        return -1;
+    if (!amax_out && (!codes || !scales))
         return -1;
     if (contract != ORACLE_CONTRACT_ROWS && contract != ORACLE_CONTRACT_COLS)
         return -1;
@@ -465,7 +565,13 @@ static int quantize_impl(int fmt, const uint16_t *src, int64_t rows, int64_t col
             free(r);
             return -1;
         }
-        if (fmt == ORACLE_FMT_MXFP8)
+        if (amax_out) {
+            for (int64_t t = 0; t < L; ++t)
+                if (isfinite(r[t]) && fabsf(r[t]) > *amax_out)
+                    *amax_out = fabsf(r[t]);
+        } else if (fmt == ORACLE_FMT_NVFP4)
+            encode_line_nvfp4(r, L, s_enc, codes + k * (L / 2), scales + k * (L / 16));
+        else if (fmt == ORACLE_FMT_MXFP8)
             encode_line_e4m3(r, L, codes + k * L, scales + k * (L / 32));
         else
             encode_line(r, L, rnd, seed, sr_tag, (uint64_t)line, codes + k * (L / 2),
@@ -487,8 +593,14 @@ static int64_t code_row_bytes(int fmt, int64_t k)
 }
 
 static double decode(int fmt, const uint8_t *codes, const uint8_t *scales, int64_t row,
-                     int64_t k, int64_t t)
+                     int64_t k, int64_t t, double s_enc)
 {
+    if (fmt == ORACLE_FMT_NVFP4) {
+        uint8_t sf = scales[row * (k / 16) + t / 16];
+        uint8_t byte = codes[row * (k / 2) + t / 2];
+        uint8_t code = (t % 2 == 0) ? (uint8_t)(byte & 0xFu) : (uint8_t)(byte >> 4);
+        return oracle_e2m1_value(code) * oracle_e4m3_value(sf) / s_enc;
+    }
     uint8_t sb = scales[row * (k / 32) + t / 32];
     if (sb == 0xFF)
         return NAN;
@@ -504,28 +616,29 @@ static double decode(int fmt, const uint8_t *codes, const uint8_t *scales, int64
 }
 
 void oracle_dequantize_fmt(int fmt, const uint8_t *codes, const uint8_t *scales, int64_t mn,
-                           int64_t k, double *out)
+                           int64_t k, double s_enc, double *out)
 {
     for (int64_t i = 0; i < mn; ++i)
         for (int64_t t = 0; t < k; ++t)
-            out[i * k + t] = decode(fmt, codes, scales, i, k, t);
+            out[i * k + t] = decode(fmt, codes, scales, i, k, t, s_enc);
 }
 
 void oracle_dequantize(const uint8_t *codes, const uint8_t *scales, int64_t mn, int64_t k,
                        double *out)
 {
-    oracle_dequantize_fmt(ORACLE_FMT_MXFP4, codes, scales, mn, k, out);
+    oracle_dequantize_fmt(ORACLE_FMT_MXFP4, codes, scales, mn, k, 1.0, out);
 }
 
-void oracle_gemm_entries_fmt(int fmt, const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq,
-                             const uint8_t *Bs, int64_t K, const int64_t *ii, const int64_t *jj,
-                             int64_t n, double *C, double *Cabs)
+void oracle_gemm_entries_fmt(int fmt, const uint8_t *Aq, const uint8_t *As, double a_senc,
+                             const uint8_t *Bq, const uint8_t *Bs, double b_senc, int64_t K,
+                             const int64_t *ii, const int64_t *jj, int64_t n, double *C,
+                             double *Cabs)
 {
     for (int64_t p = 0; p < n; ++p) {
         double acc = 0.0, acc_abs = 0.0;
         for (int64_t t = 0; t < K; ++t) {
-            double a = decode(fmt, Aq, As, ii[p], K, t);
-            double b = decode(fmt, Bq, Bs, jj[p], K, t);
+            double a = decode(fmt, Aq, As, ii[p], K, t, a_senc);
+            double b = decode(fmt, Bq, Bs, jj[p], K, t, b_senc);
             acc += a * b;
             acc_abs += fabs(a) * fabs(b);
         }
@@ -538,19 +651,21 @@ void oracle_gemm_entries(const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq
                          const uint8_t *Bs, int64_t K, const int64_t *ii, const int64_t *jj,
                          int64_t n, double *C, double *Cabs)
 {
-    oracle_gemm_entries_fmt(ORACLE_FMT_MXFP4, Aq, As, Bq, Bs, K, ii, jj, n, C, Cabs);
+    oracle_gemm_entries_fmt(ORACLE_FMT_MXFP4, Aq, As, 1.0, Bq, Bs, 1.0, K, ii, jj, n, C, Cabs);
 }
 
-void oracle_gemm_rows_fmt(int fmt, const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq,
-                          const uint8_t *Bs, int64_t M, int64_t N, int64_t K, int64_t m0,
-                          int64_t m1, double *C, double *Cabs)
+void oracle_gemm_rows_fmt(int fmt, const uint8_t *Aq, const uint8_t *As, double a_senc,
+                          const uint8_t *Bq, const uint8_t *Bs, double b_senc, int64_t M,
+                          int64_t N, int64_t K, int64_t m0, int64_t m1, double *C, double *Cabs)
 {
     (void)M;
     double *a = (double *)malloc(sizeof(double) * (size_t)K);
     double *b = (double *)malloc(sizeof(double) * (size_t)N * (size_t)K);
-    oracle_dequantize_fmt(fmt, Bq, Bs, N, K, b);
+    const int64_t block = fmt == ORACLE_FMT_NVFP4 ? 16 : 32;
+    oracle_dequantize_fmt(fmt, Bq, Bs, N, K, b_senc, b);
     for (int64_t i = m0; i < m1; ++i) {
-        oracle_dequantize_fmt(fmt, Aq + i * code_row_bytes(fmt, K), As + i * (K / 32), 1, K, a);
+        oracle_dequantize_fmt(fmt, Aq + i * code_row_bytes(fmt, K), As + i * (K / block), 1, K,
+                              a_senc, a);
         for (int64_t j = 0; j < N; ++j) {
             const double *bj = b + j * K;
             double acc = 0.0, acc_abs = 0.0;
@@ -570,5 +685,5 @@ void oracle_gemm_rows(const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq,
                       const uint8_t *Bs, int64_t M, int64_t N, int64_t K, int64_t m0,
                       int64_t m1, double *C, double *Cabs)
 {
-    oracle_gemm_rows_fmt(ORACLE_FMT_MXFP4, Aq, As, Bq, Bs, M, N, K, m0, m1, C, Cabs);
+    oracle_gemm_rows_fmt(ORACLE_FMT_MXFP4, Aq, As, 1.0, Bq, Bs, 1.0, M, N, K, m0, m1, C, Cabs);
 }

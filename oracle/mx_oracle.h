@@ -74,7 +74,7 @@ void oracle_e2m1_rne_vec(const float *v, int64_t n, uint8_t *out);
 void oracle_e2m1_sr_vec(const float *v, const uint32_t *u24, int64_t n, uint8_t *out);
 
 /* Rotation mode / rounding mode / contraction direction. */
-enum { ORACLE_FMT_MXFP4 = 0, ORACLE_FMT_MXFP8 = 1 };
+enum { ORACLE_FMT_MXFP4 = 0, ORACLE_FMT_MXFP8 = 1, ORACLE_FMT_NVFP4 = 2 };
 enum { ORACLE_ROT_NONE = 0, ORACLE_ROT_HADAMARD_DET = 1, ORACLE_ROT_HADAMARD_RAND = 2 };
 enum { ORACLE_ROUND_RNE = 0, ORACLE_ROUND_SR = 1 };
 enum { ORACLE_CONTRACT_ROWS = 0, ORACLE_CONTRACT_COLS = 1 };
@@ -122,17 +122,43 @@ int oracle_quantize_mxfp8(const uint16_t *src, int64_t rows, int64_t cols, int c
                           int rot, int rot_block, uint64_t seed, const int64_t *lines,
                           int64_t nlines, int precise, uint8_t *codes, uint8_t *scales);
 
+/* NVFP4 (the prior-work format named in [36kr]'s introduction; NVIDIA's
+ * definition): E2M1 elements in blocks of 16 along the contraction, one
+ * UE4M3 scale per block and one fp32 encode scale per tensor.
+ *   tensor scale  s_enc = 2688 / amax (fp32; 448 * 6, the largest block
+ *                 value), FLT_MAX if that overflows, 1 if amax is 0;
+ *   block scale   sf = E4M3 nearest-even of fl(fl(block_amax / 6) * s_enc);
+ *   element       E2M1 nearest-even of fl(x * fl(s_enc / sf)) (the factor at
+ *                 most FLT_MAX); decoded value e2m1 * sf / s_enc.
+ * A block with Inf/NaN gets sf = 0x7F (NaN) and zero codes; sf = 0 gives
+ * zero codes. */
+float oracle_nvfp4_tensor_scale(float amax);
+uint8_t oracle_nvfp4_block_scale(float block_amax, float s_enc);
+
+/* NVFP4-encode a bf16 matrix (rotation and line selection as in
+ * oracle_quantize): the tensor amax is taken over every (rotated) line, then
+ * the requested lines are encoded.  codes [line][L/2] (two per byte, as
+ * MXFP4), scales canonical [line][L/16]; the tensor amax and s_enc are
+ * returned through the two pointers (either may be NULL). */
+int oracle_quantize_nvfp4(const uint16_t *src, int64_t rows, int64_t cols, int contract,
+                          int rot, int rot_block, uint64_t seed, const int64_t *lines,
+                          int64_t nlines, int precise, uint8_t *codes, uint8_t *scales,
+                          float *tensor_amax, float *s_enc);
+
 /* Decode, the contraction over listed entries and over a row range, for
- * either format (fmt = ORACLE_FMT_*): codes are [mn][k/2] for MXFP4 and
- * [mn][k] for MXFP8; canonical scales [mn][k/32]. */
+ * every format (fmt = ORACLE_FMT_*): codes are [mn][k/2] for MXFP4 and
+ * NVFP4, [mn][k] for MXFP8; canonical scales [mn][k/32] (MX) or [mn][k/16]
+ * (NVFP4).  s_enc / a_senc / b_senc: the NVFP4 tensor scales (ignored for
+ * the MX formats). */
 void oracle_dequantize_fmt(int fmt, const uint8_t *codes, const uint8_t *scales, int64_t mn,
-                           int64_t k, double *out);
-void oracle_gemm_entries_fmt(int fmt, const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq,
-                             const uint8_t *Bs, int64_t K, const int64_t *ii, const int64_t *jj,
-                             int64_t n, double *C, double *Cabs);
-void oracle_gemm_rows_fmt(int fmt, const uint8_t *Aq, const uint8_t *As, const uint8_t *Bq,
-                          const uint8_t *Bs, int64_t M, int64_t N, int64_t K, int64_t m0,
-                          int64_t m1, double *C, double *Cabs);
+                           int64_t k, double s_enc, double *out);
+void oracle_gemm_entries_fmt(int fmt, const uint8_t *Aq, const uint8_t *As, double a_senc,
+                             const uint8_t *Bq, const uint8_t *Bs, double b_senc, int64_t K,
+                             const int64_t *ii, const int64_t *jj, int64_t n, double *C,
+                             double *Cabs);
+void oracle_gemm_rows_fmt(int fmt, const uint8_t *Aq, const uint8_t *As, double a_senc,
+                          const uint8_t *Bq, const uint8_t *Bs, double b_senc, int64_t M,
+                          int64_t N, int64_t K, int64_t m0, int64_t m1, double *C, double *Cabs);
 
 /* Decode codes[mn][k/2] + canonical scales[mn][k/32] into double out[mn][k]. */
 void oracle_dequantize(const uint8_t *codes, const uint8_t *scales, int64_t mn, int64_t k,
