@@ -454,15 +454,19 @@ def run_mine(args, world, rank, local):
     if rank == 0 and not args.no_extras:
         fused_side = measure_fused(L, mx, dY, X, dW, T, N, K, flush, stream, dev, step_ms,
                                    fp4_meas)
-    fp8_side = None
+    fp8_side = nv_side = None
+    peaks_var = None
     if rank == 0 and not args.no_extras:
-        fp8_meas = measure_fp8_peak(mx)
-        fp8_side = measure_mxfp8(L, mx, dY, X, T, N, K, flush, stream, dev, fp8_meas,
-                                 sorted(step_ms)[len(step_ms) // 2])
+        peaks_var = {"mxfp8": measure_mma_peak(mx, 5), "nvfp4": measure_mma_peak(mx, 2)}
+        med = sorted(step_ms)[len(step_ms) // 2]
+        fp8_side = measure_variant(L, mx, "mxfp8", dY, X, T, N, K, flush, stream, dev,
+                                   peaks_var["mxfp8"], med)
+        nv_side = measure_variant(L, mx, "nvfp4", dY, X, T, N, K, flush, stream, dev,
+                                  peaks_var["nvfp4"], med)
     side = None
     if rank == 0 and not args.no_extras and args.workload != "o_proj":
         side = measure_side_workload(L, mx, "o_proj", dev, stream, flush, min(n, 300),
-                                     args.warmup, fp4_meas, fp8_meas)
+                                     args.warmup, fp4_meas, peaks_var)
 
     # parity spot check of the timed output (oracle entries, rank 0 only)
     parity = None
@@ -530,6 +534,7 @@ def run_mine(args, world, rank, local):
             "step_launches": 2,
             "fused_wgrad": fused_side,
             "fp8_comparator": fp8_side,
+            "nvfp4_variant": nv_side,
             "fp4_peak_fraction": value / fp4_peak,
             "fp4_peak_measured": fp4_meas,
             "fp4_measured_fraction": value / fp4_meas["tflops"],
@@ -575,7 +580,7 @@ def measure_fp4_peak(mx, reps=3):
 
 
 def measure_side_workload(L, mx, name, dev, stream, flush, steps, warmup, fp4_meas,
-                          fp8_meas=None):
+                          peaks_var=None):
     """Quantise-pair + GEMM of another Wgrad shape, timed like the headline
     (L2 flushed before every step, CUDA events on the launching stream)."""
     import numpy as np
@@ -637,12 +642,15 @@ def measure_side_workload(L, mx, name, dev, stream, flush, steps, warmup, fp4_me
     flops = 2.0 * N * K * T
     hbm = load_peaks()[0]["hbm_gbs"]
     qbytes = (N + K) * T * (2 + 0.5 + 1 / 32)
-    fp8 = None
-    if fp8_meas is not None:
-        fp8 = measure_mxfp8(L, mx, dY, X, T, N, K, flush, stream, dev, fp8_meas, t_step)
+    fp8 = nv = None
+    if peaks_var is not None:
+        fp8 = measure_variant(L, mx, "mxfp8", dY, X, T, N, K, flush, stream, dev,
+                              peaks_var["mxfp8"], t_step)
+        nv = measure_variant(L, mx, "nvfp4", dY, X, T, N, K, flush, stream, dev,
+                             peaks_var["nvfp4"], t_step)
     return {"workload": f"{name} Wgrad: dY [{T},{N}] x X [{T},{K}] -> dW [{N},{K}] fp32, "
                         f"{mode_text()}",
-            "fp8_comparator": fp8,
+            "fp8_comparator": fp8, "nvfp4_variant": nv,
             "steps": steps, "ms_per_step": t_step,
             "value": flops / (t_step * 1e-3) / 1e12, "unit": "TFLOP/s",
             "step_launches": 2,
@@ -693,43 +701,58 @@ def measure_fused(L, mx, dY, X, dW, T, N, K, flush, stream, dev, step_ms, fp4_me
             "bitwise_equal_to_two_launch_step": same}
 
 
-def measure_fp8_peak(mx, reps=3):
-    """All-SM issue rate of the MXFP8 comparator GEMM's instruction,
-    tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X (M=256,
-    N=256, K=32), operands in shared memory; best of `reps`."""
+def measure_mma_peak(mx, kind, reps=3):
+    """All-SM issue rate of a variant GEMM's instruction (mx_bench_mma, pair
+    form, M=256 N=256, operands in shared memory); best of `reps`.  kind 5:
+    kind::mxf8f6f4 scale_vec::1X (MXFP8, K=32); kind 2: kind::mxf4nvf4
+    scale_vec::4X (NVFP4, K=64)."""
     best = None
     for _ in range(reps):
-        r = mx.bench_mma(kind=5, cta_group=2, n=256, mmas_per_iter=4, iters=20000)
+        r = mx.bench_mma(kind=kind, cta_group=2, n=256, mmas_per_iter=4, iters=20000)
         if best is None or r["tflops"] > best["tflops"]:
             best = r
+    name = {5: "kind::mxf8f6f4.block_scale.scale_vec::1X M=256 N=256 K=32",
+            2: "kind::mxf4nvf4.block_scale.scale_vec::4X M=256 N=256 K=64"}[kind]
     return {"tflops": best["tflops"], "ns_per_mma": best["ns_per_mma"],
-            "instruction": "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X "
-                           "M=256 N=256 K=32", "call": "mx_bench_mma", "best_of": reps}
+            "instruction": "tcgen05.mma.cta_group::2." + name, "call": "mx_bench_mma",
+            "best_of": reps}
 
 
-def measure_mxfp8(L, mx, dY, X, T, N, K, flush, stream, dev, fp8_meas, mxfp4_step_ms,
-                  reps=50):
-    """The FP8 comparator on the same Wgrad shape: mx_linear_wgrad_mxfp8
-    (MXFP8 encode of both operands + the MXFP8 GEMM, no rotation), and its
-    GEMM launch alone; medians over `reps` calls, L2 flushed before each."""
+def measure_variant(L, mx, fmt, dY, X, T, N, K, flush, stream, dev, peak, mxfp4_step_ms,
+                    reps=50):
+    """Another element format on the same Wgrad shape, through its public
+    call: "mxfp8" (the FP8 comparator: MXFP8 encode of both operands + the
+    MXFP8 GEMM, no rotation) or "nvfp4" (the NVFP4 variant: tensor-amax and
+    encode launches + the NVFP4 GEMM, deterministic Hadamard 16), and its GEMM
+    launch alone; medians over `reps` calls, L2 flushed before each."""
     import torch
     sp = stream.cuda_stream
     ptr = lambda t: t.data_ptr()
-    ws = torch.empty(mx.linear_wgrad_mxfp8_workspace_bytes(T, N, K), dtype=torch.uint8,
-                     device=dev)
+    nv = fmt == "nvfp4"
+    wsb = (mx.linear_wgrad_nvfp4_workspace_bytes(T, N, K) if nv
+           else mx.linear_wgrad_mxfp8_workspace_bytes(T, N, K))
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
     out = torch.empty((N, K), dtype=torch.float32, device=dev)
-    n_code = mx.mxfp8_codes_bytes(N, T)
     align = lambda x: (x + 255) // 256 * 256
-    aq = ws[0:]
-    as_ = ws[align(n_code):]
-    bq = ws[align(n_code) + align(mx.scales_bytes(N, T)):]
-    bs = ws[align(n_code) + align(mx.scales_bytes(N, T)) + align(mx.mxfp8_codes_bytes(K, T)):]
+    codes = mx.codes_bytes if nv else mx.mxfp8_codes_bytes
+    scales = mx.nvfp4_scales_bytes if nv else mx.scales_bytes
+    o_as = align(codes(N, T))
+    o_bq = o_as + align(scales(N, T))
+    o_bs = o_bq + align(codes(K, T))
+    o_am = o_bs + align(scales(K, T))
+    base = ws.data_ptr()
 
     def step():
-        return L.mx_linear_wgrad_mxfp8(ptr(dY), ptr(X), ptr(out), T, N, K, ptr(ws), ws.numel(), sp)
+        if nv:
+            return L.mx_linear_wgrad_nvfp4(ptr(dY), ptr(X), ptr(out), T, N, K,
+                                           mx.ROT_HADAMARD_DET, 16, 0, base, ws.numel(), sp)
+        return L.mx_linear_wgrad_mxfp8(ptr(dY), ptr(X), ptr(out), T, N, K, base, ws.numel(), sp)
 
     def gemm():
-        return L.mx_gemm_mxfp8(ptr(aq), ptr(as_), ptr(bq), ptr(bs), ptr(out), N, K, T, sp)
+        if nv:
+            return L.mx_gemm_nvfp4(base, base + o_as, base + o_am, base + o_bq, base + o_bs,
+                                   base + o_am + 4, ptr(out), N, K, T, sp)
+        return L.mx_gemm_mxfp8(base, base + o_as, base + o_bq, base + o_bs, ptr(out), N, K, T, sp)
 
     def timed(fn):
         for _ in range(3):
@@ -751,13 +774,17 @@ def measure_mxfp8(L, mx, dY, X, T, N, K, flush, stream, dev, fp8_meas, mxfp4_ste
     t_gemm = timed(gemm)             # on the operands the last step left in the workspace
     mx.check_status()
     flops = 2.0 * N * K * T
-    return {"call": "mx_linear_wgrad_mxfp8", "format": "MXFP8: E4M3 elements, E8M0 scale per "
-            "32 along T, no rotation, round to nearest even",
+    return {"call": "mx_linear_wgrad_nvfp4" if nv else "mx_linear_wgrad_mxfp8",
+            "format": ("NVFP4: E2M1 in blocks of 16 along T, UE4M3 block scale, fp32 tensor "
+                       "scale, deterministic Hadamard 16, round to nearest even") if nv else
+                      ("MXFP8: E4M3 elements, E8M0 scale per 32 along T, no rotation, round "
+                       "to nearest even"),
             "ms_per_step": t_step, "tflops": flops / (t_step * 1e-3) / 1e12,
             "gemm_ms": t_gemm, "gemm_tflops": flops / (t_gemm * 1e-3) / 1e12,
-            "fp8_peak_measured": fp8_meas,
-            "gemm_frac_fp8_measured": flops / (t_gemm * 1e-3) / 1e12 / fp8_meas["tflops"],
-            "mxfp4_step_speedup": t_step / mxfp4_step_ms, "median_of": reps, "step_launches": 2}
+            "peak_measured": peak,
+            "gemm_frac_peak_measured": flops / (t_gemm * 1e-3) / 1e12 / peak["tflops"],
+            "mxfp4_step_speedup": t_step / mxfp4_step_ms, "median_of": reps,
+            "step_launches": 3 if nv else 2}
 
 
 def measure_dual(L, mx, dY, T, N, flush, stream, dev, hbm_gbs, reps=30):

@@ -54,7 +54,7 @@ typedef enum {
     MX_ERR_WORKSPACE = 4,   /* workspace smaller than mx_linear_workspace_bytes() */
     MX_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed */
     MX_ERR_TIMEOUT = 6,     /* a device-side bounded wait expired (see mx_check_status) */
-    MX_ERR_UNSUPPORTED = 7, /* the current device is not sm_103 / sm_100 family */
+    MX_ERR_UNSUPPORTED = 7, /* not an sm_103 device, or arguments the call does not cover */
     MX_ERR_BOUNDS = 8       /* bounds-checked build only (MX_CHECKED=1): a kernel store fell
                                outside its buffer and was skipped (see mx_check_status) */
 } mx_status;
@@ -258,6 +258,48 @@ mx_status mx_gemm_mxfp8(const void *d_Aq, const void *d_As, const void *d_Bq, co
 size_t mx_linear_wgrad_mxfp8_workspace_bytes(int64_t T, int64_t N, int64_t K);
 mx_status mx_linear_wgrad_mxfp8(const void *d_dY, const void *d_X, float *d_dW, int64_t T,
                                 int64_t N, int64_t K, void *d_ws, size_t ws_bytes, void *stream);
+
+/*
+ * NVFP4 variant -- NVFP4 is named as prior work in "Neue Studie von AMD ..."
+ * (eu.36kr.com), introduction; its definition here is NVIDIA's published
+ * format: E2M1 elements in blocks of 16 along the contraction dimension, one
+ * UE4M3 scale per block and one fp32 encode scale per tensor.
+ *   tensor:  amax = largest finite |x| of the (rotated) operand;
+ *            s_enc = 2688 / amax (448 * 6, the largest block value), FLT_MAX
+ *            if that overflows, 1 if amax == 0;
+ *   block:   sf = E4M3 nearest-even of fl(fl(block_amax / 6) * s_enc),
+ *            saturating at 448 (0x7F: a block holding Inf/NaN; its codes 0);
+ *   element: E2M1 nearest-even of fl(x * min(fl(s_enc / sf), FLT_MAX))
+ *            (sf == 0: code 0); it stands for e2m1 * sf / s_enc.
+ * The same rotations as MXFP4 with Hadamard blocks of 16 or 32 (others:
+ * MX_ERR_UNSUPPORTED); round to nearest only.
+ *
+ * Layouts: codes as MXFP4 ([lines][k/2], mx_codes_bytes); scales in their
+ * own tiled layout of mx_nvfp4_scales_bytes(lines, k) bytes: byte (line r,
+ * block b of 16) at ((r/128)*(KB/4) + b/4)*512 + (r%32)*16 + ((r%128)/32)*4
+ * + b%4 with KB = 16*ceil(k/256) blocks per line (padding blocks 0).
+ *
+ * mx_quantize_nvfp4: contraction down the rows of src[rows][cols]; two
+ *   launches (the tensor amax, then the encode); *d_amax (device float,
+ *   8-byte aligned) receives the tensor amax, which mx_gemm_nvfp4 takes.
+ * mx_gemm_nvfp4: C[M][N] = (sum over K of decoded a * b), i.e. the
+ *   block-scaled product divided by s_enc(amax_a) * s_enc(amax_b) in the
+ *   epilogue; K % 32 == 0, N % 4 == 0.
+ * mx_linear_wgrad_nvfp4: dW[N][K] = dY^T X with both operands NVFP4-encoded
+ *   along T (three launches and a memset of the two amax words), workspace of
+ *   mx_linear_wgrad_nvfp4_workspace_bytes(T, N, K) bytes, 256-byte aligned.
+ */
+size_t mx_nvfp4_scales_bytes(int64_t mn, int64_t k);
+mx_status mx_quantize_nvfp4(const void *d_src, int64_t rows, int64_t cols, int rot, int rot_block,
+                            uint64_t seed, void *d_codes, void *d_scales, float *d_amax,
+                            void *stream);
+mx_status mx_gemm_nvfp4(const void *d_Aq, const void *d_As, const float *d_amax_a,
+                        const void *d_Bq, const void *d_Bs, const float *d_amax_b, float *d_C,
+                        int64_t M, int64_t N, int64_t K, void *stream);
+size_t mx_linear_wgrad_nvfp4_workspace_bytes(int64_t T, int64_t N, int64_t K);
+mx_status mx_linear_wgrad_nvfp4(const void *d_dY, const void *d_X, float *d_dW, int64_t T,
+                                int64_t N, int64_t K, int rot, int rot_block, uint64_t seed,
+                                void *d_ws, size_t ws_bytes, void *stream);
 
 /* mx_linear_fprop -- Y[T][N] = X W^T, contraction K (K % 32 == 0, N % 4 == 0). */
 mx_status mx_linear_fprop(const void *d_X, const void *d_W, float *d_Y, int64_t T, int64_t N,

@@ -14,7 +14,9 @@ from ._binding import (CONTRACT_COLS, CONTRACT_ROWS, OP_DGRAD, OP_FPROP, OP_WGRA
                        linear_workspace_bytes, NOALLOC_SCRATCH_BYTES, quantize, quantize_dual,
                        quantize_pair, quantize_into, scales_bytes, scales_to_canonical,
                        status_string, mxfp8_codes_bytes, quantize_mxfp8, gemm_mxfp8,
-                       gemm_mxfp8_into, linear_wgrad_mxfp8, linear_wgrad_mxfp8_workspace_bytes)
+                       gemm_mxfp8_into, linear_wgrad_mxfp8, linear_wgrad_mxfp8_workspace_bytes,
+                       nvfp4_scales_bytes, quantize_nvfp4, gemm_nvfp4, linear_wgrad_nvfp4,
+                       linear_wgrad_nvfp4_workspace_bytes)
 
 __all__ = [
     "CONTRACT_COLS", "CONTRACT_ROWS", "OP_DGRAD", "OP_FPROP", "OP_WGRAD", "ROT_HADAMARD_DET",
@@ -25,5 +27,6 @@ __all__ = [
     "NOALLOC_SCRATCH_BYTES", "quantize", "quantize_dual", "quantize_pair",
     "quantize_into", "scales_bytes", "scales_to_canonical", "status_string",
     "mxfp8_codes_bytes", "quantize_mxfp8", "gemm_mxfp8", "gemm_mxfp8_into", "linear_wgrad_mxfp8",
-    "linear_wgrad_mxfp8_workspace_bytes",
+    "linear_wgrad_mxfp8_workspace_bytes", "nvfp4_scales_bytes", "quantize_nvfp4", "gemm_nvfp4",
+    "linear_wgrad_nvfp4", "linear_wgrad_nvfp4_workspace_bytes",
 ]

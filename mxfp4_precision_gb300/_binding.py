@@ -27,6 +27,8 @@ EXPORTED = [
     "mx_linear_wgrad_fused", "mx_linear_wgrad_fused_supported",
     "mx_mxfp8_codes_bytes", "mx_quantize_mxfp8", "mx_gemm_mxfp8",
     "mx_linear_wgrad_mxfp8_workspace_bytes", "mx_linear_wgrad_mxfp8",
+    "mx_nvfp4_scales_bytes", "mx_quantize_nvfp4", "mx_gemm_nvfp4",
+    "mx_linear_wgrad_nvfp4_workspace_bytes", "mx_linear_wgrad_nvfp4",
     "mx_check_status",
     "mx_debug_timeout_probe", "mx_bench_mma", "mx_status_string", "mx_version",
 ]
@@ -94,6 +96,16 @@ def lib() -> ctypes.CDLL:
             L.mx_linear_wgrad_mxfp8_workspace_bytes.restype = sz
             L.mx_linear_wgrad_mxfp8.argtypes = [P, P, P, i64, i64, i64, P, sz, P]
             L.mx_linear_wgrad_mxfp8.restype = i32
+            L.mx_nvfp4_scales_bytes.argtypes = [i64, i64]
+            L.mx_nvfp4_scales_bytes.restype = sz
+            L.mx_quantize_nvfp4.argtypes = [P, i64, i64, i32, i32, u64, P, P, P, P]
+            L.mx_quantize_nvfp4.restype = i32
+            L.mx_gemm_nvfp4.argtypes = [P, P, P, P, P, P, P, i64, i64, i64, P]
+            L.mx_gemm_nvfp4.restype = i32
+            L.mx_linear_wgrad_nvfp4_workspace_bytes.argtypes = [i64, i64, i64]
+            L.mx_linear_wgrad_nvfp4_workspace_bytes.restype = sz
+            L.mx_linear_wgrad_nvfp4.argtypes = [P, P, P, i64, i64, i64, i32, i32, u64, P, sz, P]
+            L.mx_linear_wgrad_nvfp4.restype = i32
             L.mx_check_status.argtypes = [P]
             L.mx_check_status.restype = i32
             L.mx_debug_timeout_probe.argtypes = [i64, P]
@@ -290,6 +302,60 @@ def gemm_mxfp8(Aq, As, Bq, Bs, M: int, N: int, K: int, stream=None) -> torch.Ten
 
 def linear_wgrad_mxfp8_workspace_bytes(T: int, N: int, K: int) -> int:
     return int(lib().mx_linear_wgrad_mxfp8_workspace_bytes(T, N, K))
+
+
+# --------------------------------------------------------------------------- NVFP4 variant
+def nvfp4_scales_bytes(mn: int, k: int) -> int:
+    return int(lib().mx_nvfp4_scales_bytes(mn, k))
+
+
+def quantize_nvfp4(src: torch.Tensor, rot: int = ROT_NONE, rot_block: int = 16, seed: int = 0,
+                   stream=None):
+    """NVFP4 encode down the rows of src [rows, cols] (bf16): returns (codes
+    uint8 [cols, rows/2], scales uint8 [mx_nvfp4_scales_bytes], tiled, tensor
+    amax as a one-element float32 device tensor)."""
+    src = _as_bf16_bits(src)
+    rows, cols = src.shape
+    d = src.device
+    codes = torch.empty((cols, rows // 2), dtype=torch.uint8, device=d)
+    scales = torch.empty((max(1, nvfp4_scales_bytes(cols, rows)),), dtype=torch.uint8, device=d)
+    amax = torch.empty((2,), dtype=torch.float32, device=d)
+    st = lib().mx_quantize_nvfp4(_dev_ptr(src, "src"), rows, cols, rot, rot_block, seed,
+                                 _dev_ptr(codes, "codes"), _dev_ptr(scales, "scales"),
+                                 _dev_ptr(amax, "amax"), _stream(stream))
+    _check(st, "mx_quantize_nvfp4")
+    return codes, scales, amax[:1]
+
+
+def gemm_nvfp4(Aq, As, amax_a, Bq, Bs, amax_b, M: int, N: int, K: int, stream=None):
+    C = torch.empty((M, N), dtype=torch.float32, device=Aq.device)
+    st = lib().mx_gemm_nvfp4(_dev_ptr(Aq, "Aq"), _dev_ptr(As, "As"), _dev_ptr(amax_a, "amax_a"),
+                             _dev_ptr(Bq, "Bq"), _dev_ptr(Bs, "Bs"), _dev_ptr(amax_b, "amax_b"),
+                             _dev_ptr(C, "C"), M, N, K, _stream(stream))
+    _check(st, "mx_gemm_nvfp4")
+    return C
+
+
+def linear_wgrad_nvfp4_workspace_bytes(T: int, N: int, K: int) -> int:
+    return int(lib().mx_linear_wgrad_nvfp4_workspace_bytes(T, N, K))
+
+
+def linear_wgrad_nvfp4(dY, X, rot=ROT_NONE, rot_block=16, seed=0, ws=None, out=None,
+                       stream=None) -> torch.Tensor:
+    """dW[N, K] = dY^T X with both operands NVFP4-encoded along T; fp32 output."""
+    dY, X = _as_bf16_bits(dY), _as_bf16_bits(X)
+    T, N = dY.shape
+    K = X.shape[1]
+    if ws is None:
+        need = linear_wgrad_nvfp4_workspace_bytes(T, N, K)
+        ws = torch.empty((max(need, 256),), dtype=torch.uint8, device=dY.device)
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.float32, device=dY.device)
+    st = lib().mx_linear_wgrad_nvfp4(_dev_ptr(dY, "dY"), _dev_ptr(X, "X"), _dev_ptr(out, "out"),
+                                     T, N, K, rot, rot_block, seed, _dev_ptr(ws, "workspace"),
+                                     ws.numel() * ws.element_size(), _stream(stream))
+    _check(st, "mx_linear_wgrad_nvfp4")
+    return out
 
 
 def linear_wgrad_mxfp8(dY, X, ws=None, out=None, stream=None) -> torch.Tensor:

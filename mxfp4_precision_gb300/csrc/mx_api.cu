@@ -259,7 +259,48 @@ mx_status gemm_mxfp8_impl(const void *Aq, const void *As, const void *Bq, const 
         return from_cuda(cudaMemsetAsync(C, 0, static_cast<size_t>(M) * N * sizeof(float), stream));
     const DeviceInfo *dev = nullptr;
     if ((st = device_or_error(&dev)) != MX_OK) return st;
-    return from_cuda(launch_gemm_fmt(true, Aq, As, Bq, Bs, C, M, N, K, *dev, stream));
+    return from_cuda(launch_gemm_fmt(kGemmMXFP8, Aq, As, Bq, Bs, C, M, N, K, nullptr, nullptr,
+                                     *dev, stream));
+}
+
+// NVFP4 variant: encode down the rows of one or two operands (two launches:
+// tensor amax, then the encode), contract with the tensor scales.
+mx_status quantize_nvfp4_impl(const void *src0, int64_t rows0, int64_t cols0, const void *src1,
+                              int64_t rows1, int64_t cols1, int rot, int rot_block, uint64_t seed,
+                              void *codes0, void *scales0, void *codes1, void *scales1,
+                              float *amax, cudaStream_t stream) {
+    mx_status st = check_encode(src0, rows0, cols0, MX_CONTRACT_ROWS, rot, rot_block,
+                                MX_ROUND_RNE, codes0, scales0);
+    if (st != MX_OK) return st;
+    if (rot != MX_ROT_NONE && rot_block != 16 && rot_block != 32) return MX_ERR_UNSUPPORTED;
+    if (src1 != nullptr) {
+        st = check_encode(src1, rows1, cols1, MX_CONTRACT_ROWS, rot, rot_block, MX_ROUND_RNE,
+                          codes1, scales1);
+        if (st != MX_OK) return st;
+        if (rows1 == 0 || cols1 == 0) return MX_ERR_SHAPE;
+    }
+    if (rows0 == 0 || cols0 == 0) return src1 == nullptr ? MX_OK : MX_ERR_SHAPE;
+    if (amax == nullptr) return MX_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(amax) & 7u) != 0) return MX_ERR_ALIGN;
+    const DeviceInfo *dev = nullptr;
+    if ((st = device_or_error(&dev)) != MX_OK) return st;
+    return from_cuda(launch_quantize_nvfp4_colwise(src0, rows0, cols0, src1, rows1, cols1, rot,
+                                                   rot_block, seed, codes0, scales0, codes1,
+                                                   scales1, amax, *dev, stream));
+}
+
+mx_status gemm_nvfp4_impl(const void *Aq, const void *As, const float *amax_a, const void *Bq,
+                          const void *Bs, const float *amax_b, float *C, int64_t M, int64_t N,
+                          int64_t K, cudaStream_t stream) {
+    mx_status st = check_gemm(Aq, As, Bq, Bs, C, M, N, K);
+    if (st != MX_OK || M == 0 || N == 0) return st;
+    if (K == 0)
+        return from_cuda(cudaMemsetAsync(C, 0, static_cast<size_t>(M) * N * sizeof(float), stream));
+    if (amax_a == nullptr || amax_b == nullptr) return MX_ERR_INVALID_ARG;
+    const DeviceInfo *dev = nullptr;
+    if ((st = device_or_error(&dev)) != MX_OK) return st;
+    return from_cuda(launch_gemm_fmt(kGemmNVFP4, Aq, As, Bq, Bs, C, M, N, K, amax_a, amax_b,
+                                     *dev, stream));
 }
 
 // Quantise both operands of a linear op into the workspace, then contract.
@@ -477,6 +518,68 @@ mx_status mx_linear_wgrad_mxfp8(const void *d_dY, const void *d_X, float *d_dW, 
     st = quantize_mxfp8_impl(d_dY, T, N, d_X, T, K, aq, as, bq, bs, st_);
     if (st != MX_OK) return st;
     return gemm_mxfp8_impl(aq, as, bq, bs, d_dW, N, K, T, st_);
+}
+
+size_t mx_nvfp4_scales_bytes(int64_t mn, int64_t k) {
+    if (mn <= 0 || k <= 0) return 0;
+    return static_cast<size_t>(scale_groups(mn)) * 128u * static_cast<size_t>(16 * ((k + 255) / 256));
+}
+
+mx_status mx_quantize_nvfp4(const void *d_src, int64_t rows, int64_t cols, int rot, int rot_block,
+                            uint64_t seed, void *d_codes, void *d_scales, float *d_amax,
+                            void *stream) {
+    TraceRange trace("mx_quantize_nvfp4");
+    return quantize_nvfp4_impl(d_src, rows, cols, nullptr, 0, 0, rot, rot_block, seed, d_codes,
+                               d_scales, nullptr, nullptr, d_amax,
+                               static_cast<cudaStream_t>(stream));
+}
+
+mx_status mx_gemm_nvfp4(const void *d_Aq, const void *d_As, const float *d_amax_a,
+                        const void *d_Bq, const void *d_Bs, const float *d_amax_b, float *d_C,
+                        int64_t M, int64_t N, int64_t K, void *stream) {
+    TraceRange trace("mx_gemm_nvfp4");
+    return gemm_nvfp4_impl(d_Aq, d_As, d_amax_a, d_Bq, d_Bs, d_amax_b, d_C, M, N, K,
+                           static_cast<cudaStream_t>(stream));
+}
+
+size_t mx_linear_wgrad_nvfp4_workspace_bytes(int64_t T, int64_t N, int64_t K) {
+    if (T <= 0 || N <= 0 || K <= 0) return 0;
+    return align256(mx_codes_bytes(N, T)) + align256(mx_nvfp4_scales_bytes(N, T)) +
+           align256(mx_codes_bytes(K, T)) + align256(mx_nvfp4_scales_bytes(K, T)) + 256;
+}
+
+mx_status mx_linear_wgrad_nvfp4(const void *d_dY, const void *d_X, float *d_dW, int64_t T,
+                                int64_t N, int64_t K, int rot, int rot_block, uint64_t seed,
+                                void *d_ws, size_t ws_bytes, void *stream) {
+    TraceRange trace("mx_linear_wgrad_nvfp4");
+    const cudaStream_t st_ = static_cast<cudaStream_t>(stream);
+    if (T < 0 || N < 0 || K < 0) return MX_ERR_SHAPE;
+    if (N == 0 || K == 0) return MX_OK;
+    if (d_dW == nullptr) return MX_ERR_INVALID_ARG;
+    if (T == 0) {
+        mx_status st = check_gemm(nullptr, nullptr, nullptr, nullptr, d_dW, N, K, 0);
+        if (st != MX_OK) return st;
+        return from_cuda(cudaMemsetAsync(d_dW, 0, static_cast<size_t>(N) * K * sizeof(float), st_));
+    }
+    mx_status st = check_encode(d_dY, T, N, MX_CONTRACT_ROWS, rot, rot_block, MX_ROUND_RNE, d_dY,
+                                d_dY);
+    if (st != MX_OK) return st;
+    st = check_encode(d_X, T, K, MX_CONTRACT_ROWS, rot, rot_block, MX_ROUND_RNE, d_X, d_X);
+    if (st != MX_OK) return st;
+    if (rot != MX_ROT_NONE && rot_block != 16 && rot_block != 32) return MX_ERR_UNSUPPORTED;
+    if (K % 4 != 0 || !aligned16(d_dW)) return MX_ERR_ALIGN;
+    if (d_ws == nullptr || ws_bytes < mx_linear_wgrad_nvfp4_workspace_bytes(T, N, K))
+        return MX_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(d_ws) & 255u) != 0) return MX_ERR_ALIGN;
+    uint8_t *aq = static_cast<uint8_t *>(d_ws);
+    uint8_t *as = aq + align256(mx_codes_bytes(N, T));
+    uint8_t *bq = as + align256(mx_nvfp4_scales_bytes(N, T));
+    uint8_t *bs = bq + align256(mx_codes_bytes(K, T));
+    float *amax = reinterpret_cast<float *>(bs + align256(mx_nvfp4_scales_bytes(K, T)));
+    st = quantize_nvfp4_impl(d_dY, T, N, d_X, T, K, rot, rot_block, seed, aq, as, bq, bs, amax,
+                             st_);
+    if (st != MX_OK) return st;
+    return gemm_nvfp4_impl(aq, as, amax, bq, bs, amax + 1, d_dW, N, K, T, st_);
 }
 
 int mx_linear_wgrad_fused_supported(int64_t T, int64_t N, int64_t K, int rot, int rot_block,

@@ -363,6 +363,64 @@ __device__ __forceinline__ void encode_pair_e4m3(const uint64_t (&x)[32], uint4 
     }
 }
 
+// ---------------------------------------------------------------- NVFP4
+// Value of an E4M3 code (sign ignored: block scales are non-negative; the
+// NaN code never reaches this), exact in fp32.
+__device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
+    const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+    return e == 0u ? __uint2float_rn(m) * 0.001953125f            // m * 2^-9
+                   : __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+// E4M3 code of a non-negative finite value, nearest even, saturating at 448.
+__device__ __forceinline__ uint32_t f32_to_e4m3(float u) {
+    uint16_t h;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(0.0f), "f"(u));
+    return h & 0xFFu;
+}
+
+// Tensor encode scale of NVFP4 from the tensor's largest finite magnitude:
+// 2688 / amax (448 * 6, the largest block value), FLT_MAX if that overflows,
+// 1 for amax == 0.
+__device__ __forceinline__ float nv_tensor_scale(float amax) {
+    if (!(amax > 0.0f) || !(amax <= 3.402823466e38f)) return 1.0f;
+    const float s = __fdiv_rn(2688.0f, amax);
+    return s <= 3.402823466e38f ? s : 3.402823466e38f;
+}
+
+// NVFP4 encode of one block of 16 rotated values: returns the UE4M3 scale
+// code (0x7F for a block holding Inf/NaN) and the 8 code bytes in q.
+__device__ __forceinline__ uint32_t nv_encode_block16(const float *r, float s_enc, uint2 &q) {
+    uint32_t mb = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) mb = max(mb, __float_as_uint(r[i]) & 0x7FFFFFFFu);
+    if (mb >= 0x7F800000u) {
+        q = make_uint2(0, 0);
+        return 0x7Fu;
+    }
+    const float u = __fmul_rn(__fdiv_rn(__uint_as_float(mb), 6.0f), s_enc);
+    const uint32_t sf = f32_to_e4m3(u);
+    if (sf == 0u) {
+        q = make_uint2(0, 0);
+        return 0u;
+    }
+    float m = __fdiv_rn(s_enc, e4m3_to_f32(sf));
+    m = m <= 3.402823466e38f ? m : 3.402823466e38f;
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(r[i], m);
+    q = make_uint2(cvt_e2m1x8(v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]),
+                   cvt_e2m1x8(v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15]));
+    return sf;
+}
+
+// Byte offset of the NVFP4 scale of (line, block of 16) in its tiled layout:
+// 512-byte atoms of 128 lines x 4 blocks, `katoms` atoms per 128-line group.
+__device__ __forceinline__ int64_t nv_scale_offset(int64_t line, int64_t block, int64_t katoms) {
+    return ((line / 128) * katoms + block / 4) * 512 + (line % 32) * 16 + ((line % 128) / 32) * 4 +
+           (block % 4);
+}
+
 __device__ __forceinline__ void st_global_16(void *p, uint4 v) {
     asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
                  "r"(v.z), "r"(v.w)

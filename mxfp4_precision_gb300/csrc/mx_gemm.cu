@@ -56,8 +56,7 @@ namespace {
 constexpr int kTile = 256;                        // output tile (rows and columns) per pair
 constexpr int kHalf = 128;                        // rows of A / of B per CTA
 constexpr int kBKBytes = 128;                     // 256 FP4 per row per K sub-tile
-constexpr int kKSub = 2;                          // K sub-tiles per stage (K = 512)
-constexpr int kStages = 3;
+constexpr int kMaxStages = 5;
 constexpr int kWriterWarp0 = 4;                   // warps 4..7: scale writers
 constexpr int kEpiWarp0 = 8;                      // warps 8..15: epilogue
 constexpr int kEpiWarps = 8;
@@ -79,25 +78,37 @@ struct Variant {
     static_assert(kThreads * kLaunchRegs <= 65536, "launch registers fit the SM");
 };
 constexpr uint32_t kSubBytes = kHalf * kBKBytes;  // 16 KB: 128 rows x one K sub-tile
-constexpr uint32_t kSFSub = 1024;                 // scale room of 128 rows x one K sub-tile
-// Element formats: a 128-byte K sub-tile row holds 256 E2M1 (MXFP4: two
-// 512-byte scale atoms per 128 rows) or 128 E4M3 (MXFP8: one atom).
-template <bool F8>
-struct Elem {
-    static constexpr int kSubK = F8 ? 128 : 256;          // elements per sub-tile row
-    static constexpr int kAtoms = F8 ? 1 : 2;             // scale atoms per sub-tile
-    static constexpr uint32_t kSFBytes = 512u * kAtoms;   // scale bytes per 128 rows
-};
-constexpr uint32_t kOffA = 0;
-constexpr uint32_t kOffB = kKSub * kSubBytes;
-constexpr uint32_t kOffSFA = 2 * kKSub * kSubBytes;
-constexpr uint32_t kOffSFB = kOffSFA + kKSub * kSFSub;           // two 128-row groups of B
-constexpr uint32_t kStageBytes = kOffSFB + 2 * kKSub * kSFSub;   // 70 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;                    // accumulator: columns [0, 256)
-constexpr uint32_t kSFCol = 256;                   // scale slots: 24 columns per K sub-tile
-constexpr uint32_t kSFSlot = 24 * kKSub;
-static_assert(kSFCol + kStages * kSFSlot <= kTmemCols, "scale slots fit in tensor memory");
+constexpr uint32_t kSFCol = 256;                   // scale slots from column 256
+// Element formats and the stage geometry each needs.  A 128-byte K sub-tile
+// row holds 256 E2M1 (MXFP4, NVFP4) or 128 E4M3 (MXFP8).  Scales arrive as
+// 512-byte atoms of 128 rows: two per sub-tile for MXFP4 (E8M0 per 32), one
+// for MXFP8, four for NVFP4 (UE4M3 per 16).  In tensor memory a sub-tile's
+// scales take 24 columns (MX: A 8, B 16) or 48 (NVFP4: 4 per MMA for A, 8
+// for B), so NVFP4 stages hold one sub-tile and five stages fit beside the
+// accumulator; the MX formats run three stages of two sub-tiles.
+constexpr int kFmtMX4 = 0, kFmtMX8 = 1, kFmtNV4 = 2;
+template <int FMT>
+struct Elem {
+    static constexpr bool kNV = FMT == kFmtNV4;
+    static constexpr int kSubK = FMT == kFmtMX8 ? 128 : 256;   // elements per sub-tile row
+    static_assert(kSubK == 128 || kSubK == 256, "128-byte sub-tile rows");
+    static constexpr int kAtoms = FMT == kFmtMX8 ? 1 : kNV ? 4 : 2;
+    static constexpr uint32_t kSFBytes = 512u * kAtoms;         // scale bytes per 128 rows
+    static constexpr int kKSub = kNV ? 1 : 2;                   // sub-tiles per stage
+    static constexpr int kStages = kNV ? 5 : 3;
+    static constexpr uint32_t kSFSub = kNV ? 2048 : 1024;       // scale room per sub-tile
+    static constexpr uint32_t kOffA = 0;
+    static constexpr uint32_t kOffB = kKSub * kSubBytes;
+    static constexpr uint32_t kOffSFA = 2 * kKSub * kSubBytes;
+    static constexpr uint32_t kOffSFB = kOffSFA + kKSub * kSFSub;          // two row groups of B
+    static constexpr uint32_t kStageBytes = kOffSFB + 2 * kKSub * kSFSub;  // 70 KB / 38 KB
+    static constexpr uint32_t kSFCols = kNV ? 48 : 24;          // tensor-memory columns per sub-tile
+    static constexpr uint32_t kSFSlot = kSFCols * kKSub;
+    static_assert(kStages <= kMaxStages, "barrier arrays");
+    static_assert(kSFCol + kStages * kSFSlot <= kTmemCols, "scale slots fit in tensor memory");
+};
 
 // Fused Wgrad: the encoder warps of every CTA encode both operands (dY
 // [T][N], X [T][K], contraction T) into the workspace while the GEMM runs.
@@ -139,21 +150,23 @@ struct GemmArgs {
     int64_t a_groups;    // 128-row scale groups that exist for A
     int64_t b_groups;    // ... and for B
     int k_tiles;         // 256-wide K sub-tiles
-    int k_stages;        // stages per tile (ceil(k_tiles / kKSub))
+    int k_stages;        // stages per tile (ceil(k_tiles / sub-tiles per stage))
     int m_tiles;
     int n_tiles;
     int num_tiles;
     int num_items;       // one item per tile
     int c_v8;            // C rows allow 32-byte stores (N % 8 == 0, C 32-byte aligned)
     size_t c_bytes;      // extent of C (store guards)
+    const float *amax_a; // NVFP4: tensor amaxes of A and B (the result is divided by
+    const float *amax_b; //   the product of their encode scales)
     int *status;
 };
 
 struct SharedCtl {
-    uint64_t full[kStages];      // even CTA: both CTAs' operand bytes of the stage have landed
-    uint64_t sf_full[kStages];   // this CTA's scale bytes of the stage have landed
-    uint64_t empty[kStages];     // the pair's MMAs have finished reading the stage
-    uint64_t sf_ready[kStages];  // even CTA: both CTAs' scales of the stage are in tensor memory
+    uint64_t full[kMaxStages];      // even CTA: both CTAs' operand bytes of the stage have landed
+    uint64_t sf_full[kMaxStages];   // this CTA's scale bytes of the stage have landed
+    uint64_t empty[kMaxStages];     // the pair's MMAs have finished reading the stage
+    uint64_t sf_ready[kMaxStages];  // even CTA: both CTAs' scales of the stage are in tensor memory
     uint64_t acc_full;           // the tile's accumulator is complete
     uint64_t acc_empty;          // even CTA: both CTAs' epilogues have read the accumulator
     uint64_t drain;
@@ -331,14 +344,18 @@ __device__ __forceinline__ void encode_units(const FusedArgs &f, int gw, int W, 
     }
 }
 
-template <bool FUSED, bool F8>
+template <bool FUSED, int FMT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                    const __grid_constant__ CUtensorMap map_b, const GemmArgs g,
                    const __grid_constant__ FusedArgs f) {
     using V = Variant<FUSED>;
-    using E = Elem<F8>;
-    static_assert(!(FUSED && F8), "the fused launch encodes MXFP4 only");
+    using E = Elem<FMT>;
+    static_assert(!(FUSED && FMT != kFmtMX4), "the fused launch encodes MXFP4 only");
+    constexpr int kStages = E::kStages, kKSub = E::kKSub;
+    constexpr uint32_t kStageBytes = E::kStageBytes, kSFSlot = E::kSFSlot, kSFSub = E::kSFSub;
+    constexpr uint32_t kOffA = E::kOffA, kOffB = E::kOffB, kOffSFA = E::kOffSFA,
+                       kOffSFB = E::kOffSFB;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned base, kept as a shared-space pointer (offset arithmetic
     // only) so that the compiler emits shared-memory loads.  The offset is the
@@ -466,6 +483,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThr
             uint32_t idesc8[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) idesc8[j] = idesc_mxf8(2 * kHalf, kTile, j, j);
+            const uint32_t idesc_nv = idesc_nvf4(2 * kHalf, kTile);
             for (int w = pair; ok && w < g.num_items; w += npairs) {
                 const Item it = item_of(g, w);
                 if (!mbar_wait_inl(&ctl->acc_empty, acc_phase ^ 1u, g.status, abort)) break;
@@ -484,16 +502,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThr
                     for (int u = 0; u < nsub; ++u) {
                         const uint32_t sa = sbase + kOffA + u * kSubBytes;
                         const uint32_t sb = sbase + kOffB + u * kSubBytes;
-                        const uint32_t sf = slot + 24u * static_cast<uint32_t>(u);
+                        const uint32_t sf = slot + E::kSFCols * static_cast<uint32_t>(u);
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             const uint32_t acc = (ks > it.ks0 || u > 0 || j > 0) ? 1u : 0u;
-                            if constexpr (F8) {
+                            if constexpr (FMT == kFmtMX8) {
                                 // K = 32 per MMA: block j of the sub-tile's
                                 // single scale atom (byte j of its columns).
                                 mma_mxf8_pair(tmem + kAccCol, sdesc_sw128(sa + 32u * j),
                                               sdesc_sw128(sb + 32u * j), idesc8[j], sf, sf + 8u,
                                               acc);
+                            } else if constexpr (FMT == kFmtNV4) {
+                                // K = 64 per MMA: four UE4M3 scales per row,
+                                // one whole column per row group.
+                                mma_nvf4_pair(tmem + kAccCol, sdesc_sw128(sa + 32u * j),
+                                              sdesc_sw128(sb + 32u * j), idesc_nv, sf + 4u * j,
+                                              sf + 16u + 8u * j, acc);
                             } else {
                                 const uint32_t ka = static_cast<uint32_t>(j / 2);
                                 mma_mxf4_pair(tmem + kAccCol, sdesc_sw128(sa + 32u * j),
@@ -552,8 +576,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThr
                 for (int u = 0; u < nsub; ++u) {
                     const uint8_t *sfa = st + kOffSFA + u * E::kSFBytes;
                     const uint8_t *sfb = st + kOffSFB + u * E::kSFBytes;
-                    const uint32_t col = slot + 24u * static_cast<uint32_t>(u);
-                    if constexpr (F8) {
+                    const uint32_t col = slot + E::kSFCols * static_cast<uint32_t>(u);
+                    if constexpr (FMT == kFmtNV4) {
+                        // Atom j holds MMA j's scales: A at columns 4j..4j+3,
+                        // B at 16 + 8j + 4rb + c.
+                        uint32_t a16[16], b16[16];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint4 v = *reinterpret_cast<const uint4 *>(sfa + j * 512 + lane * 16);
+                            a16[4 * j + 0] = v.x;
+                            a16[4 * j + 1] = v.y;
+                            a16[4 * j + 2] = v.z;
+                            a16[4 * j + 3] = v.w;
+                        }
+                        tmem_st_32x32b_x16(col, a16);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                            for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+                                for (int rb = 0; rb < 2; ++rb) {
+                                    const uint4 v = *reinterpret_cast<const uint4 *>(
+                                        sfb + rb * kKSub * kSFSub + (2 * h + jj) * 512 + lane * 16);
+                                    b16[8 * jj + 4 * rb + 0] = v.x;
+                                    b16[8 * jj + 4 * rb + 1] = v.y;
+                                    b16[8 * jj + 4 * rb + 2] = v.z;
+                                    b16[8 * jj + 4 * rb + 3] = v.w;
+                                }
+                            tmem_st_32x32b_x16(col + 16u + 16u * h, b16);
+                        }
+                    } else if constexpr (FMT == kFmtMX8) {
                         // One atom: A at columns 0..3, B at 8..15 (ka = 0).
                         uint32_t a4[4], b8[8];
                         const uint4 va = *reinterpret_cast<const uint4 *>(sfa + lane * 16);
@@ -572,8 +624,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThr
                         }
                         tmem_st_32x32b_x4(col, a4);
                         tmem_st_32x32b_x8(col + 8u, b8);
-                        continue;
-                    }
+                    } else {
                     uint32_t a[8], b[16];
 #pragma unroll
                     for (int ka = 0; ka < 2; ++ka) {
@@ -596,6 +647,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThr
                         }
                     tmem_st_32x32b_x8(col, a);
                     tmem_st_32x32b_x16(col + 8u, b);
+                    }
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -613,6 +665,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThr
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(V::kRegsHigh) : "memory");
         const int q = warp & 3;                   // TMEM lane quarter this warp may access
         const int half = (warp - kEpiWarp0) / 4;  // column half of the 256-wide tile
+        float alpha = 1.0f;
+        if constexpr (FMT == kFmtNV4)
+            alpha = __frcp_rn(__fmul_rn(enc::nv_tensor_scale(*g.amax_a),
+                                        enc::nv_tensor_scale(*g.amax_b)));
+        (void)alpha;
         uint32_t acc_phase = 0;
         int staged = 0;                           // stages of this pair's items so far
         for (int w = pair; w < g.num_items; w += npairs) {
@@ -678,6 +735,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThr
             tmem_ld_32x32b_x32(tbase + 64u, v2);
             tmem_ld_32x32b_x32(tbase + 96u, v3);
             tmem_ld_wait();
+            if constexpr (FMT == kFmtNV4) {
+                // C = (sum of e2m1 * sf products) / (s_enc(A) * s_enc(B)).
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    v0[i] = __float_as_uint(__fmul_rn(__uint_as_float(v0[i]), alpha));
+                    v1[i] = __float_as_uint(__fmul_rn(__uint_as_float(v1[i]), alpha));
+                    v2[i] = __float_as_uint(__fmul_rn(__uint_as_float(v2[i]), alpha));
+                    v3[i] = __float_as_uint(__fmul_rn(__uint_as_float(v3[i]), alpha));
+                }
+            }
             // The accumulator is in registers: the next item may start.
             tc_fence_before();
             __syncwarp();
@@ -738,25 +805,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThr
     }
 }
 
-constexpr size_t kGemmSmem = kStages * kStageBytes + sizeof(SharedCtl) + 1024;
+template <int FMT>
+constexpr size_t gemm_smem() {
+    return Elem<FMT>::kStages * Elem<FMT>::kStageBytes + sizeof(SharedCtl) + 1024;
+}
 
 // Co-resident 2-CTA clusters of a mx_gemm_kernel variant on a device,
 // measured once.
-template <bool FUSED, bool F8>
+template <bool FUSED, int FMT>
 int gemm_clusters(const DeviceInfo &dev) {
     static std::atomic<int> cache[64];
     const int idx = dev.ordinal >= 0 && dev.ordinal < 64 ? dev.ordinal : 0;
     int n = cache[idx].load(std::memory_order_relaxed);
     if (n > 0) return n;
-    if (cudaFuncSetAttribute(mx_gemm_kernel<FUSED, F8>,
+    if (cudaFuncSetAttribute(mx_gemm_kernel<FUSED, FMT>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kGemmSmem)) != cudaSuccess)
+                             static_cast<int>(gemm_smem<FMT>())) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(2, 1, 1);
     cfg.blockDim = dim3(Variant<FUSED>::kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kGemmSmem;
-    if (cudaOccupancyMaxActiveClusters(&n, mx_gemm_kernel<FUSED, F8>, &cfg) != cudaSuccess ||
+    cfg.dynamicSmemBytes = gemm_smem<FMT>();
+    if (cudaOccupancyMaxActiveClusters(&n, mx_gemm_kernel<FUSED, FMT>, &cfg) != cudaSuccess ||
         n < 1)
         return 0;
     cache[idx].store(n, std::memory_order_relaxed);
@@ -764,9 +834,10 @@ int gemm_clusters(const DeviceInfo &dev) {
 }
 
 // Common set-up of both variants: tensor maps and the GEMM arguments.
-bool gemm_setup(bool f8, const void *Aq, const void *As, const void *Bq, const void *Bs,
+bool gemm_setup(int fmt, const void *Aq, const void *As, const void *Bq, const void *Bs,
                 float *C, int64_t M, int64_t N, int64_t K, const DeviceInfo &dev,
                 CUtensorMap *map_a, CUtensorMap *map_b, GemmArgs *g) {
+    const bool f8 = fmt == kFmtMX8, nv = fmt == kFmtNV4;
     const int64_t row_bytes = f8 ? K : K / 2;
     if (!encode_tmap_2d(map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, Aq, row_bytes, M, row_bytes,
                         kBKBytes, kHalf, CU_TENSOR_MAP_SWIZZLE_128B))
@@ -781,12 +852,13 @@ bool gemm_setup(bool f8, const void *Aq, const void *As, const void *Bq, const v
     g->M = M;
     g->N = N;
     g->K = K;
-    g->katoms = scale_katoms(K);
+    g->katoms = nv ? nv_scale_katoms(K) : scale_katoms(K);
     g->a_groups = scale_groups(M);
     g->b_groups = scale_groups(N);
-    const int64_t sub_k = f8 ? Elem<true>::kSubK : Elem<false>::kSubK;
+    const int64_t sub_k = f8 ? Elem<kFmtMX8>::kSubK : Elem<kFmtMX4>::kSubK;
+    const int ksub = nv ? Elem<kFmtNV4>::kKSub : Elem<kFmtMX4>::kKSub;
     g->k_tiles = static_cast<int>((K + sub_k - 1) / sub_k);
-    g->k_stages = (g->k_tiles + kKSub - 1) / kKSub;
+    g->k_stages = (g->k_tiles + ksub - 1) / ksub;
     const int64_t m_tiles = (M + kTile - 1) / kTile;
     const int64_t n_tiles = (N + kTile - 1) / kTile;
     if (m_tiles * n_tiles > 0x3FFFFFFF) return false;
@@ -800,24 +872,24 @@ bool gemm_setup(bool f8, const void *Aq, const void *As, const void *Bq, const v
     return true;
 }
 
-template <bool FUSED, bool F8>
+template <bool FUSED, int FMT>
 cudaError_t gemm_launch(const CUtensorMap &map_a, const CUtensorMap &map_b, const GemmArgs &g,
                         const FusedArgs &f, int pairs, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel<FUSED, F8>,
+    cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel<FUSED, FMT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kGemmSmem));
+                                         static_cast<int>(gemm_smem<FMT>()));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(2 * pairs, 1, 1);
     cfg.blockDim = dim3(Variant<FUSED>::kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kGemmSmem;
+    cfg.dynamicSmemBytes = gemm_smem<FMT>();
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, mx_gemm_kernel<FUSED, F8>, map_a, map_b, g, f);
+    e = cudaLaunchKernelEx(&cfg, mx_gemm_kernel<FUSED, FMT>, map_a, map_b, g, f);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -825,35 +897,50 @@ cudaError_t gemm_launch(const CUtensorMap &map_a, const CUtensorMap &map_b, cons
 }  // namespace
 
 namespace {
-template <bool F8>
+template <int FMT>
 cudaError_t launch_gemm_elem(const void *Aq, const void *As, const void *Bq, const void *Bs,
-                             float *C, int64_t M, int64_t N, int64_t K, const DeviceInfo &dev,
-                             cudaStream_t stream) {
+                             float *C, int64_t M, int64_t N, int64_t K, const float *amax_a,
+                             const float *amax_b, const DeviceInfo &dev, cudaStream_t stream) {
     CUtensorMap map_a, map_b;
     GemmArgs g;
-    if (!gemm_setup(F8, Aq, As, Bq, Bs, C, M, N, K, dev, &map_a, &map_b, &g))
+    if (!gemm_setup(FMT, Aq, As, Bq, Bs, C, M, N, K, dev, &map_a, &map_b, &g))
         return cudaErrorInvalidValue;
+    g.amax_a = amax_a;
+    g.amax_b = amax_b;
     // Resident CTAs: as many 2-CTA clusters as fit at once, one tile per pair.
-    const int pairs_max = gemm_clusters<false, F8>(dev);
+    const int pairs_max = gemm_clusters<false, FMT>(dev);
     if (pairs_max < 1) return cudaErrorLaunchOutOfResources;
     const int pairs = g.num_items < pairs_max ? g.num_items : pairs_max;
     FusedArgs f;
     std::memset(&f, 0, sizeof(f));
-    return gemm_launch<false, F8>(map_a, map_b, g, f, pairs, stream);
+    return gemm_launch<false, FMT>(map_a, map_b, g, f, pairs, stream);
 }
 }  // namespace
 
 cudaError_t launch_gemm(const void *Aq, const void *As, const void *Bq, const void *Bs, float *C,
                         int64_t M, int64_t N, int64_t K, const DeviceInfo &dev,
                         cudaStream_t stream) {
-    return launch_gemm_elem<false>(Aq, As, Bq, Bs, C, M, N, K, dev, stream);
+    return launch_gemm_elem<kFmtMX4>(Aq, As, Bq, Bs, C, M, N, K, nullptr, nullptr, dev, stream);
 }
 
-cudaError_t launch_gemm_fmt(bool f8, const void *Aq, const void *As, const void *Bq,
+cudaError_t launch_gemm_fmt(int fmt, const void *Aq, const void *As, const void *Bq,
                             const void *Bs, float *C, int64_t M, int64_t N, int64_t K,
-                            const DeviceInfo &dev, cudaStream_t stream) {
-    return f8 ? launch_gemm_elem<true>(Aq, As, Bq, Bs, C, M, N, K, dev, stream)
-              : launch_gemm_elem<false>(Aq, As, Bq, Bs, C, M, N, K, dev, stream);
+                            const float *amax_a, const float *amax_b, const DeviceInfo &dev,
+                            cudaStream_t stream) {
+    switch (fmt) {
+        case kGemmMXFP4:
+            return launch_gemm_elem<kFmtMX4>(Aq, As, Bq, Bs, C, M, N, K, nullptr, nullptr, dev,
+                                             stream);
+        case kGemmMXFP8:
+            return launch_gemm_elem<kFmtMX8>(Aq, As, Bq, Bs, C, M, N, K, nullptr, nullptr, dev,
+                                             stream);
+        case kGemmNVFP4:
+            if (amax_a == nullptr || amax_b == nullptr) return cudaErrorInvalidValue;
+            return launch_gemm_elem<kFmtNV4>(Aq, As, Bq, Bs, C, M, N, K, amax_a, amax_b, dev,
+                                             stream);
+        default:
+            return cudaErrorInvalidValue;
+    }
 }
 
 size_t wgrad_fused_counter_bytes(int64_t T, int64_t N, int64_t K) {
@@ -878,9 +965,9 @@ cudaError_t launch_wgrad_fused(const void *dY, const void *X, float *dW, int64_t
     CUtensorMap map_a, map_b;
     GemmArgs g;
     // dW[N][K] = A . B^T with A = dY^T (N lines), B = X^T (K lines), contraction T.
-    if (!gemm_setup(false, Aq, As, Bq, Bs, dW, N, K, T, dev, &map_a, &map_b, &g))
+    if (!gemm_setup(kFmtMX4, Aq, As, Bq, Bs, dW, N, K, T, dev, &map_a, &map_b, &g))
         return cudaErrorInvalidValue;
-    const int pairs_max = gemm_clusters<true, false>(dev);
+    const int pairs_max = gemm_clusters<true, kFmtMX4>(dev);
     if (pairs_max < 1) return cudaErrorLaunchOutOfResources;
     const int pairs = g.num_items < pairs_max ? g.num_items : pairs_max;
 
@@ -929,7 +1016,7 @@ cudaError_t launch_wgrad_fused(const void *dY, const void *X, float *dW, int64_t
     f.units = kUnitsPerChunk * f.chunks * np;
     cudaError_t e = cudaMemsetAsync(counters, 0, wgrad_fused_counter_bytes(T, N, K), stream);
     if (e != cudaSuccess) return e;
-    return gemm_launch<true, false>(map_a, map_b, g, f, pairs, stream);
+    return gemm_launch<true, kFmtMX4>(map_a, map_b, g, f, pairs, stream);
 }
 
 }  // namespace mx

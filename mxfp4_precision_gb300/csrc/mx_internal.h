@@ -25,6 +25,8 @@ bool encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *bas
 // Scale-layout geometry (see mx.h): k-atoms (4 blocks of 32) per 128-line group.
 inline int64_t scale_katoms(int64_t k) { return 2 * ((k + 255) / 256); }
 inline int64_t scale_groups(int64_t mn) { return (mn + 127) / 128; }
+// NVFP4 scale layout: 512-byte atoms of 128 lines x 4 blocks of 16.
+inline int64_t nv_scale_katoms(int64_t k) { return 4 * ((k + 255) / 256); }
 
 // Kernel launchers (argument validation happens before these are called).
 cudaError_t launch_quantize(const void *src, int64_t rows, int64_t cols, int contract, int rot,
@@ -59,10 +61,27 @@ cudaError_t launch_quantize_mxfp8_colwise(const void *src0, int64_t rows0, int64
                                           void *scales1, const DeviceInfo &dev,
                                           cudaStream_t stream);
 
-// Block-scaled GEMM over MXFP4 (f8 false) or MXFP8 (f8 true) operands.
-cudaError_t launch_gemm_fmt(bool f8, const void *Aq, const void *As, const void *Bq,
+// NVFP4 encode down the rows of one or two operands (src1 == nullptr: one):
+// zeroes amax[0..1], a first launch max-reduces each rotated operand's
+// largest finite magnitude into it, a second encodes with the tensor scale
+// 2688 / amax.  Rotation none, or Hadamard 16 / 32 (rot 1 deterministic, 2
+// with random signs); round to nearest.  Codes [cols][rows/2], scales in the
+// NVFP4 tiled layout.
+cudaError_t launch_quantize_nvfp4_colwise(const void *src0, int64_t rows0, int64_t cols0,
+                                          const void *src1, int64_t rows1, int64_t cols1, int rot,
+                                          int rot_block, uint64_t seed, void *codes0,
+                                          void *scales0, void *codes1, void *scales1,
+                                          float *amax, const DeviceInfo &dev,
+                                          cudaStream_t stream);
+
+// Block-scaled GEMM over MXFP4 (fmt 0), MXFP8 (fmt 1) or NVFP4 (fmt 2)
+// operands; NVFP4 reads the two tensor amaxes (device floats) and scales the
+// result by 1 / (s_enc(a) * s_enc(b)).
+enum { kGemmMXFP4 = 0, kGemmMXFP8 = 1, kGemmNVFP4 = 2 };
+cudaError_t launch_gemm_fmt(int fmt, const void *Aq, const void *As, const void *Bq,
                             const void *Bs, float *C, int64_t M, int64_t N, int64_t K,
-                            const DeviceInfo &dev, cudaStream_t stream);
+                            const float *amax_a, const float *amax_b, const DeviceInfo &dev,
+                            cudaStream_t stream);
 
 cudaError_t launch_gemm(const void *Aq, const void *As, const void *Bq, const void *Bs, float *C,
                         int64_t M, int64_t N, int64_t K, const DeviceInfo &dev,

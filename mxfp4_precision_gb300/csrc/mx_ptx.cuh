@@ -414,6 +414,30 @@ __device__ __forceinline__ void mma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, 
         : "memory");
 }
 
+// Instruction descriptor for kind::mxf4nvf4 with scale_vec::4X (NVFP4: E2M1
+// x E2M1, one UE4M3 scale per 16 elements, four per row per MMA), fp32
+// accumulate, K-major, tile M x N.
+__host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
+    return (1u << 7)                                      // A format: E2M1
+           | (1u << 10)                                   // B format: E2M1
+           | (static_cast<uint32_t>(N >> 3) << 17)        // N / 8
+           | (0u << 23)                                   // scale format: UE4M3
+           | (static_cast<uint32_t>(M >> 4) << 24);       // M / 16
+}
+
+// The NVFP4 form of mma_mxf4_pair (K = 64 per instruction).
+__device__ __forceinline__ void mma_nvf4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
+        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive on the barrier at shared offset `bar` of every CTA in `cta_mask`
 // once every pair operation issued so far by this thread has completed.
 __device__ __forceinline__ void tc_commit_pair(uint64_t *bar, uint16_t cta_mask) {

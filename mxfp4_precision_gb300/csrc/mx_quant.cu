@@ -67,6 +67,7 @@ struct QuantArgs {
     size_t scales_bytes;
     uint64_t seed;
     uint64_t sr_tag;
+    unsigned int *amax;  // NVFP4: the operand's tensor amax (fp32 bits; max-reduced)
     int *status;
     int tiles_inner;   // tiles along the fast tile axis
     int num_tiles;
@@ -198,9 +199,13 @@ struct ColTile {
 // all eight compute warps have released it, so no compute warp waits for the
 // slowest one.  (The dual variant keeps its registers for the row encode and
 // refills from thread 0 instead.)
-// With F8 (MXFP8, the FP8 comparator: no rotation, round to nearest) each
-// block becomes 32 E4M3 code bytes under the same E8M0 scale layout.
-template <int ROTN, bool RAND, bool SR, bool DUAL, bool F8 = false>
+// Element formats of the column encoder: MXFP4; MXFP8 (the FP8 comparator:
+// no rotation, round to nearest; each block becomes 32 E4M3 code bytes under
+// the same E8M0 scale layout); and the two passes of NVFP4 (the tensor amax
+// of the rotated operand, then the encode with its tensor scale: blocks of
+// 16, UE4M3 scales in their own tiled layout).
+constexpr int kFmtMX4 = 0, kFmtMX8 = 1, kFmtNVAmax = 2, kFmtNV4 = 3;
+template <int ROTN, bool RAND, bool SR, bool DUAL, int FMT = kFmtMX4>
 __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads, SR ? 1 : kColMinBlocks)
     mxq_colwise_kernel(
     const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
@@ -316,7 +321,7 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads, SR ? 1 
                     x[i] ^= ((bits >> i) & 1u) ? 0x8000000080000000ull : 0ull;
             }
             fwht_pairs<ROTN>(x);
-            if (SR) {  // round to nearest folds the factor into the scale multiply
+            if (SR || FMT >= kFmtNVAmax) {  // MXFP4 RNE folds the factor into its scale multiply
                 const float cn = hadamard_norm<ROTN>();
                 const uint64_t cc = pack2(cn, cn);
 #pragma unroll
@@ -326,9 +331,56 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads, SR ? 1 
 
         const int64_t tb = t0 + 32 * tbi;               // first token of this thread's block
         const int64_t c = c0 + 64 * chalf + 2 * lane;  // first of the thread's two channels
+        if constexpr (FMT == kFmtNVAmax) {
+            // Largest finite magnitude of the thread's 64 rotated values,
+            // then of the warp; one atomic per warp and tile.
+            static_assert(!SR && !DUAL, "NVFP4: round to nearest, one direction");
+            float m = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                float lo, hi;
+                unpack2(x[i], lo, hi);
+                lo = fabsf(lo);
+                hi = fabsf(hi);
+                m = fmaxf(m, lo <= 3.402823466e38f ? lo : 0.0f);
+                m = fmaxf(m, hi <= 3.402823466e38f ? hi : 0.0f);
+            }
+            const unsigned int wm = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m));
+            unsigned int *amax = second ? a1.amax : a0.amax;
+            if (lane == 0 && wm != 0u) atomicMax(amax, wm);
+            continue;
+        }
+        if constexpr (FMT == kFmtNV4) {
+            static_assert(!SR && !DUAL, "NVFP4: round to nearest, one direction");
+            const float s_enc = nv_tensor_scale(__uint_as_float(*(second ? a1.amax : a0.amax)));
+            float l[32], h[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) unpack2(x[i], l[i], h[i]);
+            uint2 c00, c01, c10, c11;
+            const uint32_t f00 = nv_encode_block16(l, s_enc, c00);
+            const uint32_t f01 = nv_encode_block16(l + 16, s_enc, c01);
+            const uint32_t f10 = nv_encode_block16(h, s_enc, c10);
+            const uint32_t f11 = nv_encode_block16(h + 16, s_enc, c11);
+            if (tb < L) {
+                uint8_t *d0 = codes + c * (L / 2) + tb / 2, *d1 = codes + (c + 1) * (L / 2) + tb / 2;
+                if (c < lines && MX_STORE_OK(d0, 16, codes, codes_bytes, a0.status))
+                    st_global_16(d0, make_uint4(c00.x, c00.y, c01.x, c01.y));
+                if (c + 1 < lines && MX_STORE_OK(d1, 16, codes, codes_bytes, a0.status))
+                    st_global_16(d1, make_uint4(c10.x, c10.y, c11.x, c11.y));
+            }
+            // Two consecutive scale bytes per line (blocks tb/16 and tb/16 + 1).
+            const int64_t kb = tb / 16;
+            uint8_t *e0 = scales + nv_scale_offset(c, kb, katoms);
+            uint8_t *e1 = scales + nv_scale_offset(c + 1, kb, katoms);
+            if (MX_STORE_OK(e0, 2, scales, scales_bytes, a0.status))
+                *reinterpret_cast<uint16_t *>(e0) = static_cast<uint16_t>(f00 | (f01 << 8));
+            if (MX_STORE_OK(e1, 2, scales, scales_bytes, a0.status))
+                *reinterpret_cast<uint16_t *>(e1) = static_cast<uint16_t>(f10 | (f11 << 8));
+            continue;
+        }
         uint4 q0, q1;
         uint32_t s0, s1;
-        if constexpr (F8) {
+        if constexpr (FMT == kFmtMX8) {
             static_assert(ROTN == 0 && !RAND && !SR && !DUAL, "MXFP8: plain encode only");
             uint4 p0[2], p1[2];
             encode_pair_e4m3(x, p0, p1, s0, s1);
@@ -797,16 +849,18 @@ cudaError_t launch_dir(int rot, int rot_block, bool sr, const Operands &o, const
 // Fills the per-operand arguments (and tensor map) of one encode.
 bool prepare_operand(const void *src, int64_t rows, int64_t cols, bool colwise, int col_tt,
                      uint64_t seed, uint64_t sr_tag, void *codes, void *scales,
-                     const DeviceInfo &dev, CUtensorMap *map, QuantArgs *a, bool f8 = false) {
+                     const DeviceInfo &dev, CUtensorMap *map, QuantArgs *a, int fmt = kFmtMX4) {
     *a = QuantArgs{};
     a->L = colwise ? rows : cols;
     a->lines = colwise ? cols : rows;
-    a->katoms = scale_katoms(a->L);
+    const bool nv = fmt == kFmtNV4 || fmt == kFmtNVAmax;
+    a->katoms = nv ? nv_scale_katoms(a->L) : scale_katoms(a->L);
     a->codes = static_cast<uint8_t *>(codes);
     a->scales = static_cast<uint8_t *>(scales);
-    a->codes_bytes = static_cast<size_t>(a->lines) * static_cast<size_t>(f8 ? a->L : a->L / 2);
+    a->codes_bytes =
+        static_cast<size_t>(a->lines) * static_cast<size_t>(fmt == kFmtMX8 ? a->L : a->L / 2);
     a->scales_bytes = static_cast<size_t>(128 * scale_groups(a->lines)) *
-                      static_cast<size_t>(4 * scale_katoms(a->L));
+                      static_cast<size_t>(4 * a->katoms);
     a->seed = seed;
     a->sr_tag = sr_tag;
     a->status = dev.status;
@@ -900,19 +954,64 @@ cudaError_t launch_quantize_mxfp8_colwise(const void *src0, int64_t rows0, int64
                                           cudaStream_t stream) {
     Operands o;
     if (!prepare_operand(src0, rows0, cols0, true, 128, 0, 1, codes0, scales0, dev, &o.map0,
-                         &o.a0, true))
+                         &o.a0, kFmtMX8))
         return cudaErrorInvalidValue;
     o.map1 = o.map0;
     o.a1 = QuantArgs{};
     if (src1 != nullptr &&
         !prepare_operand(src1, rows1, cols1, true, 128, 0, 2, codes1, scales1, dev, &o.map1,
-                         &o.a1, true))
+                         &o.a1, kFmtMX8))
         return cudaErrorInvalidValue;
     o.ar = QuantArgs{};
     const size_t smem = kStages * kTileBytes + 1024 + 1024;
-    return launch_persistent_n(mxq_colwise_kernel<0, false, false, false, true>,
+    return launch_persistent_n(mxq_colwise_kernel<0, false, false, false, kFmtMX8>,
                                kColProducerThreads, o.a0.num_tiles + o.a1.num_tiles, smem, dev,
                                stream, o.map0, o.map1, o.a0, o.a1, o.ar);
+}
+
+namespace {
+template <int ROTN, bool RAND>
+cudaError_t launch_nv_passes(const Operands &o, const DeviceInfo &dev, cudaStream_t stream) {
+    const size_t smem = kStages * kTileBytes + 1024 + 1024;
+    const int n = o.a0.num_tiles + o.a1.num_tiles;
+    cudaError_t e = launch_persistent_n(mxq_colwise_kernel<ROTN, RAND, false, false, kFmtNVAmax>,
+                                        kColProducerThreads, n, smem, dev, stream, o.map0, o.map1,
+                                        o.a0, o.a1, o.ar);
+    if (e != cudaSuccess) return e;
+    return launch_persistent_n(mxq_colwise_kernel<ROTN, RAND, false, false, kFmtNV4>,
+                               kColProducerThreads, n, smem, dev, stream, o.map0, o.map1, o.a0,
+                               o.a1, o.ar);
+}
+}  // namespace
+
+cudaError_t launch_quantize_nvfp4_colwise(const void *src0, int64_t rows0, int64_t cols0,
+                                          const void *src1, int64_t rows1, int64_t cols1, int rot,
+                                          int rot_block, uint64_t seed, void *codes0,
+                                          void *scales0, void *codes1, void *scales1,
+                                          float *amax, const DeviceInfo &dev,
+                                          cudaStream_t stream) {
+    Operands o;
+    if (!prepare_operand(src0, rows0, cols0, true, 128, seed, 1, codes0, scales0, dev, &o.map0,
+                         &o.a0, kFmtNV4))
+        return cudaErrorInvalidValue;
+    o.a0.amax = reinterpret_cast<unsigned int *>(amax);
+    o.map1 = o.map0;
+    o.a1 = QuantArgs{};
+    if (src1 != nullptr) {
+        if (!prepare_operand(src1, rows1, cols1, true, 128, seed, 2, codes1, scales1, dev, &o.map1,
+                             &o.a1, kFmtNV4))
+            return cudaErrorInvalidValue;
+        o.a1.amax = reinterpret_cast<unsigned int *>(amax + 1);
+    }
+    o.ar = QuantArgs{};
+    cudaError_t e = cudaMemsetAsync(amax, 0, (src1 != nullptr ? 2 : 1) * sizeof(float), stream);
+    if (e != cudaSuccess) return e;
+    if (rot == 0) return launch_nv_passes<0, false>(o, dev, stream);
+    if (rot_block == 16) return rot == 2 ? launch_nv_passes<16, true>(o, dev, stream)
+                                         : launch_nv_passes<16, false>(o, dev, stream);
+    if (rot_block == 32) return rot == 2 ? launch_nv_passes<32, true>(o, dev, stream)
+                                         : launch_nv_passes<32, false>(o, dev, stream);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace mx

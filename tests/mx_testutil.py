@@ -23,6 +23,17 @@ def tile_scales(canon: np.ndarray, mn: int, k: int) -> np.ndarray:
     return np.ascontiguousarray(arr.transpose(0, 3, 2, 1, 4)).reshape(-1)
 
 
+def tile_scales_nv(canon: np.ndarray, mn: int, k: int) -> np.ndarray:
+    """NVFP4 canonical scales [mn, k/16] -> flat tiled layout: the same atom
+    geometry (128 lines x 4 blocks per 512 bytes) over KB = 16*ceil(k/256)
+    blocks of 16 per line (padding zero)."""
+    MP, KB = 128 * ((mn + 127) // 128), 16 * ((k + 255) // 256)
+    full = np.zeros((MP, KB), dtype=np.uint8)
+    full[:mn, :k // 16] = canon
+    arr = full.reshape(MP // 128, 4, 32, KB // 4, 4)
+    return np.ascontiguousarray(arr.transpose(0, 3, 2, 1, 4)).reshape(-1)
+
+
 def untile_scales(flat: np.ndarray, mn: int, k: int) -> np.ndarray:
     MP, KB = padded_dims(mn, k)
     arr = np.asarray(flat, dtype=np.uint8)[:MP * KB].reshape(MP // 128, KB // 4, 32, 4, 4)
