@@ -47,7 +47,18 @@ using namespace enc;
 #ifndef MXQ_STAGES
 #define MXQ_STAGES 2
 #endif
-constexpr int kStages = MXQ_STAGES;  // TMA ring depth per CTA
+constexpr int kStages = MXQ_STAGES;  // TMA ring depth per CTA (wide and row kernels)
+// The column kernel: a 3-deep ring and one output staging buffer (measured
+// best of ring 2/3 x buffers 1/2 at two CTAs per SM; MXFP8's larger staging
+// box keeps a 2-deep ring so that two CTAs still fit).
+#ifndef MXQ_COL_RING
+#define MXQ_COL_RING 3
+#endif
+#ifndef MXQ_STAGE_BUFS
+#define MXQ_STAGE_BUFS 1
+#endif
+constexpr int kColRing = MXQ_COL_RING;      // TMA ring depth of the column kernel
+constexpr int kStageBufs = MXQ_STAGE_BUFS;  // its output staging buffers
 // Two resident CTAs per SM (shared memory allows no more with two stages):
 // the round-to-nearest colwise kernels are held to 128 registers so that the
 // random-sign variants do not fall to one CTA per SM.
@@ -205,18 +216,46 @@ struct ColTile {
 // of the rotated operand, then the encode with its tensor scale: blocks of
 // 16, UE4M3 scales in their own tiled layout).
 constexpr int kFmtMX4 = 0, kFmtMX8 = 1, kFmtNVAmax = 2, kFmtNV4 = 3;
+//
+// Output path (every variant but DUAL and the amax pass): each warp writes
+// its codes and scale bytes into a shared-memory staging buffer laid out as
+// the tile's global image -- the codes as a [128 lines][64 B] box (128 B for
+// MXFP8) in the TMA's swizzled layout, the scales as the tile's whole
+// 512-byte scale atom (two atoms for NVFP4), which the tiled layout stores
+// contiguously.  After a named barrier, one thread stores the box with a TMA
+// tensor store and the atom with a bulk copy: whole lines reach L2 instead of
+// 16-byte pieces of 64 lines and single bytes.  Two staging buffers
+// alternate; the barrier that opens a tile also ANDs the warps' wait
+// verdicts, so an abort leaves every warp the same way and no warp waits at
+// a barrier the others have left.
+template <int FMT>
+struct ColStage {
+    static constexpr uint32_t kCodeBytes = FMT == kFmtMX8 ? 16384u : 8192u;  // 128 lines
+    static constexpr uint32_t kScaleBytes = FMT == kFmtNV4 ? 1024u : 512u;
+    // One buffer, a whole number of 1 KB (the swizzle patterns repeat every 512 B
+    // or 1 KB, so every codes box starts on such a boundary).
+    static constexpr uint32_t kBytes = (kCodeBytes + kScaleBytes + 1023u) / 1024u * 1024u;
+    static constexpr int kRing = FMT == kFmtMX8 && kColRing > 2 ? 2 : kColRing;  // TMA ring depth
+};
+constexpr int kStageBarrier = 1;   // named barrier of the 8 compute warps
+
 template <int ROTN, bool RAND, bool SR, bool DUAL, int FMT = kFmtMX4>
 __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads, SR ? 1 : kColMinBlocks)
     mxq_colwise_kernel(
     const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
+    const __grid_constant__ CUtensorMap cmap0, const __grid_constant__ CUtensorMap cmap1,
     const QuantArgs a0, const QuantArgs a1, const QuantArgs ar) {
+    constexpr bool kStaged = !DUAL && FMT != kFmtNVAmax;
+    using S = ColStage<FMT>;
+    constexpr int kColRing = S::kRing;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned base, kept as a shared-space pointer (offset arithmetic
     // only) so that the compiler emits shared-memory loads.
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint8_t *tiles = smem;                                   // kStages x 32 KB
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kTileBytes);
-    uint64_t *empty = full + kStages;
+    uint8_t *tiles = smem;                                   // kColRing x 32 KB
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kColRing * kTileBytes);
+    uint64_t *empty = full + kColRing;
+    uint8_t *staging = smem + kColRing * kTileBytes + 1024;  // kStageBufs x S::kBytes (1 KB aligned)
     __shared__ int abort_flag;
 
     using G = ColTile<ROTN>;
@@ -225,7 +264,7 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads, SR ? 1 
     const int chalf = warp / G::TOKEN_BLOCKS;  // this warp's 64-channel slice of the tile
     const int total = a0.num_tiles + a1.num_tiles;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kColRing; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kThreads / 32);
         }
@@ -233,6 +272,10 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads, SR ? 1 
         fence_barrier_init();
         prefetch_tmap(&map0);
         if (a1.num_tiles > 0) prefetch_tmap(&map1);
+        if (kStaged) {
+            prefetch_tmap(&cmap0);
+            if (a1.num_tiles > 0) prefetch_tmap(&cmap1);
+        }
     }
     __syncthreads();
     griddep_wait();
@@ -248,21 +291,21 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads, SR ? 1 
     };
     if (DUAL) {
         if (threadIdx.x == 0) {
-            for (int s = 0; s < kStages; ++s) {
+            for (int s = 0; s < kColRing; ++s) {
                 const int tile = blockIdx.x + s * gridDim.x;
                 if (tile < total) issue(tile, s);
             }
         }
     } else if (warp == kThreads / 32) {
         // ---- producer warp: stage s of iteration it is refilled once the
-        // compute warps have released its previous use (iteration it - kStages).
+        // compute warps have released its previous use (iteration it - kColRing).
         if (lane == 0) {
             for (int it = 0;; ++it) {
                 const int tile = blockIdx.x + it * gridDim.x;
                 if (tile >= total) break;
-                const int s = it % kStages;
-                if (it >= kStages &&
-                    !mbar_wait(&empty[s], ((it / kStages) - 1) & 1u, a0.status, &abort_flag))
+                const int s = it % kColRing;
+                if (it >= kColRing &&
+                    !mbar_wait(&empty[s], ((it / kColRing) - 1) & 1u, a0.status, &abort_flag))
                     break;
                 issue(tile, s);
             }
@@ -273,8 +316,8 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads, SR ? 1 
     for (int it = 0;; ++it) {
         const int tile = blockIdx.x + it * gridDim.x;
         if (tile >= total) break;
-        const int s = it % kStages;
-        const uint32_t parity = (it / kStages) & 1u;
+        const int s = it % kColRing;
+        const uint32_t parity = (it / kColRing) & 1u;
         const bool second = tile >= a0.num_tiles;
         const int lt = second ? tile - a0.num_tiles : tile;
         const int inner = second ? a1.tiles_inner : a0.tiles_inner;
@@ -293,7 +336,14 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads, SR ? 1 
         int ok = 1;
         if (lane == 0) ok = mbar_wait(&full[s], parity, a0.status, &abort_flag) ? 1 : 0;
         ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-        if (!ok) break;
+        if constexpr (kStaged) {
+            // The staging buffer of this tile was last stored kStageBufs tiles
+            // ago: that store has read it once at most kStageBufs - 1 are pending.
+            if (threadIdx.x == 0) bulk_wait_group_read<kStageBufs - 1>();
+            if (!bar_and(kStageBarrier, kThreads, ok != 0)) break;
+        } else if (!ok) {
+            break;
+        }
 
         // Column pair (64*chalf + 2*lane, +1), tokens 32*tbi .. 32*tbi+31, as
         // 32 register pairs {channel 2*lane, channel 2*lane+1}.
@@ -308,7 +358,7 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads, SR ? 1 
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
         if (DUAL && threadIdx.x == 0) {
-            const int nt = tile + kStages * gridDim.x;
+            const int nt = tile + kColRing * gridDim.x;
             if (nt < total && mbar_wait(&empty[s], parity, a0.status, &abort_flag)) issue(nt, s);
         }
 
@@ -350,6 +400,10 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads, SR ? 1 
             if (lane == 0 && wm != 0u) atomicMax(amax, wm);
             continue;
         }
+        // This tile's staging buffer and the thread's two lines in it.
+        uint8_t *stc = staging + (it % kStageBufs) * S::kBytes;  // codes box
+        uint8_t *sts = stc + S::kCodeBytes;                   // scale atom(s)
+        const int r0 = 64 * chalf + 2 * lane;                 // line of the tile (r0, r0 + 1)
         if constexpr (FMT == kFmtNV4) {
             static_assert(!SR && !DUAL, "NVFP4: round to nearest, one direction");
             const float s_enc = nv_tensor_scale(__uint_as_float(*(second ? a1.amax : a0.amax)));
@@ -361,39 +415,30 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads, SR ? 1 
             const uint32_t f01 = nv_encode_block16(l + 16, s_enc, c01);
             const uint32_t f10 = nv_encode_block16(h, s_enc, c10);
             const uint32_t f11 = nv_encode_block16(h + 16, s_enc, c11);
-            if (tb < L) {
-                uint8_t *d0 = codes + c * (L / 2) + tb / 2, *d1 = codes + (c + 1) * (L / 2) + tb / 2;
-                if (c < lines && MX_STORE_OK(d0, 16, codes, codes_bytes, a0.status))
-                    st_global_16(d0, make_uint4(c00.x, c00.y, c01.x, c01.y));
-                if (c + 1 < lines && MX_STORE_OK(d1, 16, codes, codes_bytes, a0.status))
-                    st_global_16(d1, make_uint4(c10.x, c10.y, c11.x, c11.y));
-            }
-            // Two consecutive scale bytes per line (blocks tb/16 and tb/16 + 1).
-            const int64_t kb = tb / 16;
-            uint8_t *e0 = scales + nv_scale_offset(c, kb, katoms);
-            uint8_t *e1 = scales + nv_scale_offset(c + 1, kb, katoms);
-            if (MX_STORE_OK(e0, 2, scales, scales_bytes, a0.status))
-                *reinterpret_cast<uint16_t *>(e0) = static_cast<uint16_t>(f00 | (f01 << 8));
-            if (MX_STORE_OK(e1, 2, scales, scales_bytes, a0.status))
-                *reinterpret_cast<uint16_t *>(e1) = static_cast<uint16_t>(f10 | (f11 << 8));
-            continue;
-        }
+            // 64-byte swizzle: 16-byte chunk j of line r at j ^ ((r >> 1) & 3).
+            const int sw = tbi ^ ((r0 >> 1) & 3);
+            *reinterpret_cast<uint4 *>(stc + r0 * 64 + sw * 16) = make_uint4(c00.x, c00.y, c01.x, c01.y);
+            *reinterpret_cast<uint4 *>(stc + (r0 + 1) * 64 + sw * 16) =
+                make_uint4(c10.x, c10.y, c11.x, c11.y);
+            // Blocks 2*tbi and 2*tbi + 1 of 16: atom tbi / 2, bytes 2 * (tbi % 2) + {0, 1}.
+            const int so = (tbi / 2) * 512 + 4 * (r0 / 32) + 2 * (tbi % 2);
+            *reinterpret_cast<uint16_t *>(sts + so + (r0 % 32) * 16) =
+                static_cast<uint16_t>(f00 | (f01 << 8));
+            *reinterpret_cast<uint16_t *>(sts + so + ((r0 + 1) % 32) * 16) =
+                static_cast<uint16_t>(f10 | (f11 << 8));
+        } else {
         uint4 q0, q1;
         uint32_t s0, s1;
         if constexpr (FMT == kFmtMX8) {
             static_assert(ROTN == 0 && !RAND && !SR && !DUAL, "MXFP8: plain encode only");
             uint4 p0[2], p1[2];
             encode_pair_e4m3(x, p0, p1, s0, s1);
-            if (tb < L) {
-                uint8_t *d0 = codes + c * L + tb, *d1 = codes + (c + 1) * L + tb;
-                if (c < lines && MX_STORE_OK(d0, 32, codes, codes_bytes, a0.status)) {
-                    st_global_16(d0, p0[0]);
-                    st_global_16(d0 + 16, p0[1]);
-                }
-                if (c + 1 < lines && MX_STORE_OK(d1, 32, codes, codes_bytes, a0.status)) {
-                    st_global_16(d1, p1[0]);
-                    st_global_16(d1 + 16, p1[1]);
-                }
+            // 128-byte lines, 128-byte swizzle: chunk j of line r at j ^ (r & 7).
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                *reinterpret_cast<uint4 *>(stc + r0 * 128 + ((2 * tbi + k) ^ (r0 & 7)) * 16) = p0[k];
+                *reinterpret_cast<uint4 *>(stc + (r0 + 1) * 128 + ((2 * tbi + k) ^ ((r0 + 1) & 7)) * 16) =
+                    p1[k];
             }
         } else {
         if (SR) {
@@ -410,19 +455,54 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads, SR ? 1 
             encode_pair_rne<(ROTN > 0)>(x, ROTN > 0 ? hadamard_norm<ROTN>() : 1.0f, q0, q1, s0, s1);
         }
 
-        if (tb < L) {
-            uint8_t *d0 = codes + c * (L / 2) + tb / 2, *d1 = codes + (c + 1) * (L / 2) + tb / 2;
-            if (c < lines && MX_STORE_OK(d0, 16, codes, codes_bytes, a0.status)) st_global_16(d0, q0);
-            if (c + 1 < lines && MX_STORE_OK(d1, 16, codes, codes_bytes, a0.status))
-                st_global_16(d1, q1);
+        if constexpr (DUAL) {
+            if (tb < L) {
+                uint8_t *d0 = codes + c * (L / 2) + tb / 2, *d1 = codes + (c + 1) * (L / 2) + tb / 2;
+                if (c < lines && MX_STORE_OK(d0, 16, codes, codes_bytes, a0.status))
+                    st_global_16(d0, q0);
+                if (c + 1 < lines && MX_STORE_OK(d1, 16, codes, codes_bytes, a0.status))
+                    st_global_16(d1, q1);
+            }
+            // Scale bytes (padding lines / blocks included: their input is zero).
+            const int64_t kb = tb / 32;
+            uint8_t *e0 = scales + scale_offset(c, kb, katoms);
+            uint8_t *e1 = scales + scale_offset(c + 1, kb, katoms);
+            if (MX_STORE_OK(e0, 1, scales, scales_bytes, a0.status)) *e0 = static_cast<uint8_t>(s0);
+            if (MX_STORE_OK(e1, 1, scales, scales_bytes, a0.status)) *e1 = static_cast<uint8_t>(s1);
+            continue;
         }
+        // 64-byte swizzle: 16-byte chunk j of line r at j ^ ((r >> 1) & 3).
+        const int sw = tbi ^ ((r0 >> 1) & 3);
+        *reinterpret_cast<uint4 *>(stc + r0 * 64 + sw * 16) = q0;
+        *reinterpret_cast<uint4 *>(stc + (r0 + 1) * 64 + sw * 16) = q1;
         }
-        // Scale bytes (padding lines / blocks included: their input is zero).
-        const int64_t kb = tb / 32;
-        uint8_t *e0 = scales + scale_offset(c, kb, katoms), *e1 = scales + scale_offset(c + 1, kb, katoms);
-        if (MX_STORE_OK(e0, 1, scales, scales_bytes, a0.status)) *e0 = static_cast<uint8_t>(s0);
-        if (MX_STORE_OK(e1, 1, scales, scales_bytes, a0.status)) *e1 = static_cast<uint8_t>(s1);
+        // Scale atom: line r, block tbi at (r % 32) * 16 + (r / 32) * 4 + tbi.
+        sts[(r0 % 32) * 16 + 4 * (r0 / 32) + tbi] = static_cast<uint8_t>(s0);
+        sts[((r0 + 1) % 32) * 16 + 4 * (r0 / 32) + tbi] = static_cast<uint8_t>(s1);
+        }
+        (void)c;
+        (void)tb;
+        if constexpr (kStaged) {
+            // Publish the staged tile to the async proxy, then one thread stores
+            // it: the codes box at (token byte t0 / 2 or t0, line c0) -- the TMA
+            // clips lines past `lines` and tokens past L -- and the scale
+            // atom(s) of (line group c0 / 128, tokens t0 .. t0 + 127).
+            fence_proxy_async_smem();
+            asm volatile("bar.sync %0, %1;" ::"n"(kStageBarrier), "n"(kThreads) : "memory");
+            if (threadIdx.x == 0) {
+                tma_store_2d(second ? &cmap1 : &cmap0, stc,
+                             static_cast<int32_t>(FMT == kFmtMX8 ? t0 : t0 / 2),
+                             static_cast<int32_t>(c0));
+                const int64_t atom = (c0 / 128) * katoms + (FMT == kFmtNV4 ? t0 / 64 : t0 / 128);
+                uint8_t *sdst = scales + atom * 512;
+                if (MX_STORE_OK(sdst, S::kScaleBytes, scales, scales_bytes, a0.status))
+                    bulk_store(sdst, sts, S::kScaleBytes);
+                bulk_commit_group();
+            }
+        }
     }
+    // Every store has completed (global writes included) before the CTA leaves.
+    if (kStaged && threadIdx.x == 0) bulk_wait_group_0();
 }
 
 // Column-wise encode for Hadamard sizes 64, 128 and 256.  Each thread owns
@@ -783,10 +863,16 @@ cudaError_t launch_persistent(Kern kernel, int num_tiles, size_t smem, const Dev
 
 struct Operands {
     CUtensorMap map0, map1;
+    CUtensorMap cmap0, cmap1;  // codes outputs (column encodes that stage their tiles)
     QuantArgs a0, a1;
     QuantArgs ar;  // row-direction output of a dual encode
     bool dual = false;
 };
+
+template <int FMT>
+constexpr size_t col_smem() {
+    return ColStage<FMT>::kRing * kTileBytes + 1024 + 1024 + kStageBufs * ColStage<FMT>::kBytes;
+}
 
 template <bool COLWISE, int ROTN, bool RAND>
 cudaError_t launch_rot(bool sr, const Operands &o, const DeviceInfo &dev, cudaStream_t stream) {
@@ -804,19 +890,21 @@ cudaError_t launch_rot(bool sr, const Operands &o, const DeviceInfo &dev, cudaSt
                                       dev, stream, o.map0, o.map1, o.a0, o.a1, o.ar);
     }
     else if constexpr (COLWISE) {
-        const size_t smem = kStages * kTileBytes + 1024 + 1024;
+        const size_t smem = col_smem<kFmtMX4>();
         const int n = o.a0.num_tiles + o.a1.num_tiles;
         if (o.dual)
             return sr ? launch_persistent(mxq_colwise_kernel<ROTN, RAND, true, true>, n, smem, dev,
-                                          stream, o.map0, o.map1, o.a0, o.a1, o.ar)
+                                          stream, o.map0, o.map1, o.cmap0, o.cmap1, o.a0, o.a1,
+                                          o.ar)
                       : launch_persistent(mxq_colwise_kernel<ROTN, RAND, false, true>, n, smem,
-                                          dev, stream, o.map0, o.map1, o.a0, o.a1, o.ar);
+                                          dev, stream, o.map0, o.map1, o.cmap0, o.cmap1, o.a0,
+                                          o.a1, o.ar);
         return sr ? launch_persistent_n(mxq_colwise_kernel<ROTN, RAND, true, false>,
                                         kColProducerThreads, n, smem, dev, stream, o.map0, o.map1,
-                                        o.a0, o.a1, o.ar)
+                                        o.cmap0, o.cmap1, o.a0, o.a1, o.ar)
                   : launch_persistent_n(mxq_colwise_kernel<ROTN, RAND, false, false>,
                                         kColProducerThreads, n, smem, dev, stream, o.map0, o.map1,
-                                        o.a0, o.a1, o.ar);
+                                        o.cmap0, o.cmap1, o.a0, o.a1, o.ar);
     }
     const size_t smem = kStages * kTileBytes + 1024 + 1024;
     return sr ? launch_persistent(mxq_rowwise_kernel<ROTN, RAND, true>, o.a0.num_tiles, smem, dev,
@@ -849,7 +937,8 @@ cudaError_t launch_dir(int rot, int rot_block, bool sr, const Operands &o, const
 // Fills the per-operand arguments (and tensor map) of one encode.
 bool prepare_operand(const void *src, int64_t rows, int64_t cols, bool colwise, int col_tt,
                      uint64_t seed, uint64_t sr_tag, void *codes, void *scales,
-                     const DeviceInfo &dev, CUtensorMap *map, QuantArgs *a, int fmt = kFmtMX4) {
+                     const DeviceInfo &dev, CUtensorMap *map, QuantArgs *a, int fmt = kFmtMX4,
+                     CUtensorMap *cmap = nullptr) {
     *a = QuantArgs{};
     a->L = colwise ? rows : cols;
     a->lines = colwise ? cols : rows;
@@ -873,6 +962,16 @@ bool prepare_operand(const void *src, int64_t rows, int64_t cols, bool colwise, 
         if (line_tiles * k_tiles > 0x3FFFFFFF) return false;
         a->num_tiles = static_cast<int>(line_tiles * k_tiles);
         a->tiles_inner = static_cast<int>(line_tiles);
+        if (cmap != nullptr) {
+            // The staged codes box of a 128-token x 128-line tile: 64 B (128 B
+            // for MXFP8) of each line, swizzled like the staging writes.
+            const bool f8 = fmt == kFmtMX8;
+            const uint64_t row = static_cast<uint64_t>(f8 ? a->L : a->L / 2);
+            if (!encode_tmap_2d(cmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, row,
+                                static_cast<uint64_t>(a->lines), row, f8 ? 128 : 64, 128,
+                                f8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
+                return false;
+        }
         return encode_tmap_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, src, cols, rows, cols * 2,
                               col_tc, col_tt, CU_TENSOR_MAP_SWIZZLE_NONE);
     }
@@ -895,9 +994,10 @@ cudaError_t launch_quantize(const void *src, int64_t rows, int64_t cols, int con
     Operands o;
     const int tt = (rot != 0 && rot_block == 256) ? 256 : 128;
     if (!prepare_operand(src, rows, cols, colwise, tt, seed, sr_tag, codes, scales, dev, &o.map0,
-                         &o.a0))
+                         &o.a0, kFmtMX4, colwise ? &o.cmap0 : nullptr))
         return cudaErrorInvalidValue;
     o.map1 = o.map0;
+    o.cmap1 = o.cmap0;
     o.a1 = QuantArgs{};
     o.ar = QuantArgs{};
     if (colwise) return launch_dir<true>(rot, rot_block, rnd == 1, o, dev, stream);
@@ -912,9 +1012,9 @@ cudaError_t launch_quantize_pair_colwise(const void *src0, int64_t rows0, int64_
     Operands o;
     const int tt = (rot != 0 && rot_block == 256) ? 256 : 128;
     if (!prepare_operand(src0, rows0, cols0, true, tt, seed, 1, codes0, scales0, dev, &o.map0,
-                         &o.a0) ||
+                         &o.a0, kFmtMX4, &o.cmap0) ||
         !prepare_operand(src1, rows1, cols1, true, tt, seed, 2, codes1, scales1, dev, &o.map1,
-                         &o.a1))
+                         &o.a1, kFmtMX4, &o.cmap1))
         return cudaErrorInvalidValue;
     o.ar = QuantArgs{};
     return launch_dir<true>(rot, rot_block, rnd == 1, o, dev, stream);
@@ -930,6 +1030,7 @@ cudaError_t launch_quantize_dual(const void *src, int64_t rows, int64_t cols, in
                          &o.a0))
         return cudaErrorInvalidValue;
     o.map1 = o.map0;
+    o.cmap0 = o.cmap1 = o.map0;   // not read: the dual variant stores its codes directly
     o.a1 = QuantArgs{};
     o.ar = QuantArgs{};
     o.ar.L = cols;
@@ -954,33 +1055,36 @@ cudaError_t launch_quantize_mxfp8_colwise(const void *src0, int64_t rows0, int64
                                           cudaStream_t stream) {
     Operands o;
     if (!prepare_operand(src0, rows0, cols0, true, 128, 0, 1, codes0, scales0, dev, &o.map0,
-                         &o.a0, kFmtMX8))
+                         &o.a0, kFmtMX8, &o.cmap0))
         return cudaErrorInvalidValue;
     o.map1 = o.map0;
+    o.cmap1 = o.cmap0;
     o.a1 = QuantArgs{};
     if (src1 != nullptr &&
         !prepare_operand(src1, rows1, cols1, true, 128, 0, 2, codes1, scales1, dev, &o.map1,
-                         &o.a1, kFmtMX8))
+                         &o.a1, kFmtMX8, &o.cmap1))
         return cudaErrorInvalidValue;
     o.ar = QuantArgs{};
-    const size_t smem = kStages * kTileBytes + 1024 + 1024;
     return launch_persistent_n(mxq_colwise_kernel<0, false, false, false, kFmtMX8>,
-                               kColProducerThreads, o.a0.num_tiles + o.a1.num_tiles, smem, dev,
-                               stream, o.map0, o.map1, o.a0, o.a1, o.ar);
+                               kColProducerThreads, o.a0.num_tiles + o.a1.num_tiles,
+                               col_smem<kFmtMX8>(), dev, stream, o.map0, o.map1, o.cmap0, o.cmap1,
+                               o.a0, o.a1, o.ar);
 }
 
 namespace {
 template <int ROTN, bool RAND>
 cudaError_t launch_nv_passes(const Operands &o, const DeviceInfo &dev, cudaStream_t stream) {
-    const size_t smem = kStages * kTileBytes + 1024 + 1024;
     const int n = o.a0.num_tiles + o.a1.num_tiles;
+    // The amax pass stores nothing: no staging buffers.
     cudaError_t e = launch_persistent_n(mxq_colwise_kernel<ROTN, RAND, false, false, kFmtNVAmax>,
-                                        kColProducerThreads, n, smem, dev, stream, o.map0, o.map1,
-                                        o.a0, o.a1, o.ar);
+                                        kColProducerThreads, n,
+                                        ColStage<kFmtNVAmax>::kRing * kTileBytes + 1024 + 1024,
+                                        dev, stream, o.map0, o.map1, o.cmap0, o.cmap1, o.a0, o.a1,
+                                        o.ar);
     if (e != cudaSuccess) return e;
     return launch_persistent_n(mxq_colwise_kernel<ROTN, RAND, false, false, kFmtNV4>,
-                               kColProducerThreads, n, smem, dev, stream, o.map0, o.map1, o.a0,
-                               o.a1, o.ar);
+                               kColProducerThreads, n, col_smem<kFmtNV4>(), dev, stream, o.map0,
+                               o.map1, o.cmap0, o.cmap1, o.a0, o.a1, o.ar);
 }
 }  // namespace
 
@@ -992,14 +1096,15 @@ cudaError_t launch_quantize_nvfp4_colwise(const void *src0, int64_t rows0, int64
                                           cudaStream_t stream) {
     Operands o;
     if (!prepare_operand(src0, rows0, cols0, true, 128, seed, 1, codes0, scales0, dev, &o.map0,
-                         &o.a0, kFmtNV4))
+                         &o.a0, kFmtNV4, &o.cmap0))
         return cudaErrorInvalidValue;
     o.a0.amax = reinterpret_cast<unsigned int *>(amax);
     o.map1 = o.map0;
+    o.cmap1 = o.cmap0;
     o.a1 = QuantArgs{};
     if (src1 != nullptr) {
         if (!prepare_operand(src1, rows1, cols1, true, 128, seed, 2, codes1, scales1, dev, &o.map1,
-                             &o.a1, kFmtNV4))
+                             &o.a1, kFmtNV4, &o.cmap1))
             return cudaErrorInvalidValue;
         o.a1.amax = reinterpret_cast<unsigned int *>(amax + 1);
     }
