@@ -857,6 +857,7 @@ def run_sweep(args):
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     peaks, _ = load_peaks()
     fp4_peak = peaks["bf16_tflops"] * NOMINAL_FP4_OVER_BF16
+    fp4_meas = measure_fp4_peak(mx)["tflops"]
     reps = args.sweep_reps
 
     def timed(fn):
@@ -948,6 +949,7 @@ def run_sweep(args):
               "quantizer_frac_hbm": qbytes / (t_q * 1e-3) / 1e9 / peaks["hbm_gbs"],
               "gemm_tflops": flops / (t_g * 1e-3) / 1e12,
               "gemm_frac_fp4": flops / (t_g * 1e-3) / 1e12 / fp4_peak,
+              "gemm_frac_fp4_measured": flops / (t_g * 1e-3) / 1e12 / fp4_meas,
               "tflops_incl_quant": flops / ((t_q + t_g) * 1e-3) / 1e12})
 
     # cuBLAS bf16 GEMM of the same Wgrad shapes (context only, not the path)

@@ -421,6 +421,39 @@ __device__ __forceinline__ int64_t nv_scale_offset(int64_t line, int64_t block, 
            (block % 4);
 }
 
+// Stochastic-rounding encode of one block of 32 that draws its randomness 8
+// elements at a time (one Philox call per 8, in the order of sr_draws32), so
+// that only 8 draws are live at once: the same codes as encode_block32<true>
+// fed by sr_draws32(seed, tag, e0, u).
+__device__ __forceinline__ uint32_t encode_block32_sr(const float (&r)[32], uint4 &q,
+                                                      uint64_t seed, uint64_t tag, uint64_t e0) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) m = max(m, __float_as_uint(r[i]) & 0x7FFFFFFFu);
+    if (m >= 0x7F800000u) {  // Inf or NaN in the block: NaN scale, zero codes
+        q = make_uint4(0, 0, 0, 0);
+        return 0xFFu;
+    }
+    const uint32_t e = m >> 23;
+    const uint32_t sb = e >= 2u ? e - 2u : 0u;            // floor(log2 amax) - 2 + 127, >= 0
+    const float inv = __uint_as_float((254u - sb) << 23);  // 2^(127 - sb), exact
+    uint32_t w[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        uint64_t o[4];
+        philox4x64_10(e0 / 8 + g, seed, tag, o);
+        uint32_t word = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t u24 = static_cast<uint32_t>(o[k / 2] >> (32 * (k % 2))) >> 8;
+            word |= e2m1_sr_code(__fmul_rn(r[8 * g + k], inv), u24) << (4 * k);
+        }
+        w[g] = word;
+    }
+    q = make_uint4(w[0], w[1], w[2], w[3]);
+    return sb;
+}
+
 __device__ __forceinline__ void st_global_16(void *p, uint4 v) {
     asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
                  "r"(v.z), "r"(v.w)

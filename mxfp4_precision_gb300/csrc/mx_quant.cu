@@ -63,6 +63,10 @@ constexpr int kStageBufs = MXQ_STAGE_BUFS;  // its output staging buffers
 // the round-to-nearest colwise kernels are held to 128 registers so that the
 // random-sign variants do not fall to one CTA per SM.
 constexpr int kColMinBlocks = 2;
+#ifndef MXQ_SR_MINB
+#define MXQ_SR_MINB 1
+#endif
+constexpr int kColSRMinBlocks = MXQ_SR_MINB;  // stochastic rounding (see the SR encode)
 constexpr int kThreads = 256;           // compute threads (8 warps)
 constexpr int kColProducerThreads = kThreads + 32;  // + a TMA producer warp
 constexpr uint32_t kTileBytes = 32768;  // one staged bf16 tile (128 x 128, 256 x 64 or 64 x 256)
@@ -240,7 +244,8 @@ struct ColStage {
 constexpr int kStageBarrier = 1;   // named barrier of the 8 compute warps
 
 template <int ROTN, bool RAND, bool SR, bool DUAL, int FMT = kFmtMX4>
-__global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads, SR ? 1 : kColMinBlocks)
+__global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads,
+                                  SR ? (DUAL ? 1 : kColSRMinBlocks) : kColMinBlocks)
     mxq_colwise_kernel(
     const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
     const __grid_constant__ CUtensorMap cmap0, const __grid_constant__ CUtensorMap cmap1,
@@ -255,6 +260,10 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads, SR ? 1 
     uint8_t *tiles = smem;                                   // kColRing x 32 KB
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kColRing * kTileBytes);
     uint64_t *empty = full + kColRing;
+    // Random-sign words of each stage's tile (4 x 32 tokens), written by the
+    // thread that issues the stage's load before it arms the stage barrier:
+    // one Philox call per tile instead of one per warp.
+    uint32_t *signw = reinterpret_cast<uint32_t *>(empty + kColRing);
     uint8_t *staging = smem + kColRing * kTileBytes + 1024;  // kStageBufs x S::kBytes (1 KB aligned)
     __shared__ int abort_flag;
 
@@ -285,6 +294,16 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads, SR ? 1 
         const bool second = tile >= a0.num_tiles;
         const int lt = second ? tile - a0.num_tiles : tile;
         const int inner = second ? a1.tiles_inner : a0.tiles_inner;
+        if constexpr (RAND) {
+            const int64_t t0 = static_cast<int64_t>(lt / inner) * G::TT;
+            uint64_t o[4];
+            philox4x64_10(static_cast<uint64_t>(t0 / 256), a0.seed, 0, o);
+#pragma unroll
+            for (int k = 0; k < G::TOKEN_BLOCKS; ++k) {
+                const int chunk = static_cast<int>((t0 % 256) / 32) + k;
+                signw[s * G::TOKEN_BLOCKS + k] = static_cast<uint32_t>(o[chunk / 2] >> (32 * (chunk % 2)));
+            }
+        }
         mbar_arrive_expect_tx(&full[s], kTileBytes);
         tma_load_2d(tiles + s * kTileBytes, second ? &map1 : &map0, &full[s], (lt % inner) * G::TC,
                     (lt / inner) * G::TT);
@@ -354,6 +373,7 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads, SR ? 1 
             const uint32_t v = tw[(tbi * 32 + i) * (G::TC / 2) + chalf * 32 + lane];
             x[i] = pack2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
         }
+        const uint32_t sbits = RAND ? signw[s * G::TOKEN_BLOCKS + tbi] : 0u;
         if (DUAL) dual_rows<G::TC, SR>(tw, t0, c0, a0, ar);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
@@ -364,11 +384,9 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads, SR ? 1 
 
         if (ROTN > 0) {
             if (RAND) {
-                const uint32_t bits = sign_bits32(a0.seed, static_cast<uint64_t>(t0 / 256),
-                                                  static_cast<int>((t0 % 256) / 32) + tbi);
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
-                    x[i] ^= ((bits >> i) & 1u) ? 0x8000000080000000ull : 0ull;
+                    x[i] ^= ((sbits >> i) & 1u) ? 0x8000000080000000ull : 0ull;
             }
             fwht_pairs<ROTN>(x);
             if (SR || FMT >= kFmtNVAmax) {  // MXFP4 RNE folds the factor into its scale multiply
@@ -446,11 +464,8 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads, SR ? 1 
             float x0[32], x1[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) unpack2(x[i], x0[i], x1[i]);
-            uint32_t u[32];
-            sr_draws32(a0.seed, tag, static_cast<uint64_t>(c * L + tb), u);
-            s0 = encode_block32<true>(x0, q0, u);
-            sr_draws32(a0.seed, tag, static_cast<uint64_t>((c + 1) * L + tb), u);
-            s1 = encode_block32<true>(x1, q1, u);
+            s0 = encode_block32_sr(x0, q0, a0.seed, tag, static_cast<uint64_t>(c * L + tb));
+            s1 = encode_block32_sr(x1, q1, a0.seed, tag, static_cast<uint64_t>((c + 1) * L + tb));
         } else {
             encode_pair_rne<(ROTN > 0)>(x, ROTN > 0 ? hadamard_norm<ROTN>() : 1.0f, q0, q1, s0, s1);
         }
