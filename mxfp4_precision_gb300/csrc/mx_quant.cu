@@ -191,6 +191,45 @@ __device__ __forceinline__ void dual_rows(const uint32_t *tw, int64_t t0, int64_
     }
 }
 
+// The same row-direction encode for the staged column kernel (TC = 128): the
+// codes go to the row image's [128 tokens][64 B] box (64-byte swizzle) and the
+// scale bytes to its 512-byte atom (tokens t0 .. t0+127, channel atom c0/128);
+// only the padding blocks past the last channel tile, which no tile's atom
+// covers, are stored directly.
+template <bool SR>
+__device__ __forceinline__ void dual_rows_staged(const uint32_t *tw, int64_t t0, int64_t c0,
+                                                 const QuantArgs &a0, const QuantArgs &ar,
+                                                 uint8_t *rc, uint8_t *rs) {
+    constexpr int TC = 128;
+    const int64_t row_lines_pad = (ar.lines + 127) / 128 * 128;
+    const int64_t grid_end = (a0.lines + 127) / 128 * 128;  // channels the tiles cover
+    const int64_t kb_pad = ar.katoms * 4;                    // padded blocks per row
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int b = threadIdx.x + kThreads * h;
+        const int trow = b / (TC / 32), cb = b % (TC / 32);
+        const int64_t t = t0 + trow;
+        const int64_t c = c0 + 32 * cb;
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int jj = (j + trow) & 3;
+            const uint4 v = *reinterpret_cast<const uint4 *>(tw + trow * (TC / 2) + 16 * cb + 4 * jj);
+            w[4 * jj] = v.x, w[4 * jj + 1] = v.y, w[4 * jj + 2] = v.z, w[4 * jj + 3] = v.w;
+        }
+        uint4 q;
+        const uint32_t sb =
+            encode_row_block<SR>(w, q, a0.seed, ar.sr_tag, static_cast<uint64_t>(t * ar.L + c));
+        *reinterpret_cast<uint4 *>(rc + trow * 64 + ((cb ^ ((trow >> 1) & 3)) * 16)) = q;
+        rs[(trow % 32) * 16 + (trow / 32) * 4 + cb] = static_cast<uint8_t>(sb);
+        if (c0 + TC == grid_end && t < row_lines_pad) {
+            const int64_t pb = grid_end / 32 + cb;
+            uint8_t *pdst = ar.scales + scale_offset(t, pb, ar.katoms);
+            if (pb < kb_pad && MX_STORE_OK(pdst, 1, ar.scales, ar.scales_bytes, ar.status))
+                *pdst = 0;
+        }
+    }
+}
 
 // Column-wise encode for no rotation and Hadamard sizes 16 and 32.  One
 // launch encodes up to two operands (the two Wgrad operands): tiles
@@ -250,9 +289,12 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads,
     const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
     const __grid_constant__ CUtensorMap cmap0, const __grid_constant__ CUtensorMap cmap1,
     const QuantArgs a0, const QuantArgs a1, const QuantArgs ar) {
-    constexpr bool kStaged = !DUAL && FMT != kFmtNVAmax;
+    constexpr bool kStaged = FMT != kFmtNVAmax;
     using S = ColStage<FMT>;
-    constexpr int kColRing = S::kRing;
+    // The dual variant stages two images (column and row direction) and
+    // keeps a 2-deep ring so that two CTAs still fit.
+    constexpr int kColRing = DUAL ? 2 : S::kRing;
+    constexpr int kImages = DUAL ? 2 : 1;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned base, kept as a shared-space pointer (offset arithmetic
     // only) so that the compiler emits shared-memory loads.
@@ -264,7 +306,7 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads,
     // thread that issues the stage's load before it arms the stage barrier:
     // one Philox call per tile instead of one per warp.
     uint32_t *signw = reinterpret_cast<uint32_t *>(empty + kColRing);
-    uint8_t *staging = smem + kColRing * kTileBytes + 1024;  // kStageBufs x S::kBytes (1 KB aligned)
+    uint8_t *staging = smem + kColRing * kTileBytes + 1024;  // kStageBufs x kImages x S::kBytes
     __shared__ int abort_flag;
 
     using G = ColTile<ROTN>;
@@ -349,6 +391,8 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads,
         const size_t scales_bytes = second ? a1.scales_bytes : a0.scales_bytes;
         (void)codes_bytes;
         (void)scales_bytes;
+        (void)lines;
+        (void)codes;
         const int64_t t0 = static_cast<int64_t>(lt / inner) * G::TT;
         const int64_t c0 = static_cast<int64_t>(lt % inner) * G::TC;
 
@@ -374,7 +418,12 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads,
             x[i] = pack2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
         }
         const uint32_t sbits = RAND ? signw[s * G::TOKEN_BLOCKS + tbi] : 0u;
-        if (DUAL) dual_rows<G::TC, SR>(tw, t0, c0, a0, ar);
+        // This tile's staging buffer: the column image (codes box, scale
+        // atoms), then with DUAL the row image.
+        uint8_t *stc = staging + (it % kStageBufs) * kImages * S::kBytes;
+        uint8_t *sts = stc + S::kCodeBytes;
+        if constexpr (DUAL)
+            dual_rows_staged<SR>(tw, t0, c0, a0, ar, stc + S::kBytes, stc + S::kBytes + S::kCodeBytes);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
         if (DUAL && threadIdx.x == 0) {
@@ -418,9 +467,6 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads,
             if (lane == 0 && wm != 0u) atomicMax(amax, wm);
             continue;
         }
-        // This tile's staging buffer and the thread's two lines in it.
-        uint8_t *stc = staging + (it % kStageBufs) * S::kBytes;  // codes box
-        uint8_t *sts = stc + S::kCodeBytes;                   // scale atom(s)
         const int r0 = 64 * chalf + 2 * lane;                 // line of the tile (r0, r0 + 1)
         if constexpr (FMT == kFmtNV4) {
             static_assert(!SR && !DUAL, "NVFP4: round to nearest, one direction");
@@ -470,22 +516,6 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads,
             encode_pair_rne<(ROTN > 0)>(x, ROTN > 0 ? hadamard_norm<ROTN>() : 1.0f, q0, q1, s0, s1);
         }
 
-        if constexpr (DUAL) {
-            if (tb < L) {
-                uint8_t *d0 = codes + c * (L / 2) + tb / 2, *d1 = codes + (c + 1) * (L / 2) + tb / 2;
-                if (c < lines && MX_STORE_OK(d0, 16, codes, codes_bytes, a0.status))
-                    st_global_16(d0, q0);
-                if (c + 1 < lines && MX_STORE_OK(d1, 16, codes, codes_bytes, a0.status))
-                    st_global_16(d1, q1);
-            }
-            // Scale bytes (padding lines / blocks included: their input is zero).
-            const int64_t kb = tb / 32;
-            uint8_t *e0 = scales + scale_offset(c, kb, katoms);
-            uint8_t *e1 = scales + scale_offset(c + 1, kb, katoms);
-            if (MX_STORE_OK(e0, 1, scales, scales_bytes, a0.status)) *e0 = static_cast<uint8_t>(s0);
-            if (MX_STORE_OK(e1, 1, scales, scales_bytes, a0.status)) *e1 = static_cast<uint8_t>(s1);
-            continue;
-        }
         // 64-byte swizzle: 16-byte chunk j of line r at j ^ ((r >> 1) & 3).
         const int sw = tbi ^ ((r0 >> 1) & 3);
         *reinterpret_cast<uint4 *>(stc + r0 * 64 + sw * 16) = q0;
@@ -512,6 +542,19 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads,
                 uint8_t *sdst = scales + atom * 512;
                 if (MX_STORE_OK(sdst, S::kScaleBytes, scales, scales_bytes, a0.status))
                     bulk_store(sdst, sts, S::kScaleBytes);
+                if constexpr (DUAL) {
+                    // The row image: tokens t0 .. t0+127 as lines, channels as
+                    // the contraction (box at channel byte c0 / 2, line t0;
+                    // cmap1 maps the row codes).  Tiles past the last 128-token
+                    // scale group only hold padding rows.
+                    if (t0 < (ar.lines + 127) / 128 * 128) {
+                        tma_store_2d(&cmap1, stc + S::kBytes, static_cast<int32_t>(c0 / 2),
+                                     static_cast<int32_t>(t0));
+                        uint8_t *rdst = ar.scales + ((t0 / 128) * ar.katoms + c0 / 128) * 512;
+                        if (MX_STORE_OK(rdst, 512, ar.scales, ar.scales_bytes, a0.status))
+                            bulk_store(rdst, stc + S::kBytes + S::kCodeBytes, 512);
+                    }
+                }
                 bulk_commit_group();
             }
         }
@@ -884,9 +927,10 @@ struct Operands {
     bool dual = false;
 };
 
-template <int FMT>
+template <int FMT, bool DUAL = false>
 constexpr size_t col_smem() {
-    return ColStage<FMT>::kRing * kTileBytes + 1024 + 1024 + kStageBufs * ColStage<FMT>::kBytes;
+    return (DUAL ? 2 : ColStage<FMT>::kRing) * kTileBytes + 1024 + 1024 +
+           kStageBufs * (DUAL ? 2 : 1) * ColStage<FMT>::kBytes;
 }
 
 template <bool COLWISE, int ROTN, bool RAND>
@@ -906,12 +950,13 @@ cudaError_t launch_rot(bool sr, const Operands &o, const DeviceInfo &dev, cudaSt
     }
     else if constexpr (COLWISE) {
         const size_t smem = col_smem<kFmtMX4>();
+        const size_t dsmem = col_smem<kFmtMX4, true>();
         const int n = o.a0.num_tiles + o.a1.num_tiles;
         if (o.dual)
-            return sr ? launch_persistent(mxq_colwise_kernel<ROTN, RAND, true, true>, n, smem, dev,
-                                          stream, o.map0, o.map1, o.cmap0, o.cmap1, o.a0, o.a1,
-                                          o.ar)
-                      : launch_persistent(mxq_colwise_kernel<ROTN, RAND, false, true>, n, smem,
+            return sr ? launch_persistent(mxq_colwise_kernel<ROTN, RAND, true, true>, n, dsmem,
+                                          dev, stream, o.map0, o.map1, o.cmap0, o.cmap1, o.a0,
+                                          o.a1, o.ar)
+                      : launch_persistent(mxq_colwise_kernel<ROTN, RAND, false, true>, n, dsmem,
                                           dev, stream, o.map0, o.map1, o.cmap0, o.cmap1, o.a0,
                                           o.a1, o.ar);
         return sr ? launch_persistent_n(mxq_colwise_kernel<ROTN, RAND, true, false>,
@@ -1042,10 +1087,15 @@ cudaError_t launch_quantize_dual(const void *src, int64_t rows, int64_t cols, in
     Operands o;
     const int tt = (rot != 0 && rot_block == 256) ? 256 : 128;
     if (!prepare_operand(src, rows, cols, true, tt, seed, 1, codes_t, scales_t, dev, &o.map0,
-                         &o.a0))
+                         &o.a0, kFmtMX4, &o.cmap0))
         return cudaErrorInvalidValue;
     o.map1 = o.map0;
-    o.cmap0 = o.cmap1 = o.map0;   // not read: the dual variant stores its codes directly
+    // The column kernel's dual variant has no second operand: cmap1 maps the
+    // row-direction codes [rows][cols / 2] in 128-token x 64-byte boxes.
+    if (!encode_tmap_2d(&o.cmap1, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes_n,
+                        static_cast<uint64_t>(cols / 2), static_cast<uint64_t>(rows),
+                        static_cast<uint64_t>(cols / 2), 64, 128, CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
     o.a1 = QuantArgs{};
     o.ar = QuantArgs{};
     o.ar.L = cols;
