@@ -952,6 +952,27 @@ def run_sweep(args):
               "gemm_frac_fp4_measured": flops / (t_g * 1e-3) / 1e12 / fp4_meas,
               "tflops_incl_quant": flops / ((t_q + t_g) * 1e-3) / 1e12})
 
+    # cuBLASLt's block-scaled FP4 GEMM on the same encoded operands (context only, not the
+    # path; optional: reported as unavailable where this torch build does not take FP4)
+    quant(mx.ROT_HADAMARD_DET, 32, mx.ROUND_RNE, 0)
+    gemm()
+    try:
+        fa = aq.view(torch.float4_e2m1fn_x2).view(N, T // 2)
+        fb = bq.view(torch.float4_e2m1fn_x2).view(K, T // 2)
+        sa, sb = as_.view(torch.float8_e8m0fnu), bs.view(torch.float8_e8m0fnu)
+        lib_mm = lambda: torch._scaled_mm(fa, fb.t(), sa, sb, out_dtype=torch.bfloat16)
+        ref = lib_mm().float()
+        torch.cuda.synchronize(dev)
+        rel = float((ref - dW).norm() / dW.norm())
+        t_l = timed(lib_mm)
+        emit({"sweep": "cublaslt_mxfp4_reference", "workload": f"down_proj Wgrad T={T} N={N} K={K}",
+              "call": "torch._scaled_mm(float4_e2m1fn_x2, float8_e8m0fnu scales), bf16 out",
+              "ms": t_l, "tflops": flops / (t_l * 1e-3) / 1e12,
+              "rel_diff_vs_mx_gemm": rel,
+              "note": "same codes and tiled scales as mx_gemm; its output rounds to bf16"})
+    except Exception as e:                       # not offered by this torch / cuBLASLt
+        emit({"sweep": "cublaslt_mxfp4_reference", "unavailable": f"{type(e).__name__}: {e}"[:300]})
+
     # cuBLAS bf16 GEMM of the same Wgrad shapes (context only, not the path)
     for wl, (tt, nn, kk) in (("o_proj", (8192, 4096, 4096)), ("down_proj", (T, N, K))):
         a = dY.view(torch.bfloat16)[:tt, :nn]
@@ -993,6 +1014,35 @@ def run_sweep(args):
             del ws, out
     emit({"sweep": "qkv_gateup", "op": "all six", "ms": total_ms,
           "gflop": total_flops / 1e9, "tflops_incl_quant": total_flops / (total_ms * 1e-3) / 1e12})
+    del t4
+    torch.cuda.empty_cache()
+
+    # ---- the oracle at full size on this host (a reported baseline, not the target):
+    # its encode single-threaded, its double GEMM partitioned by output columns over
+    # every host core (the oracle's C calls release the GIL; arithmetic unchanged)
+    from concurrent.futures import ThreadPoolExecutor
+    cores = host_cores()
+    for name in ("tiny", "o_proj", "down_proj"):
+        cfg, T_, N_, K_ = ("tiny", 256, 128, 256) if name == "tiny" else WORKLOADS[name]
+        dd = config_inputs(cfg, seed=0, only=("dY", "X"))
+        t0 = time.perf_counter()
+        Aq, As = oracle.quantize(dd["dY"], oracle.CONTRACT_ROWS, oracle.ROT_HADAMARD_DET, 32,
+                                 oracle.ROUND_RNE, 0, 1)
+        Bq, Bs = oracle.quantize(dd["X"], oracle.CONTRACT_ROWS, oracle.ROT_HADAMARD_DET, 32,
+                                 oracle.ROUND_RNE, 0, 2)
+        tq = time.perf_counter() - t0
+        edges = np.linspace(0, K_, max(1, min(cores, K_ // 8)) + 1).astype(int)
+        t0 = time.perf_counter()
+        with ThreadPoolExecutor(len(edges) - 1) as ex:
+            list(ex.map(lambda i: oracle.gemm(Aq, As, Bq[edges[i]:edges[i + 1]],
+                                              Bs[edges[i]:edges[i + 1]]), range(len(edges) - 1)))
+        tg = time.perf_counter() - t0
+        fl = 2.0 * N_ * K_ * T_
+        emit({"sweep": "oracle_full_size", "workload": f"{name} Wgrad T={T_} N={N_} K={K_}, "
+              "deterministic Hadamard 32, RNE", "encode_s_one_core": tq,
+              "gemm_s": tg, "gemm_threads": len(edges) - 1, "host_cores": cores,
+              "tflops_incl_encode": fl / (tq + tg) / 1e12})
+        del dd, Aq, As, Bq, Bs
     return 0
 
 
