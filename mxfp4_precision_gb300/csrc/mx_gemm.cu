@@ -177,7 +177,10 @@ struct SharedCtl {
 
 // Tile order: bands of kBand tile rows, column by column within a band, so
 // that the tiles in flight at once share few A and B panels (L2 reuse).
-constexpr int kBand = 8;
+#ifndef MXG_BAND
+#define MXG_BAND 8
+#endif
+constexpr int kBand = MXG_BAND;
 __device__ __forceinline__ void tile_coords(const GemmArgs &g, int t, int &mb, int &nb) {
     const int per_band = kBand * g.n_tiles;
     const int band = t / per_band, r = t % per_band;

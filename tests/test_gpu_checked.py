@@ -32,6 +32,15 @@ def libs():
         L.mx_check_status.argtypes = [P]
         L.mx_scales_bytes.argtypes = [i64, i64]
         L.mx_scales_bytes.restype = sz
+        L.mx_quantize_mxfp8.argtypes = [P, i64, i64, P, P, P]
+        L.mx_gemm_mxfp8.argtypes = [P, P, P, P, P, i64, i64, i64, P]
+        L.mx_quantize_nvfp4.argtypes = [P, i64, i64, i32, i32, u64, P, P, P, P]
+        L.mx_gemm_nvfp4.argtypes = [P, P, P, P, P, P, P, i64, i64, i64, P]
+        L.mx_nvfp4_scales_bytes.argtypes = [i64, i64]
+        L.mx_nvfp4_scales_bytes.restype = sz
+        L.mx_linear_workspace_bytes.argtypes = [i32, i64, i64, i64]
+        L.mx_linear_workspace_bytes.restype = sz
+        L.mx_linear_wgrad_fused.argtypes = [P, P, P, i64, i64, i64, i32, i32, i32, u64, P, sz, P]
     return normal, checked
 
 
@@ -113,3 +122,53 @@ def test_checked_gemm_stays_in_bounds(libs, M, N, K):
         assert L.mx_check_status(None) == 0
         outs.append(C.cpu().numpy())
     assert np.array_equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 136, 800), (136, 392, 288), (384, 256, 1056)])
+def test_checked_mxfp8_and_nvfp4_stay_in_bounds(libs, M, N, K):
+    """The FP8 comparator's and the NVFP4 variant's encoders (staged tile
+    stores, the NVFP4 amax pass) and GEMMs, with exact-size buffers."""
+    a, b = _bits((K, M), 7), _bits((K, N), 8)
+    outs = []
+    for L in libs:
+        got = []
+        # MXFP8: one code byte per element
+        a8 = [_buf(M * K), _buf(L.mx_scales_bytes(M, K))]
+        b8 = [_buf(N * K), _buf(L.mx_scales_bytes(N, K))]
+        assert L.mx_quantize_mxfp8(a.data_ptr(), K, M, a8[0].data_ptr(), a8[1].data_ptr(), None) == 0
+        assert L.mx_quantize_mxfp8(b.data_ptr(), K, N, b8[0].data_ptr(), b8[1].data_ptr(), None) == 0
+        C8 = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        assert L.mx_gemm_mxfp8(a8[0].data_ptr(), a8[1].data_ptr(), b8[0].data_ptr(),
+                               b8[1].data_ptr(), C8.data_ptr(), M, N, K, None) == 0
+        # NVFP4 with a deterministic Hadamard 16
+        amax = torch.zeros(4, dtype=torch.float32, device="cuda")
+        a4 = [_buf(M * K // 2), _buf(L.mx_nvfp4_scales_bytes(M, K))]
+        b4 = [_buf(N * K // 2), _buf(L.mx_nvfp4_scales_bytes(N, K))]
+        assert L.mx_quantize_nvfp4(a.data_ptr(), K, M, 1, 16, 0, a4[0].data_ptr(),
+                                   a4[1].data_ptr(), amax.data_ptr(), None) == 0
+        assert L.mx_quantize_nvfp4(b.data_ptr(), K, N, 1, 16, 0, b4[0].data_ptr(),
+                                   b4[1].data_ptr(), amax.data_ptr() + 8, None) == 0
+        C4 = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        assert L.mx_gemm_nvfp4(a4[0].data_ptr(), a4[1].data_ptr(), amax.data_ptr(),
+                               b4[0].data_ptr(), b4[1].data_ptr(), amax.data_ptr() + 8,
+                               C4.data_ptr(), M, N, K, None) == 0
+        assert L.mx_check_status(None) == 0
+        outs.append([t.cpu().numpy() for t in (*a8, *b8, C8, *a4, *b4, C4, amax)])
+    for u, v in zip(*outs):
+        assert np.array_equal(u, v)
+
+
+def test_checked_fused_wgrad_stays_in_bounds(libs):
+    """The one-launch Wgrad (encoder warps inside the GEMM) on several panel groups."""
+    T, N, K = 1024, 768, 512
+    dy, x = _bits((T, N), 9), _bits((T, K), 10)
+    outs = []
+    for L in libs:
+        need = L.mx_linear_workspace_bytes(2, T, N, K)       # MX_OP_WGRAD
+        ws = _buf(need)
+        dW = torch.empty((N, K), dtype=torch.float32, device="cuda")
+        assert L.mx_linear_wgrad_fused(dy.data_ptr(), x.data_ptr(), dW.data_ptr(), T, N, K, 1, 32,
+                                       0, 0, ws.data_ptr(), need, None) == 0
+        assert L.mx_check_status(None) == 0
+        outs.append(dW.cpu().numpy())
+    assert np.array_equal(outs[0].view(np.int32), outs[1].view(np.int32))

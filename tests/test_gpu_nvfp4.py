@@ -134,3 +134,30 @@ def test_wgrad_full_size_sampled(name):
     B = oracle.quantize_nvfp4(X, oracle.CONTRACT_ROWS, oracle.ROT_HADAMARD_DET, 16, lines=jb)
     Cref, Cabs = oracle.gemm(A[0], A[1], B[0], B[1], oracle.FMT_NVFP4, A[3], B[3])
     assert_gemm_close(out.cpu().numpy()[np.ix_(ia, jb)], Cref, Cabs, f"{name} nvfp4 wgrad")
+
+
+@pytest.mark.slow
+def test_encode_every_line_o_proj_operand():
+    """Every code and scale byte of the o_proj dY operand (8192 x 4096,
+    Hadamard 16), the oracle partitioned by lines over the host cores (each
+    call takes the tensor amax over every line, then encodes its share)."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    dY = config_inputs("o_proj", only=("dY",))["dY"]
+    T, N = dY.shape
+    codes, scales, amax = mx.quantize_nvfp4(_dev(dY), mx.ROT_HADAMARD_DET, 16, 0)
+    mx.check_status()
+    parts = max(1, min(os.cpu_count() or 1, 32))
+    edges = np.linspace(0, N, parts + 1).astype(int)
+
+    def one(i):
+        return oracle.quantize_nvfp4(dY, oracle.CONTRACT_ROWS, oracle.ROT_HADAMARD_DET, 16,
+                                     lines=np.arange(edges[i], edges[i + 1]))
+    with ThreadPoolExecutor(parts) as ex:
+        res = list(ex.map(one, range(parts)))
+    assert float(amax.item()) == res[0][2]
+    ref_c = np.concatenate([r[0] for r in res])
+    ref_s = np.concatenate([r[1] for r in res])
+    assert np.array_equal(codes.cpu().numpy(), ref_c)
+    tiled = scales.cpu().numpy()[:mx.nvfp4_scales_bytes(N, T)]
+    assert np.array_equal(tiled, tile_scales_nv(ref_s, N, T))
