@@ -8,17 +8,21 @@
 // minus 2, the largest E2M1 exponent) and each element is rounded to E2M1
 // (nearest-even, or stochastically) and packed two per byte.
 //
-// Three kernels, all persistent with a 2-deep ring of 32 KB TMA tiles (up to
-// two resident CTAs per SM):
+// Three kernels, all persistent with a ring of 32 KB TMA tiles (3 deep for the
+// column kernel, 2 for the others; two resident CTAs per SM):
 //   mxq_colwise       contraction down the rows of src[T][C] (Wgrad operands,
 //                     Dgrad's W), no rotation or Hadamard 16/32: a 128-token
 //                     x 128-channel tile; each thread owns 2 adjacent
 //                     channels x 32 tokens as packed f32x2 pairs, so the
 //                     transpose is free (it reads a column pair from shared
 //                     memory) and the Hadamard and the block amax stay in
-//                     registers.  A ninth warp refills the ring.  With DUAL
-//                     it also encodes the staged tile along the channels
-//                     (the Dgrad encoding of the same dY).
+//                     registers.  A ninth warp refills the ring.  Outputs
+//                     leave through a shared-memory staging image (one TMA
+//                     box of codes, one bulk copy of the scale atom per
+//                     tile).  With DUAL it also encodes the staged tile
+//                     along the channels (the Dgrad encoding of the same
+//                     dY); with other element formats it writes MXFP8 or
+//                     NVFP4 instead.
 //   mxq_colwise_wide  the same direction for Hadamard 64/128/256 (128 x 128
 //                     tiles, 256 x 64 for 256): each thread owns one
 //                     channel x 64 tokens as pairs {t, t+32}; the
@@ -234,10 +238,10 @@ __device__ __forceinline__ void dual_rows_staged(const uint32_t *tw, int64_t t0,
 // Column-wise encode for no rotation and Hadamard sizes 16 and 32.  One
 // launch encodes up to two operands (the two Wgrad operands): tiles
 // [0, a0.num_tiles) belong to operand 0, the rest to operand 1.  Every warp
-// works on its own 32-token slice of the tile, so no CTA-wide barrier is taken
-// inside the loop: each warp marks the stage consumed on an mbarrier, and the
-// stage is refilled once all eight have.  Tile: 128 tokens x 128 channels of
-// bf16 (32 KB, 256-byte contiguous row segments).
+// works on its own 32-token slice of the tile and marks the stage consumed on
+// an mbarrier as soon as it holds its values; the stage is refilled once all
+// eight have.  Tile: 128 tokens x 128 channels of bf16 (32 KB, 256-byte
+// contiguous row segments).
 template <int ROTN>
 struct ColTile {
     static_assert(ROTN <= 32, "larger Hadamard sizes use mxq_colwise_wide_kernel");
@@ -250,9 +254,9 @@ struct ColTile {
 // row-direction encoding (blocks of 32 along the channels, no rotation) to
 // `ar`, from the same staged tiles: one HBM read serves both encodings.
 // Without DUAL, a ninth warp is the TMA producer: it refills each stage once
-// all eight compute warps have released it, so no compute warp waits for the
-// slowest one.  (The dual variant keeps its registers for the row encode and
-// refills from thread 0 instead.)
+// all eight compute warps have released it.  (The dual variant keeps its
+// registers for the row encode and refills from thread 0 instead.)
+//
 // Element formats of the column encoder: MXFP4; MXFP8 (the FP8 comparator:
 // no rotation, round to nearest; each block becomes 32 E4M3 code bytes under
 // the same E8M0 scale layout); and the two passes of NVFP4 (the tensor amax
