@@ -378,6 +378,7 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads,
         return;
     }
 
+    float amax_run0 = 0.0f, amax_run1 = 0.0f;  // NVFP4 amax pass: running maxima per operand
     for (int it = 0;; ++it) {
         const int tile = blockIdx.x + it * gridDim.x;
         if (tile >= total) break;
@@ -454,9 +455,11 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads,
         const int64_t c = c0 + 64 * chalf + 2 * lane;  // first of the thread's two channels
         if constexpr (FMT == kFmtNVAmax) {
             // Largest finite magnitude of the thread's 64 rotated values,
-            // then of the warp; one atomic per warp and tile.
+            // kept per operand across the warp's tiles; the warp's maxima
+            // reach global memory once, at the end (one atomic per warp and
+            // operand instead of one per tile on a single word).
             static_assert(!SR && !DUAL, "NVFP4: round to nearest, one direction");
-            float m = 0.0f;
+            float m = second ? amax_run1 : amax_run0;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 float lo, hi;
@@ -466,9 +469,7 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads,
                 m = fmaxf(m, lo <= 3.402823466e38f ? lo : 0.0f);
                 m = fmaxf(m, hi <= 3.402823466e38f ? hi : 0.0f);
             }
-            const unsigned int wm = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m));
-            unsigned int *amax = second ? a1.amax : a0.amax;
-            if (lane == 0 && wm != 0u) atomicMax(amax, wm);
+            (second ? amax_run1 : amax_run0) = m;
             continue;
         }
         const int r0 = 64 * chalf + 2 * lane;                 // line of the tile (r0, r0 + 1)
@@ -562,6 +563,12 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads,
                 bulk_commit_group();
             }
         }
+    }
+    if constexpr (FMT == kFmtNVAmax) {
+        const unsigned int w0 = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(amax_run0));
+        const unsigned int w1 = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(amax_run1));
+        if (lane == 0 && w0 != 0u) atomicMax(a0.amax, w0);
+        if (lane == 0 && w1 != 0u && a1.num_tiles > 0) atomicMax(a1.amax, w1);
     }
     // Every store has completed (global writes included) before the CTA leaves.
     if (kStaged && threadIdx.x == 0) bulk_wait_group_0();
