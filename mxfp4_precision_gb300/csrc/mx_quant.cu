@@ -590,17 +590,41 @@ struct WideTile {
     static constexpr int CPW = 32 / LPC;                  // channels per warp (ROTN > 64)
 };
 
+// Ring depth and output path of the wide kernel, per Hadamard size (measured
+// on the down_proj operands): size 64 gains from a 3-deep ring and the staged
+// output (84.6 -> ~79 us); sizes 128 and 256, whose cross-lane stages and
+// bank conflicts dominate, are fastest with a 2-deep ring and direct stores.
+#ifndef MXQ_WIDE_STAGE_MAX
+#define MXQ_WIDE_STAGE_MAX 64
+#endif
+template <bool DUAL, int ROTN>
+struct WideRing {
+    static constexpr int kRing = !DUAL && ROTN == 64 ? 3 : 2;
+};
+
 template <int ROTN, bool RAND, bool SR, bool DUAL>
 __global__ void __launch_bounds__(kThreads, SR ? 1 : kColMinBlocks) mxq_colwise_wide_kernel(
     const __grid_constant__ CUtensorMap map0, const __grid_constant__ CUtensorMap map1,
+    const __grid_constant__ CUtensorMap cmap0, const __grid_constant__ CUtensorMap cmap1,
     const QuantArgs a0, const QuantArgs a1, const QuantArgs ar) {
     static_assert(ROTN == 64 || ROTN == 128 || ROTN == 256, "sizes 64..256 only");
     using G = WideTile<ROTN>;
+    // Hadamard 64 writes through the staging image of the column kernel (one
+    // TMA box of codes, one scale atom per 128 x 128 tile); 128 and 256 store
+    // directly (see WideRing).
+    constexpr bool kStagedW = !DUAL && G::TT == 128 && ROTN <= MXQ_WIDE_STAGE_MAX;
+    constexpr int kStages = WideRing<DUAL, ROTN>::kRing;
+    using S = ColStage<kFmtMX4>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *tiles = smem;                                   // kStages x 32 KB
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kTileBytes);
     uint64_t *empty = full + kStages;
+    // Random-sign words of each stage's tile (one 64-bit word per 64-token
+    // segment), written by the issuing thread before it arms the stage.
+    uint64_t *signw = empty + kStages;
+    uint8_t *stc = smem + kStages * kTileBytes + 1024;       // staging image (kStagedW)
+    uint8_t *sts = stc + S::kCodeBytes;
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -617,6 +641,10 @@ __global__ void __launch_bounds__(kThreads, SR ? 1 : kColMinBlocks) mxq_colwise_
         fence_barrier_init();
         prefetch_tmap(&map0);
         if (a1.num_tiles > 0) prefetch_tmap(&map1);
+        if (kStagedW) {
+            prefetch_tmap(&cmap0);
+            if (a1.num_tiles > 0) prefetch_tmap(&cmap1);
+        }
     }
     __syncthreads();
     griddep_wait();
@@ -626,6 +654,13 @@ __global__ void __launch_bounds__(kThreads, SR ? 1 : kColMinBlocks) mxq_colwise_
         const bool second = tile >= a0.num_tiles;
         const int lt = second ? tile - a0.num_tiles : tile;
         const int inner = second ? a1.tiles_inner : a0.tiles_inner;
+        if constexpr (RAND) {
+            const int64_t t0 = static_cast<int64_t>(lt / inner) * G::TT;
+            uint64_t o[4];
+            philox4x64_10(static_cast<uint64_t>(t0 / 256), a0.seed, 0, o);
+#pragma unroll
+            for (int k = 0; k < G::TT / 64; ++k) signw[s * 4 + k] = o[(t0 % 256) / 64 + k];
+        }
         mbar_arrive_expect_tx(&full[s], kTileBytes);
         tma_load_2d(tiles + s * kTileBytes, second ? &map1 : &map0, &full[s], (lt % inner) * G::TC,
                     (lt / inner) * G::TT);
@@ -660,7 +695,14 @@ __global__ void __launch_bounds__(kThreads, SR ? 1 : kColMinBlocks) mxq_colwise_
         int ok = 1;
         if (lane == 0) ok = mbar_wait(&full[s], parity, a0.status, &abort_flag) ? 1 : 0;
         ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-        if (!ok) break;
+        if constexpr (kStagedW) {
+            // The staging image was last stored one tile ago; the barrier also
+            // ANDs the warps' wait verdicts (see the column kernel).
+            if (threadIdx.x == 0) bulk_wait_group_read<0>();
+            if (!bar_and(kStageBarrier, kThreads, ok != 0)) break;
+        } else if (!ok) {
+            break;
+        }
 
         uint64_t x[32];
         const uint16_t *th = reinterpret_cast<const uint16_t *>(tiles + s * kTileBytes);
@@ -670,6 +712,7 @@ __global__ void __launch_bounds__(kThreads, SR ? 1 : kColMinBlocks) mxq_colwise_
             const uint32_t hi = th[(seg * 64 + 32 + i) * G::TC + ch];
             x[i] = pack2(__uint_as_float(lo << 16), __uint_as_float(hi << 16));
         }
+        const uint64_t sw = RAND ? signw[s * 4 + seg] : 0ull;
         if (DUAL)
             dual_rows<G::TC, SR>(reinterpret_cast<const uint32_t *>(th), t0, c0, a0, ar);
         __syncwarp();
@@ -681,11 +724,8 @@ __global__ void __launch_bounds__(kThreads, SR ? 1 : kColMinBlocks) mxq_colwise_
 
         const int64_t tb = t0 + 64 * seg;  // first token of this thread's segment
         if (RAND) {
-            // Both 32-bit sign words of the segment come from one Philox block.
-            uint64_t o[4];
-            philox4x64_10(static_cast<uint64_t>(tb / 256), a0.seed, 0, o);
-            const uint64_t w = o[(tb % 256) / 64];
-            const uint32_t blo = static_cast<uint32_t>(w), bhi = static_cast<uint32_t>(w >> 32);
+            // The segment's two 32-bit sign words (one 64-bit Philox output word).
+            const uint32_t blo = static_cast<uint32_t>(sw), bhi = static_cast<uint32_t>(sw >> 32);
 #pragma unroll
             for (int i = 0; i < 32; ++i)
                 x[i] ^= (((blo >> i) & 1u) ? 0x80000000ull : 0ull) |
@@ -735,6 +775,26 @@ __global__ void __launch_bounds__(kThreads, SR ? 1 : kColMinBlocks) mxq_colwise_
         } else {
             encode_pair_rne<true>(x, hadamard_norm<ROTN>(), q0, q1, s0, s1);
         }
+        if constexpr (kStagedW) {
+            // Line ch of the codes box: chunks 2*seg and 2*seg + 1 (64-byte
+            // swizzle); scale atom bytes of blocks 2*seg, 2*seg + 1.
+            const int sx = (ch >> 1) & 3;
+            *reinterpret_cast<uint4 *>(stc + ch * 64 + ((2 * seg) ^ sx) * 16) = q0;
+            *reinterpret_cast<uint4 *>(stc + ch * 64 + ((2 * seg + 1) ^ sx) * 16) = q1;
+            *reinterpret_cast<uint16_t *>(sts + (ch % 32) * 16 + (ch / 32) * 4 + 2 * seg) =
+                static_cast<uint16_t>(s0 | (s1 << 8));
+            fence_proxy_async_smem();
+            asm volatile("bar.sync %0, %1;" ::"n"(kStageBarrier), "n"(kThreads) : "memory");
+            if (threadIdx.x == 0) {
+                tma_store_2d(second ? &cmap1 : &cmap0, stc, static_cast<int32_t>(t0 / 2),
+                             static_cast<int32_t>(c0));
+                uint8_t *sdst = scales + ((c0 / 128) * katoms + t0 / 128) * 512;
+                if (MX_STORE_OK(sdst, 512, scales, scales_bytes, a0.status))
+                    bulk_store(sdst, sts, 512);
+                bulk_commit_group();
+            }
+            continue;
+        }
         if (tb < L && c < lines) {
             uint8_t *d = codes + c * (L / 2) + tb / 2;
             if (MX_STORE_OK(d, 32, codes, codes_bytes, a0.status)) {
@@ -747,6 +807,7 @@ __global__ void __launch_bounds__(kThreads, SR ? 1 : kColMinBlocks) mxq_colwise_
         if (MX_STORE_OK(e0, 1, scales, scales_bytes, a0.status)) *e0 = static_cast<uint8_t>(s0);
         if (MX_STORE_OK(e1, 1, scales, scales_bytes, a0.status)) *e1 = static_cast<uint8_t>(s1);
     }
+    if (kStagedW && threadIdx.x == 0) bulk_wait_group_0();
 }
 
 // ---------------------------------------------------------------- rowwise
@@ -947,17 +1008,25 @@ constexpr size_t col_smem() {
 template <bool COLWISE, int ROTN, bool RAND>
 cudaError_t launch_rot(bool sr, const Operands &o, const DeviceInfo &dev, cudaStream_t stream) {
     if constexpr (COLWISE && ROTN >= 64) {
-        const size_t smem = kStages * kTileBytes + 1024 + 1024;
+        // Ring tiles, the barrier region and (128-token tiles) one staging image.
+        const size_t smem = WideRing<false, ROTN>::kRing * kTileBytes + 1024 + 1024 +
+                            (ROTN <= MXQ_WIDE_STAGE_MAX && ROTN < 256 ? ColStage<kFmtMX4>::kBytes
+                                                                       : 0);
+        const size_t dsmem = WideRing<true, ROTN>::kRing * kTileBytes + 1024 + 1024;
         const int n = o.a0.num_tiles + o.a1.num_tiles;
         if (o.dual)
-            return sr ? launch_persistent(mxq_colwise_wide_kernel<ROTN, RAND, true, true>, n, smem,
-                                          dev, stream, o.map0, o.map1, o.a0, o.a1, o.ar)
-                      : launch_persistent(mxq_colwise_wide_kernel<ROTN, RAND, false, true>, n, smem,
-                                          dev, stream, o.map0, o.map1, o.a0, o.a1, o.ar);
+            return sr ? launch_persistent(mxq_colwise_wide_kernel<ROTN, RAND, true, true>, n, dsmem,
+                                          dev, stream, o.map0, o.map1, o.cmap0, o.cmap1, o.a0,
+                                          o.a1, o.ar)
+                      : launch_persistent(mxq_colwise_wide_kernel<ROTN, RAND, false, true>, n,
+                                          dsmem, dev, stream, o.map0, o.map1, o.cmap0, o.cmap1,
+                                          o.a0, o.a1, o.ar);
         return sr ? launch_persistent(mxq_colwise_wide_kernel<ROTN, RAND, true, false>, n, smem,
-                                      dev, stream, o.map0, o.map1, o.a0, o.a1, o.ar)
+                                      dev, stream, o.map0, o.map1, o.cmap0, o.cmap1, o.a0, o.a1,
+                                      o.ar)
                   : launch_persistent(mxq_colwise_wide_kernel<ROTN, RAND, false, false>, n, smem,
-                                      dev, stream, o.map0, o.map1, o.a0, o.a1, o.ar);
+                                      dev, stream, o.map0, o.map1, o.cmap0, o.cmap1, o.a0, o.a1,
+                                      o.ar);
     }
     else if constexpr (COLWISE) {
         const size_t smem = col_smem<kFmtMX4>();
