@@ -17,16 +17,21 @@
 //                256-wide K sub-tiles (128-byte swizzle) per stage, into a
 //                3-stage shared-memory ring.  Both CTAs' operand loads
 //                complete on the even CTA's stage barrier.
-//   warp 2       scale producer: the stage's block scales (this CTA's A rows;
-//                all 256 B rows) on a barrier of their own, so that the scale
-//                writers start while the operands are still in flight.
+//   warp 2       scale producer: the stages' block scales (this CTA's A rows;
+//                all 256 B rows) into a ring of their own, for the MX formats
+//                two slots deeper than the operand ring, so that they already
+//                wait in shared memory when a stage's tensor-memory scale
+//                columns come free.
 //   warp 1       tensor-memory allocation (pair); in the even CTA, the MMA
 //                issuer: per stage, 8 MMAs and one commit that frees the
 //                stage in both CTAs.
-//   warps 4..7   scale writers: warp 4+q moves the stage's block scales from
-//                shared memory into lane quarter q of its CTA's tensor memory
-//                with tcgen05.st (copy instructions would enter the MMA pipe
-//                and serialise with the MMAs), then signals the MMA thread.
+//   warps 4..7   scale writers: once the MMAs that last read the stage's
+//                scale columns have finished, warp 4+q moves the block scales
+//                from shared memory into lane quarter q of its CTA's tensor
+//                memory with tcgen05.st (copy instructions would enter the MMA
+//                pipe and serialise with the MMAs) and arrives on the stage's
+//                full barrier, which thus covers operands and scales: the MMA
+//                thread waits on one barrier per stage.
 //   warps 8..15  epilogue: tcgen05.ld the CTA's 128 x 256 accumulator half
 //                (each warp one 32-lane quarter x 128 columns) into registers,
 //                release tensor memory to the MMA thread at once, then store
@@ -57,6 +62,7 @@ constexpr int kTile = 256;                        // output tile (rows and colum
 constexpr int kHalf = 128;                        // rows of A / of B per CTA
 constexpr int kBKBytes = 128;                     // 256 FP4 per row per K sub-tile
 constexpr int kMaxStages = 5;
+constexpr int kMaxSFRing = 7;
 constexpr int kWriterWarp0 = 4;                   // warps 4..7: scale writers
 constexpr int kEpiWarp0 = 8;                      // warps 8..15: epilogue
 constexpr int kEpiWarps = 8;
@@ -101,12 +107,21 @@ struct Elem {
     static constexpr uint32_t kSFSub = kNV ? 2048 : 1024;       // scale room per sub-tile
     static constexpr uint32_t kOffA = 0;
     static constexpr uint32_t kOffB = kKSub * kSubBytes;
-    static constexpr uint32_t kOffSFA = 2 * kKSub * kSubBytes;
-    static constexpr uint32_t kOffSFB = kOffSFA + kKSub * kSFSub;          // two row groups of B
-    static constexpr uint32_t kStageBytes = kOffSFB + 2 * kKSub * kSFSub;  // 70 KB / 38 KB
+    static constexpr uint32_t kStageBytes = 2 * kKSub * kSubBytes;         // 64 KB / 32 KB
+    // Scales travel in a ring of their own (A's row group, then B's two).
+    // MX: two slots deeper than the operand ring, so that they are in
+    // shared memory before the stage's tensor-memory scale columns come
+    // free.  NVFP4 (four MMAs per stage, twice the scale columns per MMA):
+    // as deep as the operand ring and loaded once the stage is free, so
+    // that the writers wait on one barrier per stage (a second wait made
+    // them slower than its MMAs).
+    static constexpr int kSFRing = kNV ? kStages : kStages + 2;
+    static constexpr bool kSFAhead = kSFRing > kStages;
+    static constexpr uint32_t kOffSFB = kKSub * kSFSub;
+    static constexpr uint32_t kSFSlotBytes = 3 * kKSub * kSFSub;          // 6 KB
     static constexpr uint32_t kSFCols = kNV ? 48 : 24;          // tensor-memory columns per sub-tile
     static constexpr uint32_t kSFSlot = kSFCols * kKSub;
-    static_assert(kStages <= kMaxStages, "barrier arrays");
+    static_assert(kStages <= kMaxStages && kSFRing <= kMaxSFRing, "barrier arrays");
     static_assert(kSFCol + kStages * kSFSlot <= kTmemCols, "scale slots fit in tensor memory");
 };
 
@@ -164,9 +179,10 @@ struct GemmArgs {
 
 struct SharedCtl {
     uint64_t full[kMaxStages];      // even CTA: both CTAs' operand bytes of the stage have landed
-    uint64_t sf_full[kMaxStages];   // this CTA's scale bytes of the stage have landed
+                                    //   and both CTAs' scales are in tensor memory
     uint64_t empty[kMaxStages];     // the pair's MMAs have finished reading the stage
-    uint64_t sf_ready[kMaxStages];  // even CTA: both CTAs' scales of the stage are in tensor memory
+    uint64_t sf_full[kMaxSFRing];   // this CTA's scale bytes of a scale slot have landed
+    uint64_t sf_free[kMaxSFRing];   // this CTA's scale writers have read the slot
     uint64_t acc_full;           // the tile's accumulator is complete
     uint64_t acc_empty;          // even CTA: both CTAs' epilogues have read the accumulator
     uint64_t drain;
@@ -356,25 +372,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThr
     using E = Elem<FMT>;
     static_assert(!(FUSED && FMT != kFmtMX4), "the fused launch encodes MXFP4 only");
     constexpr int kStages = E::kStages, kKSub = E::kKSub;
+    constexpr int kSFRing = E::kSFRing;
     constexpr uint32_t kStageBytes = E::kStageBytes, kSFSlot = E::kSFSlot, kSFSub = E::kSFSub;
-    constexpr uint32_t kOffA = E::kOffA, kOffB = E::kOffB, kOffSFA = E::kOffSFA,
-                       kOffSFB = E::kOffSFB;
+    constexpr uint32_t kOffA = E::kOffA, kOffB = E::kOffB, kOffSFB = E::kOffSFB,
+                       kSFSlotBytes = E::kSFSlotBytes;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned base, kept as a shared-space pointer (offset arithmetic
     // only) so that the compiler emits shared-memory loads.  The offset is the
     // same in both CTAs of the pair (same kernel, same static layout).
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    SharedCtl *ctl = reinterpret_cast<SharedCtl *>(smem + kStages * kStageBytes);
+    uint8_t *sf_ring = smem + kStages * kStageBytes;
+    SharedCtl *ctl = reinterpret_cast<SharedCtl *>(sf_ring + kSFRing * kSFSlotBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&ctl->full[s], 1);
-            mbar_init(&ctl->sf_full[s], 1);
+            // The even CTA's producer (arming the operand bytes) and the four
+            // scale writers of each CTA.
+            mbar_init(&ctl->full[s], 1 + 2 * 4);
             mbar_init(&ctl->empty[s], 1);
-            mbar_init(&ctl->sf_ready[s], 2 * 4);
+        }
+        for (int j = 0; j < kSFRing; ++j) {
+            mbar_init(&ctl->sf_full[j], 1);
+            mbar_init(&ctl->sf_free[j], 4);
         }
         mbar_init(&ctl->acc_full, 1);
         mbar_init(&ctl->acc_empty, 2 * kEpiWarps);
@@ -407,7 +429,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThr
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(V::kRegsLow) : "memory");
         if ((warp == 0 || warp == 2) && lane == 0) {
             // ------------------------------------------------------------ producers
+            // Warp 0 fills the operand ring, warp 2 the scale ring.
             const bool scales = warp == 2;
+            const int ring = scales ? kSFRing : kStages;
+            const bool on_free = scales && E::kSFAhead;
             int stage = 0, n_issued = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -417,13 +442,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThr
                 tile_coords(g, it.tile, mb, nb);
                 const int64_t ga = 2 * static_cast<int64_t>(mb) + rank;  // this CTA's A scale group
                 for (int ks = it.ks0; ks < it.ks1; ++ks) {
-                    if (!mbar_wait_inl(&ctl->empty[stage], phase ^ 1u, g.status, abort)) {
+                    if (!mbar_wait_inl(on_free ? &ctl->sf_free[stage] : &ctl->empty[stage],
+                                       phase ^ 1u, g.status, abort)) {
                         ok = false;
                         break;
                     }
                     const int kt0 = ks * kKSub;
                     const int nsub = g.k_tiles - kt0 < kKSub ? g.k_tiles - kt0 : kKSub;
                     uint8_t *st = smem + stage * kStageBytes;
+                    uint8_t *sfs = sf_ring + stage * kSFSlotBytes;
                     if constexpr (FUSED) {
                         // This stage's 512 tokens of both panels are encoded.
                         const unsigned int want = kUnitsPerChunk;
@@ -444,12 +471,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThr
                             if (2 * static_cast<int64_t>(nb) + rb < g.b_groups) bytes += sub_bytes;
                         mbar_arrive_expect_tx(&ctl->sf_full[stage], bytes);
                         if (ga < g.a_groups)
-                            bulk_load(st + kOffSFA, g.As + (ga * g.katoms + E::kAtoms * kt0) * 512,
+                            bulk_load(sfs, g.As + (ga * g.katoms + E::kAtoms * kt0) * 512,
                                       sub_bytes, &ctl->sf_full[stage]);
                         for (int rb = 0; rb < 2; ++rb) {
                             const int64_t gb = 2 * static_cast<int64_t>(nb) + rb;
                             if (gb < g.b_groups)
-                                bulk_load(st + kOffSFB + rb * kKSub * kSFSub,
+                                bulk_load(sfs + kOffSFB + rb * kKSub * kSFSub,
                                           g.Bs + (gb * g.katoms + E::kAtoms * kt0) * 512,
                                           sub_bytes, &ctl->sf_full[stage]);
                         }
@@ -470,7 +497,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThr
                         }
                         *reinterpret_cast<volatile int *>(&ctl->issued) = ++n_issued;
                     }
-                    if (++stage == kStages) {
+                    if (++stage == ring) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -492,8 +519,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThr
                 if (!mbar_wait_inl(&ctl->acc_empty, acc_phase ^ 1u, g.status, abort)) break;
                 tc_fence_after();
                 for (int ks = it.ks0; ks < it.ks1; ++ks) {
-                    if (!mbar_wait_inl(&ctl->sf_ready[stage], phase, g.status, abort) ||
-                        !mbar_wait_inl(&ctl->full[stage], phase, g.status, abort)) {
+                    if (!mbar_wait_inl(&ctl->full[stage], phase, g.status, abort)) {
                         ok = false;
                         break;
                     }
@@ -556,15 +582,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThr
         // holds exactly those four rows.
         const int q = warp & 3;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
-        int stage = 0;
-        uint32_t phase = 0;
+        // Per stage: the scales are in this CTA's scale slot (sf_full) and
+        // the stage's tensor-memory columns are free (empty: the MMAs that
+        // last read them have finished); then write, release the scale slot
+        // and arrive on the even CTA's full barrier.
+        int stage = 0, sj = 0;
+        uint32_t phase = 0, sphase = 0;
         for (int w = pair; w < g.num_items; w += npairs) {
             const Item it = item_of(g, w);
             bool ok = true;
             for (int ks = it.ks0; ks < it.ks1; ++ks) {
                 int okw = 1;
-                if (lane == 0)
-                    okw = mbar_wait_inl(&ctl->sf_full[stage], phase, g.status, abort) ? 1 : 0;
+                if (lane == 0) {
+                    // Without the deeper ring the scales were loaded after
+                    // the stage came free: sf_full implies empty.
+                    okw = mbar_wait_inl(&ctl->sf_full[sj], sphase, g.status, abort) ? 1 : 0;
+                    if (E::kSFAhead && okw)
+                        okw = mbar_wait_inl(&ctl->empty[stage], phase ^ 1u, g.status, abort) ? 1 : 0;
+                }
                 okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
                 if (!okw) {
                     ok = false;
@@ -573,12 +608,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThr
                 tc_fence_after();
                 const int kt0 = ks * kKSub;
                 const int nsub = g.k_tiles - kt0 < kKSub ? g.k_tiles - kt0 : kKSub;
-                const uint8_t *st = smem + stage * kStageBytes;
+                const uint8_t *sfs = sf_ring + sj * kSFSlotBytes;
                 const uint32_t slot =
                     lane_base + kSFCol + kSFSlot * static_cast<uint32_t>(stage);
                 for (int u = 0; u < nsub; ++u) {
-                    const uint8_t *sfa = st + kOffSFA + u * E::kSFBytes;
-                    const uint8_t *sfb = st + kOffSFB + u * E::kSFBytes;
+                    const uint8_t *sfa = sfs + u * E::kSFBytes;
+                    const uint8_t *sfb = sfs + kOffSFB + u * E::kSFBytes;
                     const uint32_t col = slot + E::kSFCols * static_cast<uint32_t>(u);
                     if constexpr (FMT == kFmtNV4) {
                         // Atom j holds MMA j's scales: A at columns 4j..4j+3,
@@ -655,10 +690,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThr
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) arrive_even(&ctl->sf_ready[stage]);
+                if (lane == 0) {
+                    if (E::kSFAhead) mbar_arrive(&ctl->sf_free[sj]);
+                    arrive_even(&ctl->full[stage]);
+                }
                 if (++stage == kStages) {
                     stage = 0;
                     phase ^= 1u;
+                }
+                if (++sj == kSFRing) {
+                    sj = 0;
+                    sphase ^= 1u;
                 }
             }
             if (!ok) break;
@@ -810,7 +852,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThr
 
 template <int FMT>
 constexpr size_t gemm_smem() {
-    return Elem<FMT>::kStages * Elem<FMT>::kStageBytes + sizeof(SharedCtl) + 1024;
+    return Elem<FMT>::kStages * Elem<FMT>::kStageBytes +
+           Elem<FMT>::kSFRing * Elem<FMT>::kSFSlotBytes + sizeof(SharedCtl) + 1024;
 }
 
 // Co-resident 2-CTA clusters of a mx_gemm_kernel variant on a device,
