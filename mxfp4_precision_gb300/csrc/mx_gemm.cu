@@ -194,7 +194,7 @@ struct SharedCtl {
 // Tile order: bands of kBand tile rows, column by column within a band, so
 // that the tiles in flight at once share few A and B panels (L2 reuse).
 #ifndef MXG_BAND
-#define MXG_BAND 8
+#define MXG_BAND 16
 #endif
 constexpr int kBand = MXG_BAND;
 __device__ __forceinline__ void tile_coords(const GemmArgs &g, int t, int &mb, int &nb) {
