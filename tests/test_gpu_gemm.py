@@ -71,10 +71,11 @@ def test_gemm_small_last_round(N):
     assert assert_gemm_close(C, Cref, Cabs, f"small last round {M}x{N}x{K}") < 1e-5
 
 
-@pytest.mark.parametrize("K", [1536, 1312])
+@pytest.mark.parametrize("K", [1536, 1312, 1280, 1056])
 def test_gemm_odd_stage_count(K):
-    """Three 512-wide K stages per tile (the last one half full for K = 1536's
-    neighbour 1312, whose contraction tail is ragged too)."""
+    """Three 512-wide K stages per tile, over several tiles per pair (so the
+    operand and scale rings wrap).  1312: the last 256-wide sub-tile is ragged;
+    1280 and 1056: the last stage holds one sub-tile (1056: ragged too)."""
     n_tiles = 8
     m_tiles = (_pairs() + 6 + n_tiles - 1) // n_tiles
     M, N = 256 * m_tiles, 256 * n_tiles
@@ -86,7 +87,7 @@ def test_gemm_odd_stage_count(K):
 
 
 def test_gemm_last_round_across_bands():
-    """Tiles run in bands of 8 tile rows; here the last round spans the end of
+    """Tiles run in bands of 16 tile rows; here the last round spans the end of
     one band and a whole later band of one row (17 x 5 tiles)."""
     M, N, K = 17 * 256, 5 * 256, 1024
     Aq, As = _operand(M, K, 17, 1e-3)
