@@ -592,8 +592,8 @@ struct WideTile {
 
 // Ring depth and output path of the wide kernel, per Hadamard size (measured
 // on the down_proj operands): size 64 gains from a 3-deep ring and the staged
-// output (84.6 -> ~79 us); sizes 128 and 256, whose cross-lane stages and
-// bank conflicts dominate, are fastest with a 2-deep ring and direct stores.
+// output (84.6 -> ~79 us); sizes 128 and 256, whose cross-lane stages
+// dominate, are fastest with a 2-deep ring and direct stores.
 #ifndef MXQ_WIDE_STAGE_MAX
 #define MXQ_WIDE_STAGE_MAX 64
 #endif
