@@ -58,9 +58,9 @@ def _pairs():
 
 @pytest.mark.parametrize("N", [2048, 2048 - 100, 1792 + 100])
 def test_gemm_small_last_round(N):
-    """A few more 256 x 256 tiles than pairs (a short last round).  N = 1948
-    and N = 1892 leave the last column tile 156 and 100 wide; M is ragged
-    too."""
+    """A few more 256 x 256 tiles than pairs: two rounds (the launcher spreads
+    them over fewer pairs).  N = 1948 and N = 1892 leave the last column tile
+    156 and 100 wide; M is ragged too."""
     n_tiles = (N + 255) // 256
     m_tiles = (_pairs() + 4 + n_tiles - 1) // n_tiles
     M, K = 256 * m_tiles - 37, 1024
@@ -98,7 +98,7 @@ def test_gemm_last_round_across_bands():
 
 
 def test_gemm_large_last_round():
-    """More tiles than pairs, with a last round of more than half the pairs."""
+    """More tiles than pairs, by more than half the pairs (two rounds)."""
     n_tiles = 8
     m_tiles = (_pairs() + _pairs() // 2 + 10 + n_tiles - 1) // n_tiles
     M, N, K = 256 * m_tiles, 256 * n_tiles, 512
