@@ -9,14 +9,16 @@
 // (nearest-even, or stochastically) and packed two per byte.
 //
 // Three kernels, all persistent with a ring of 32 KB TMA tiles (3 deep for the
-// column kernel, 2 for the others; two resident CTAs per SM):
+// column kernel and the wide kernel's Hadamard 64, 2 for the others; two
+// resident CTAs per SM):
 //   mxq_colwise       contraction down the rows of src[T][C] (Wgrad operands,
 //                     Dgrad's W), no rotation or Hadamard 16/32: a 128-token
 //                     x 128-channel tile; each thread owns 2 adjacent
 //                     channels x 32 tokens as packed f32x2 pairs, so the
 //                     transpose is free (it reads a column pair from shared
 //                     memory) and the Hadamard and the block amax stay in
-//                     registers.  A ninth warp refills the ring.  Outputs
+//                     registers.  A ninth warp refills the ring (thread 0
+//                     in the dual variant).  Outputs
 //                     leave through a shared-memory staging image (one TMA
 //                     box of codes, one bulk copy of the scale atom per
 //                     tile).  With DUAL it also encodes the staged tile
