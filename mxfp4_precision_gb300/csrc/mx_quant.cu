@@ -287,6 +287,12 @@ struct ColStage {
     static constexpr int kRing = FMT == kFmtMX8 && kColRing > 2 ? 2 : kColRing;  // TMA ring depth
 };
 constexpr int kStageBarrier = 1;   // named barrier of the 8 compute warps
+// L2 priorities of the column kernel's copies: the bf16 input (read once)
+// is evicted first, the encoded codes and scales (read next by the GEMM)
+// last.
+#ifndef MXQ_L2_HINTS
+#define MXQ_L2_HINTS 1
+#endif
 
 template <int ROTN, bool RAND, bool SR, bool DUAL, int FMT = kFmtMX4>
 __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads,
@@ -353,8 +359,14 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads,
             }
         }
         mbar_arrive_expect_tx(&full[s], kTileBytes);
+#if MXQ_L2_HINTS
+        // The bf16 input is read once: its lines are the first L2 evicts.
+        tma_load_2d_hint(tiles + s * kTileBytes, second ? &map1 : &map0, &full[s],
+                         (lt % inner) * G::TC, (lt / inner) * G::TT, l2_evict_first_policy());
+#else
         tma_load_2d(tiles + s * kTileBytes, second ? &map1 : &map0, &full[s], (lt % inner) * G::TC,
                     (lt / inner) * G::TT);
+#endif
     };
     if (DUAL) {
         if (threadIdx.x == 0) {
@@ -542,13 +554,23 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads,
             fence_proxy_async_smem();
             asm volatile("bar.sync %0, %1;" ::"n"(kStageBarrier), "n"(kThreads) : "memory");
             if (threadIdx.x == 0) {
+                const int64_t atom = (c0 / 128) * katoms + (FMT == kFmtNV4 ? t0 / 64 : t0 / 128);
+                uint8_t *sdst = scales + atom * 512;
+#if MXQ_L2_HINTS
+                // The codes and scales are read next by the GEMM: keep them in L2.
+                const uint64_t keep = l2_evict_last_policy();
+                tma_store_2d_hint(second ? &cmap1 : &cmap0, stc,
+                                  static_cast<int32_t>(FMT == kFmtMX8 ? t0 : t0 / 2),
+                                  static_cast<int32_t>(c0), keep);
+                if (MX_STORE_OK(sdst, S::kScaleBytes, scales, scales_bytes, a0.status))
+                    bulk_store_hint(sdst, sts, S::kScaleBytes, keep);
+#else
                 tma_store_2d(second ? &cmap1 : &cmap0, stc,
                              static_cast<int32_t>(FMT == kFmtMX8 ? t0 : t0 / 2),
                              static_cast<int32_t>(c0));
-                const int64_t atom = (c0 / 128) * katoms + (FMT == kFmtNV4 ? t0 / 64 : t0 / 128);
-                uint8_t *sdst = scales + atom * 512;
                 if (MX_STORE_OK(sdst, S::kScaleBytes, scales, scales_bytes, a0.status))
                     bulk_store(sdst, sts, S::kScaleBytes);
+#endif
                 if constexpr (DUAL) {
                     // The row image: tokens t0 .. t0+127 as lines, channels as
                     // the contraction (box at channel byte c0 / 2, line t0;
