@@ -132,6 +132,14 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
 
 // 2-D tiled load: box at (c0 = innermost coordinate, c1) into shared `dst`,
 // completion signalled on `bar` (transaction bytes).
+// Brings a 2-D box of a tensor into L2 ahead of its load (no shared memory,
+// no barrier; coordinates outside the tensor are ignored like a load's).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
                                             int32_t c0, int32_t c1) {
     asm volatile(
