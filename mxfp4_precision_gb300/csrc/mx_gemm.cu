@@ -467,11 +467,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThr
                 tile_coords(g, it.tile, mb, nb);
                 const int64_t ga = 2 * static_cast<int64_t>(mb) + rank;  // this CTA's A scale group
 #if MXG_PFB
-                if (!scales && w + npairs < g.num_items) {
+                if (!FUSED && !scales && w + npairs < g.num_items) {
                     // The B panel of this pair's next tile, when it is a new
                     // column: read from DRAM by all the column's pairs at once
                     // otherwise.  Each pair of this band brings its share of
-                    // the panel's K range into L2 a tile ahead.
+                    // the panel's K range into L2 a tile ahead.  (Not in the
+                    // fused launch, whose panels may not be encoded yet.)
                     int mb2, nb2;
                     tile_coords(g, item_of(g, w + npairs).tile, mb2, nb2);
                     if (nb2 != nb) {
