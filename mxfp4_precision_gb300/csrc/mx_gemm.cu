@@ -191,15 +191,10 @@ struct SharedCtl {
     int issued;                  // stages whose operand loads this CTA has issued (monotonic)
 };
 
-// Tile order: bands of kBand tile rows, column by column within a band, so
-// that the tiles in flight at once share few A and B panels (L2 reuse).
-// Pairs per launch: as many as fit, or (MXG_BALANCE) just enough for the
-// same number of rounds, so that every pair holds a tile in the last round
-// (o_proj: 64 pairs x 4 tiles instead of 76 pairs with 28 in the last round;
-// the same makespan with less contention).
 // The output is written once and not read here: its stores bypass L1 and
 // are the first lines L2 evicts, so that they do not push the operand panels
 // (read by every tile of a band) out of L2 (o_proj GEMM 56.1 -> 54.0 us).
+// 1: streaming stores instead; 0: plain stores.
 #ifndef MXG_ST_KIND
 #define MXG_ST_KIND 2
 #endif
@@ -215,9 +210,15 @@ struct SharedCtl {
 #ifndef MXG_PFB
 #define MXG_PFB 1
 #endif
+// Pairs per launch: as many as fit, or (MXG_BALANCE) just enough for the
+// same number of rounds, so that every pair holds a tile in the last round
+// (o_proj: 64 pairs x 4 tiles instead of 76 pairs with 28 in the last round;
+// the same makespan with less contention).
 #ifndef MXG_BALANCE
 #define MXG_BALANCE 1
 #endif
+// Tile order: bands of kBand tile rows, column by column within a band, so
+// that the tiles in flight at once share few A and B panels (L2 reuse).
 #ifndef MXG_BAND
 #define MXG_BAND 16
 #endif
