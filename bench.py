@@ -486,6 +486,10 @@ def run_mine(args, world, rank, local):
     wl = args.workload
 
     def tr(kernel, file):
+        # The captures are of the default mode (deterministic Hadamard 32,
+        # round to nearest); another mode runs other kernel code.
+        if (MODE["rot"], MODE["rot_block"], MODE["round"]) != ("hadamard_det", 32, "rne"):
+            return None
         hit = traffic.get((kernel, wl))
         if hit and hit[0] == kernel_source_hash(file):
             return hit[1]
