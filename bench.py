@@ -433,13 +433,16 @@ def run_mine(args, world, rank, local):
         torch.cuda.synchronize(dev)
         return t0.elapsed_time(t1)
 
-    e2e_value = e2e_ms = serial_ms = None
+    e2e_value = e2e_ms = serial_ms = link = None
     if not args.no_e2e:
         e2e_run(2, True)                                 # warm-up
         e2e_ms = reduce_max(e2e_run(n_e2e, True), world, dev)
         serial_ms = e2e_run(n_e2e, False)
         mx.check_status()
         e2e_value = world * n_e2e * flops_step / (e2e_ms * 1e-3) / 1e12
+        link = measure_link(dY_h, X_h, dW_h, dY_d, X_d, dW_d, s_in, s_out, dev)
+        link["e2e_frac_of_both"] = ((dY_h.numel() * 2 + X_h.numel() * 2 + dW_h[0].numel() * 4)
+                                    / (e2e_ms / n_e2e * 1e-3) / 1e9) / link["both_gbs"]
 
     # side measurement: the dual-output encode of dY (both backward encodings
     # from one read) against the two single-direction encodes it replaces
@@ -556,7 +559,8 @@ def run_mine(args, world, rank, local):
                 "schedule": "steps pipelined over input-copy / compute / output-copy "
                             "streams, two device buffer sets",
                 "serial_ms_per_step": serial_ms / n_e2e,
-                "serial_value": world * n_e2e * flops_step / (serial_ms * 1e-3) / 1e12},
+                "serial_value": world * n_e2e * flops_step / (serial_ms * 1e-3) / 1e12,
+                "host_link": link},
             "gpu_launches": 2 * n,
             "dual_quantiser": dual,
             "clocks": clk,
@@ -789,6 +793,51 @@ def measure_variant(L, mx, fmt, dY, X, T, N, K, flush, stream, dev, peak, mxfp4_
             "gemm_frac_peak_measured": flops / (t_gemm * 1e-3) / 1e12 / peak["tflops"],
             "mxfp4_step_speedup": t_step / mxfp4_step_ms, "median_of": reps,
             "step_launches": 3 if nv else 2}
+
+
+def measure_link(dY_h, X_h, dW_h, dY_d, X_d, dW_d, s_in, s_out, dev, reps=5):
+    """The host link on its own, for the e2e figure's roofline: the step's input copies host -> device
+    alone, its dW copy device -> host alone, and both at once on the two copy streams (median of
+    ``reps``).  ``e2e_frac_of_both`` is then the e2e step's bytes per second over the both-ways rate."""
+    import torch
+    def run(fn):
+        ts = []
+        for r in range(reps + 1):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            cur = torch.cuda.current_stream(dev)
+            a.record(cur)
+            s_in.wait_stream(cur)
+            s_out.wait_stream(cur)
+            fn()
+            cur.wait_stream(s_in)
+            cur.wait_stream(s_out)
+            b.record(cur)
+            torch.cuda.synchronize(dev)
+            if r:
+                ts.append(a.elapsed_time(b))
+        ts.sort()
+        return ts[len(ts) // 2]
+
+    def h2d():
+        with torch.cuda.stream(s_in):
+            dY_d[1].copy_(dY_h, non_blocking=True)
+            X_d[1].copy_(X_h, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s_out):
+            dW_h[1].copy_(dW_d[1], non_blocking=True)
+
+    def both():
+        h2d()
+        d2h()
+
+    bi, bo = dY_h.numel() * 2 + X_h.numel() * 2, dW_h[1].numel() * 4
+    t_in, t_out, t_both = run(h2d), run(d2h), run(both)
+    return {"h2d_gbs": bi / (t_in * 1e-3) / 1e9, "d2h_gbs": bo / (t_out * 1e-3) / 1e9,
+            "both_gbs": (bi + bo) / (t_both * 1e-3) / 1e9,
+            "note": "plain copies of the step's own buffers on the e2e copy streams; the link is "
+                    "the e2e bound (both directions share it)"}
 
 
 def measure_dual(L, mx, dY, T, N, flush, stream, dev, hbm_gbs, reps=30):
