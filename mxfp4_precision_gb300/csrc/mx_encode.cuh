@@ -110,18 +110,27 @@ __device__ __forceinline__ void scale_by_norm(float (&x)[32]) {
 
 // ---------------------------------------------------------------- encoding
 // E2M1 with stochastic rounding: lower grid neighbour lo, step to the next;
-// round up iff u24 < (|v| - lo) / step * 2^24 (exact in fp32).
+// round up iff u24 < (|v| - lo) / step * 2^24.  Taken on the bits of |v|:
+// from 1 up, a binade holds two grid points (the leading mantissa bit picks
+// one) and (|v| - lo) / step * 2^24 is 4x the 22 mantissa bits below it, so
+// the decision u24 / 4 < those bits is the carry out of adding their
+// complement 2^22 - 1 - u24 / 4; in [0.5, 1) it is 2x the 23 mantissa bits
+// against u24 / 2.  Below 0.5 the threshold |v| * 2^25 is compared in fp32
+// (exact).  |v| >= 6 and Inf give 6, NaN gives zero.
 __device__ __forceinline__ uint32_t e2m1_sr_code(float v, uint32_t u24) {
-    const uint32_t sign = (__float_as_uint(v) >> 28) & 8u;
-    const float a = fabsf(v);
-    if (a >= 6.0f) return sign | 7u;
-    const uint32_t lo = (a >= 0.5f) + (a >= 1.0f) + (a >= 1.5f) + (a >= 2.0f) + (a >= 3.0f) +
-                        (a >= 4.0f);
-    const float lov = lo <= 4 ? 0.5f * static_cast<float>(lo) : (lo == 5 ? 3.0f : 4.0f);
-    const float inv_step_2p24 = lo < 4 ? 33554432.0f : (lo < 6 ? 16777216.0f : 8388608.0f);
-    const float thr = __fmul_rn(__fsub_rn(a, lov), inv_step_2p24);
-    const uint32_t up = static_cast<float>(u24) < thr ? 1u : 0u;
-    return sign | (lo + up);
+    const uint32_t b = __float_as_uint(v);
+    const uint32_t sign = (b >> 28) & 8u;
+    const uint32_t m = b & 0x7FFFFFFFu;
+    uint32_t c;
+    if (m >= 0x3F800000u) {         // |v| >= 1: codes 2 (1.0) .. 7 (6.0)
+        c = ((m + (~(u24 >> 2) & 0x3FFFFFu)) >> 22) - 0xFCu;
+        if (m >= 0x40C00000u) c = m > 0x7F800000u ? 0u : 7u;
+    } else if (m >= 0x3F000000u) {  // [0.5, 1): code 1 (0.5) or 2 (1.0)
+        c = ((m + (~(u24 >> 1) & 0x7FFFFFu)) >> 23) - 0x7Du;
+    } else {                        // [0, 0.5): code 0 or 1 (0.5)
+        c = static_cast<float>(u24) < __fmul_rn(__uint_as_float(m), 33554432.0f) ? 1u : 0u;
+    }
+    return sign | c;
 }
 
 // Pack e2m1(v[2j]) into the low nibble and e2m1(v[2j+1]) into the high nibble
