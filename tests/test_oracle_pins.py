@@ -302,6 +302,38 @@ def test_sr_representable_unchanged_and_saturates():
     assert all(oracle.e2m1_value(int(k)) == 6.0 for k in c)
 
 
+
+def test_sr_decision_exact_at_thresholds():
+    """The SR rule as exact rational arithmetic: round |v| up to the next E2M1 grid point iff
+    u24 < (|v| - lo) / (hi - lo) * 2^24, with v's fp32 value taken exactly.  Draws on both sides
+    of each threshold catch a <= for <, a wrong step in one binade or a lost low mantissa bit."""
+    from fractions import Fraction
+    rng = np.random.default_rng(11)
+    bits = rng.integers(0, 0x40E00000, size=6000, dtype=np.uint32)     # |v| from 0 to 7
+    bits = np.concatenate([bits, np.array([0x00000001, 0x3EFFFFFF, 0x3F000001, 0x3F7FFFFF,
+                                           0x3FBFFFFF, 0x3FC00001, 0x40BFFFFF], np.uint32)])
+    grid = [Fraction(g) for g in ("0", "0.5", "1", "1.5", "2", "3", "4", "6")]
+    vs, us, want = [], [], []
+    for b in bits:
+        v = np.uint32(b).view(np.float32)
+        a = Fraction(float(v))
+        if a >= 6:
+            vs.append(v); us.append(12345); want.append(6.0)
+            continue
+        lo = max(g for g in grid if g <= a)
+        hi = min(g for g in grid if g > a)
+        t = (a - lo) / (hi - lo) * 2 ** 24
+        f = int(t)                                   # floor (t >= 0)
+        for u in {max(f - 1, 0), f, min(f + 1, 2 ** 24 - 1)}:
+            vs.append(v); us.append(u)
+            want.append(float(hi if u < t else lo))
+    sign = np.where(rng.integers(0, 2, size=len(vs)) == 1, -1.0, 1.0)
+    v_arr = (np.array(vs, dtype=np.float32) * sign).astype(np.float32)
+    codes = oracle.e2m1_sr(v_arr, np.array(us, dtype=np.uint32))
+    got = np.array([oracle.e2m1_value(int(c)) for c in codes])
+    assert np.array_equal(got, np.array(want) * sign)
+
+
 # ---------------------------------------------------------------------------
 # Whole-operand encoding
 # ---------------------------------------------------------------------------
