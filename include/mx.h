@@ -120,11 +120,14 @@ mx_status mx_scales_to_canonical(const void *d_scales, int64_t lines, int64_t k,
  *              (ignored for MX_ROT_NONE).  The Hadamard is Sylvester-ordered,
  *              normalised by 1/sqrt(rot_block), evaluated in fp32 as butterfly
  *              stages of stride 1, 2, ..., rot_block/2 then one multiply.
- *   rnd        mx_round.  SR draws: Philox4x64-10, key (seed, 1), counter
- *              (e/8, 0, 0, 0), e = line*k + position; 24-bit draw u; round away
- *              from the lower grid neighbour iff u < frac * 2^24.
- *   seed       key for the random sign (key (seed, 0), bit t%256 of the 256-bit
- *              block t/256, t = position along k) and for SR.
+ *   rnd        mx_round.  SR draws come from the random stream (seed, 1):
+ *              Philox4x32-10 with key (seed low 32 bits, seed high 32 bits)
+ *              and counter (n low, n high, tag low, tag high) for block n and
+ *              tag 1.  Element e = line*k + position takes the top 24 bits u of
+ *              word e%4 of block e/4 and rounds away from the lower grid
+ *              neighbour iff u < frac * 2^24.
+ *   seed       key of the random sign (stream (seed, 0): bit t%32 of word
+ *              (t%128)/32 of block t/128, t = position along k) and of SR.
  *   d_codes    mx_codes_bytes(lines, k) bytes; d_scales mx_scales_bytes(lines, k).
  * rows == 0 or cols == 0: returns MX_OK and launches nothing.
  */

@@ -1,4 +1,4 @@
-// mx_encode.cuh -- device building blocks of the MXFP4 encoders: Philox4x64-10
+// mx_encode.cuh -- device building blocks of the MXFP4 encoders: Philox4x32-10
 // draws, Hadamard butterflies, block amax and shared exponent, E2M1 rounding
 // and packing, and the tiled scale layout.  Shared by the stand-alone
 // encoders (mx_quant.cu) and the encoder warps of the fused Wgrad GEMM
@@ -19,26 +19,25 @@
 namespace mx {
 namespace enc {
 
-// ---------------------------------------------------------------- Philox4x64-10
-// Salmon et al., "Parallel Random Numbers: As Easy as 1, 2, 3" (SC'11).
-__device__ __forceinline__ void philox4x64_10(uint64_t c0, uint64_t k0, uint64_t k1,
-                                              uint64_t (&o)[4]) {
-    const uint64_t mul_a = 0xD2E7470EE14C6C93ull, mul_b = 0xCA5A826395121157ull;
-    const uint64_t weyl_a = 0x9E3779B97F4A7C15ull, weyl_b = 0xBB67AE8584CAA73Bull;
-    uint64_t x0 = c0, x1 = 0, x2 = 0, x3 = 0;
+// ---------------------------------------------------------------- Philox4x32-10
+// Salmon et al., "Parallel Random Numbers: As Easy as 1, 2, 3" (SC'11).  Each
+// round is two 32 x 32 -> 64-bit products (one wide multiply each).
+__device__ __forceinline__ void philox4x32_10(uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3,
+                                              uint32_t k0, uint32_t k1, uint32_t (&o)[4]) {
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
         if (r > 0) {
-            k0 += weyl_a;
-            k1 += weyl_b;
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
         }
-        const uint64_t lo_a = mul_a * x0, hi_a = __umul64hi(mul_a, x0);
-        const uint64_t lo_b = mul_b * x2, hi_b = __umul64hi(mul_b, x2);
-        const uint64_t n0 = hi_b ^ x1 ^ k0, n2 = hi_a ^ x3 ^ k1;
+        const uint64_t pa = static_cast<uint64_t>(0xD2511F53u) * x0;
+        const uint64_t pb = static_cast<uint64_t>(0xCD9E8D57u) * x2;
+        const uint32_t n0 = static_cast<uint32_t>(pb >> 32) ^ x1 ^ k0;
+        const uint32_t n2 = static_cast<uint32_t>(pa >> 32) ^ x3 ^ k1;
         x0 = n0;
-        x1 = lo_b;
+        x1 = static_cast<uint32_t>(pb);
         x2 = n2;
-        x3 = lo_a;
+        x3 = static_cast<uint32_t>(pa);
     }
     o[0] = x0;
     o[1] = x1;
@@ -46,25 +45,34 @@ __device__ __forceinline__ void philox4x64_10(uint64_t c0, uint64_t k0, uint64_t
     o[3] = x3;
 }
 
-// 32 consecutive 24-bit SR draws for flat indices e0 .. e0+31 (e0 % 8 == 0).
+// Block n of the random stream (seed, tag): key = the seed's 32-bit halves
+// (low first), counter = (n low, n high, tag low, tag high).  The random
+// signs are stream (seed, 0), the SR draws of operand A (seed, 1) and of B
+// (seed, 2).
+__device__ __forceinline__ void philox_block(uint64_t seed, uint64_t tag, uint64_t n,
+                                             uint32_t (&o)[4]) {
+    philox4x32_10(static_cast<uint32_t>(n), static_cast<uint32_t>(n >> 32),
+                  static_cast<uint32_t>(tag), static_cast<uint32_t>(tag >> 32),
+                  static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32), o);
+}
+
+// 32 consecutive 24-bit SR draws for flat indices e0 .. e0+31 (e0 % 4 == 0):
+// element e takes the top 24 bits of word e % 4 of block e / 4.
 __device__ __forceinline__ void sr_draws32(uint64_t seed, uint64_t tag, uint64_t e0,
                                            uint32_t (&u)[32]) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint64_t o[4];
-        philox4x64_10(e0 / 8 + q, seed, tag, o);
+    for (int q = 0; q < 8; ++q) {
+        uint32_t o[4];
+        philox_block(seed, tag, e0 / 4 + q, o);
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            u[8 * q + j] = static_cast<uint32_t>(o[j / 2] >> (32 * (j % 2))) >> 8;
+        for (int j = 0; j < 4; ++j) u[4 * q + j] = o[j] >> 8;
     }
 }
 
-// 32 random sign bits for positions 32*chunk .. 32*chunk+31 of the 256-block
-// `blk256` (bit i set -> d = -1).
-__device__ __forceinline__ uint32_t sign_bits32(uint64_t seed, uint64_t blk256, int chunk) {
-    uint64_t o[4];
-    philox4x64_10(blk256, seed, 0, o);
-    return static_cast<uint32_t>(o[chunk / 2] >> (32 * (chunk % 2)));
+// 128 random sign bits of tokens 128*n .. 128*n+127: bit t % 32 of word
+// (t % 128) / 32 (bit set -> d = -1).
+__device__ __forceinline__ void sign_block128(uint64_t seed, uint64_t n, uint32_t (&o)[4]) {
+    philox_block(seed, 0, n, o);
 }
 
 __device__ __forceinline__ void apply_signs(float (&x)[32], uint32_t bits) {
@@ -430,9 +438,9 @@ __device__ __forceinline__ int64_t nv_scale_offset(int64_t line, int64_t block, 
            (block % 4);
 }
 
-// Stochastic-rounding encode of one block of 32 that draws its randomness 8
-// elements at a time (one Philox call per 8, in the order of sr_draws32), so
-// that only 8 draws are live at once: the same codes as encode_block32<true>
+// Stochastic-rounding encode of one block of 32 that draws its randomness 4
+// elements at a time (one Philox call per 4, in the order of sr_draws32), so
+// that only 4 draws are live at once: the same codes as encode_block32<true>
 // fed by sr_draws32(seed, tag, e0, u).
 __device__ __forceinline__ uint32_t encode_block32_sr(const float (&r)[32], uint4 &q,
                                                       uint64_t seed, uint64_t tag, uint64_t e0) {
@@ -449,13 +457,15 @@ __device__ __forceinline__ uint32_t encode_block32_sr(const float (&r)[32], uint
     uint32_t w[4];
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
-        uint64_t o[4];
-        philox4x64_10(e0 / 8 + g, seed, tag, o);
         uint32_t word = 0;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const uint32_t u24 = static_cast<uint32_t>(o[k / 2] >> (32 * (k % 2))) >> 8;
-            word |= e2m1_sr_code(__fmul_rn(r[8 * g + k], inv), u24) << (4 * k);
+        for (int h = 0; h < 2; ++h) {
+            uint32_t o[4];
+            philox_block(seed, tag, e0 / 4 + 2 * g + h, o);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                word |= e2m1_sr_code(__fmul_rn(r[8 * g + 4 * h + k], inv), o[k] >> 8)
+                        << (4 * (4 * h + k));
         }
         w[g] = word;
     }

@@ -69,10 +69,13 @@ constexpr int kStageBufs = MXQ_STAGE_BUFS;  // its output staging buffers
 // the round-to-nearest colwise kernels are held to 128 registers so that the
 // random-sign variants do not fall to one CTA per SM.
 constexpr int kColMinBlocks = 2;
+// The stochastic-rounding column kernel also runs two CTAs per SM: at the
+// 96-register bound it spills a few words, and the second CTA's warps hide
+// the Philox multiply chains (down_proj SR encode 448.8 -> 334.6 us).
 #ifndef MXQ_SR_MINB
-#define MXQ_SR_MINB 1
+#define MXQ_SR_MINB 2
 #endif
-constexpr int kColSRMinBlocks = MXQ_SR_MINB;  // stochastic rounding (see the SR encode)
+constexpr int kColSRMinBlocks = MXQ_SR_MINB;
 constexpr int kThreads = 256;           // compute threads (8 warps)
 constexpr int kColProducerThreads = kThreads + 32;  // + a TMA producer warp
 constexpr uint32_t kTileBytes = 32768;  // one staged bf16 tile (128 x 128, 256 x 64 or 64 x 256)
@@ -349,14 +352,12 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads,
         const int lt = second ? tile - a0.num_tiles : tile;
         const int inner = second ? a1.tiles_inner : a0.tiles_inner;
         if constexpr (RAND) {
+            static_assert(G::TT == 128, "one 128-bit sign block per tile");
             const int64_t t0 = static_cast<int64_t>(lt / inner) * G::TT;
-            uint64_t o[4];
-            philox4x64_10(static_cast<uint64_t>(t0 / 256), a0.seed, 0, o);
+            uint32_t o[4];
+            sign_block128(a0.seed, static_cast<uint64_t>(t0 / 128), o);
 #pragma unroll
-            for (int k = 0; k < G::TOKEN_BLOCKS; ++k) {
-                const int chunk = static_cast<int>((t0 % 256) / 32) + k;
-                signw[s * G::TOKEN_BLOCKS + k] = static_cast<uint32_t>(o[chunk / 2] >> (32 * (chunk % 2)));
-            }
+            for (int k = 0; k < G::TOKEN_BLOCKS; ++k) signw[s * G::TOKEN_BLOCKS + k] = o[k];
         }
         mbar_arrive_expect_tx(&full[s], kTileBytes);
 #if MXQ_L2_HINTS
@@ -679,11 +680,16 @@ __global__ void __launch_bounds__(kThreads, SR ? 1 : kColMinBlocks) mxq_colwise_
         const int lt = second ? tile - a0.num_tiles : tile;
         const int inner = second ? a1.tiles_inner : a0.tiles_inner;
         if constexpr (RAND) {
+            // Sign word of each 64-token segment: two 32-bit words of its 128-bit block.
+            static_assert(G::TT % 128 == 0, "tiles start on a sign block");
             const int64_t t0 = static_cast<int64_t>(lt / inner) * G::TT;
-            uint64_t o[4];
-            philox4x64_10(static_cast<uint64_t>(t0 / 256), a0.seed, 0, o);
 #pragma unroll
-            for (int k = 0; k < G::TT / 64; ++k) signw[s * 4 + k] = o[(t0 % 256) / 64 + k];
+            for (int h = 0; h < G::TT / 128; ++h) {
+                uint32_t o[4];
+                sign_block128(a0.seed, static_cast<uint64_t>(t0 / 128 + h), o);
+                signw[s * 4 + 2 * h] = o[0] | (static_cast<uint64_t>(o[1]) << 32);
+                signw[s * 4 + 2 * h + 1] = o[2] | (static_cast<uint64_t>(o[3]) << 32);
+            }
         }
         mbar_arrive_expect_tx(&full[s], kTileBytes);
         tma_load_2d(tiles + s * kTileBytes, second ? &map1 : &map0, &full[s], (lt % inner) * G::TC,
@@ -748,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, SR ? 1 : kColMinBlocks) mxq_colwise_
 
         const int64_t tb = t0 + 64 * seg;  // first token of this thread's segment
         if (RAND) {
-            // The segment's two 32-bit sign words (one 64-bit Philox output word).
+            // The segment's two 32-bit sign words (tokens tb .. tb+31, tb+32 .. tb+63).
             const uint32_t blo = static_cast<uint32_t>(sw), bhi = static_cast<uint32_t>(sw >> 32);
 #pragma unroll
             for (int i = 0; i < 32; ++i)
@@ -919,11 +925,12 @@ __global__ void __launch_bounds__(kThreads) mxq_rowwise_kernel(const __grid_cons
 
         if (ROTN > 0) {
             if (RAND) {
-                uint64_t o[4];
-                philox4x64_10(static_cast<uint64_t>(col0 / 256), p.seed, 0, o);
-                const int ba = blk_a, bb = blk_a + 4;
-                apply_signs(xa, static_cast<uint32_t>(o[ba / 2] >> (32 * (ba % 2))));
-                apply_signs(xb, static_cast<uint32_t>(o[bb / 2] >> (32 * (bb % 2))));
+                // blocks blk_a and blk_a + 4: word blk_a of the tile's two 128-bit sign blocks
+                uint32_t oa[4], ob[4];
+                sign_block128(p.seed, static_cast<uint64_t>(col0 / 128), oa);
+                sign_block128(p.seed, static_cast<uint64_t>(col0 / 128 + 1), ob);
+                apply_signs(xa, blk_a == 0 ? oa[0] : blk_a == 1 ? oa[1] : blk_a == 2 ? oa[2] : oa[3]);
+                apply_signs(xb, blk_a == 0 ? ob[0] : blk_a == 1 ? ob[1] : blk_a == 2 ? ob[2] : ob[3]);
             }
             fwht_in_thread<ROTN>(xa);
             fwht_in_thread<ROTN>(xb);

@@ -54,7 +54,7 @@ def lib() -> ctypes.CDLL:
             L = ctypes.CDLL(_SO)
             P = ctypes.c_void_p
             i64, u64, i32 = ctypes.c_int64, ctypes.c_uint64, ctypes.c_int
-            L.oracle_philox4x64_10.argtypes = [P, P, P]
+            L.oracle_philox4x32_10.argtypes = [P, P, P]
             L.oracle_sign.argtypes = [u64, i64]
             L.oracle_sign.restype = i32
             L.oracle_sr_u24.argtypes = [u64, u64, u64]
@@ -115,11 +115,11 @@ def _ptr(a: np.ndarray) -> int:
 # --------------------------------------------------------------------------
 # scalar / vector element routines
 # --------------------------------------------------------------------------
-def philox4x64_10(ctr, key) -> np.ndarray:
-    c = np.ascontiguousarray(np.asarray(ctr, dtype=np.uint64).reshape(4))
-    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint64).reshape(2))
-    out = np.zeros(4, dtype=np.uint64)
-    lib().oracle_philox4x64_10(_ptr(c), _ptr(k), _ptr(out))
+def philox4x32_10(ctr, key) -> np.ndarray:
+    c = np.ascontiguousarray(np.asarray(ctr, dtype=np.uint32).reshape(4))
+    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint32).reshape(2))
+    out = np.zeros(4, dtype=np.uint32)
+    lib().oracle_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
     return out
 
 

@@ -30,70 +30,64 @@
 #include <string.h>
 
 /* ------------------------------------------------------------------------ */
-/* Philox4x64-10, written from the description in Salmon et al., SC'11:      */
-/* each round multiplies words 0 and 2 by two odd constants, splits the      */
-/* 128-bit products into hi/lo halves, and mixes the highs with words 1, 3   */
-/* and the round key; the key is bumped by two Weyl constants between        */
+/* Philox4x32-10, written from the description in Salmon et al., SC'11:      */
+/* each round multiplies words 0 and 2 by two odd 32-bit constants, splits   */
+/* the 64-bit products into hi/lo halves, and mixes the highs with words 1,  */
+/* 3 and the round key; the key is bumped by two Weyl constants between      */
 /* rounds.                                                                   */
 /* ------------------------------------------------------------------------ */
-static const uint64_t PHILOX_MUL_A = 0xD2E7470EE14C6C93ULL;
-static const uint64_t PHILOX_MUL_B = 0xCA5A826395121157ULL;
-static const uint64_t PHILOX_WEYL_A = 0x9E3779B97F4A7C15ULL; /* golden ratio */
-static const uint64_t PHILOX_WEYL_B = 0xBB67AE8584CAA73BULL; /* sqrt(3) - 1  */
+static const uint32_t PHILOX_MUL_A = 0xD2511F53u;
+static const uint32_t PHILOX_MUL_B = 0xCD9E8D57u;
+static const uint32_t PHILOX_WEYL_A = 0x9E3779B9u; /* golden ratio */
+static const uint32_t PHILOX_WEYL_B = 0xBB67AE85u; /* sqrt(3) - 1  */
 
-static void mul_128(uint64_t a, uint64_t b, uint64_t *hi, uint64_t *lo)
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4])
 {
-    unsigned __int128 p = (unsigned __int128)a * (unsigned __int128)b;
-    *hi = (uint64_t)(p >> 64);
-    *lo = (uint64_t)p;
-}
-
-void oracle_philox4x64_10(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4])
-{
-    uint64_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
-    uint64_t k0 = key[0], k1 = key[1];
+    uint32_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
     for (int round = 0; round < 10; ++round) {
         if (round > 0) {
             k0 += PHILOX_WEYL_A;
             k1 += PHILOX_WEYL_B;
         }
-        uint64_t hi_a, lo_a, hi_b, lo_b;
-        mul_128(PHILOX_MUL_A, x0, &hi_a, &lo_a);
-        mul_128(PHILOX_MUL_B, x2, &hi_b, &lo_b);
-        uint64_t n0 = hi_b ^ x1 ^ k0;
-        uint64_t n1 = lo_b;
-        uint64_t n2 = hi_a ^ x3 ^ k1;
-        uint64_t n3 = lo_a;
+        uint64_t pa = (uint64_t)PHILOX_MUL_A * (uint64_t)x0;
+        uint64_t pb = (uint64_t)PHILOX_MUL_B * (uint64_t)x2;
+        uint32_t n0 = (uint32_t)(pb >> 32) ^ x1 ^ k0;
+        uint32_t n1 = (uint32_t)pb;
+        uint32_t n2 = (uint32_t)(pa >> 32) ^ x3 ^ k1;
+        uint32_t n3 = (uint32_t)pa;
         x0 = n0; x1 = n1; x2 = n2; x3 = n3;
     }
     out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
 }
 
-/* Sign vector: one Philox call (key (seed, 0), counter (t/256, 0, 0, 0))
- * gives 256 bits; position t uses bit (t mod 64) of word ((t mod 256) / 64).
+/* One 128-bit block of the stream (seed, tag): key = the seed's two 32-bit
+ * halves (low first), counter = (n low, n high, tag low, tag high). */
+static void philox_block(uint64_t seed, uint64_t tag, uint64_t n, uint32_t out[4])
+{
+    uint32_t ctr[4] = {(uint32_t)n, (uint32_t)(n >> 32), (uint32_t)tag, (uint32_t)(tag >> 32)};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    oracle_philox4x32_10(ctr, key, out);
+}
+
+/* Sign vector: block n = t/128 of the stream (seed, 0) gives 128 bits;
+ * position t uses bit (t mod 32) of word ((t mod 128) / 32).
  * Bit 1 means d_t = -1. */
 int oracle_sign(uint64_t seed, int64_t t)
 {
-    uint64_t ctr[4] = {(uint64_t)t / 256u, 0, 0, 0};
-    uint64_t key[2] = {seed, 0};
-    uint64_t out[4];
-    oracle_philox4x64_10(ctr, key, out);
-    unsigned b = (unsigned)((uint64_t)t % 256u);
-    return ((out[b / 64] >> (b % 64)) & 1u) ? -1 : +1;
+    uint32_t out[4];
+    philox_block(seed, 0, (uint64_t)t / 128u, out);
+    unsigned b = (unsigned)((uint64_t)t % 128u);
+    return ((out[b / 32] >> (b % 32)) & 1u) ? -1 : +1;
 }
 
-/* SR draw: one Philox call (key (seed, tag), counter (e/8, 0, 0, 0)) gives
- * eight 32-bit words w_j = 32-bit half (j mod 2) of 64-bit word j/2 (low half
- * first); element e uses w_(e mod 8) >> 8. */
+/* SR draw: block n = e/4 of the stream (seed, tag) gives four 32-bit words;
+ * element e uses word (e mod 4) >> 8. */
 uint32_t oracle_sr_u24(uint64_t seed, uint64_t tag, uint64_t e)
 {
-    uint64_t ctr[4] = {e / 8u, 0, 0, 0};
-    uint64_t key[2] = {seed, tag};
-    uint64_t out[4];
-    oracle_philox4x64_10(ctr, key, out);
-    unsigned j = (unsigned)(e % 8u);
-    uint32_t w = (uint32_t)(out[j / 2] >> (32u * (j % 2)));
-    return w >> 8;
+    uint32_t out[4];
+    philox_block(seed, tag, e / 4u, out);
+    return out[e % 4u] >> 8;
 }
 
 /* ------------------------------------------------------------------------ */

@@ -19,7 +19,7 @@
  *           (bias 127), E2M1 element (bias 1, max 6, no Inf/NaN); its 8-bit
  *           member MXFP8 (E4M3 element, bias 7, max 448) is the block-scaled
  *           form of the FP8 baseline of [36kr] "Ende-zu-Ende-Effizienz".
- *   Philox4x64-10: Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As
+ *   Philox4x32-10: Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As
  *           Easy as 1, 2, 3", SC'11.
  *
  * Every routine is single-threaded and written for readability, not speed.
@@ -32,14 +32,18 @@
 extern "C" {
 #endif
 
-/* Philox4x64 with 10 rounds (Salmon et al. SC'11): out = philox(ctr, key). */
-void oracle_philox4x64_10(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4]);
+/* Philox4x32 with 10 rounds (Salmon et al. SC'11): out = philox(ctr, key). */
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
 
-/* Random sign d_t in {+1,-1} for absolute contraction position t, key (seed, 0).
+/* Random sign d_t in {+1,-1} for absolute contraction position t: stream
+ * (seed, tag 0), block t/128, bit t mod 128.
  * Reading of [36kr] "Fehlerdiagnoseexperiment" (Hadamard with random sign flip). */
 int oracle_sign(uint64_t seed, int64_t t);
 
-/* 24-bit stochastic-rounding draw for flat element index e, key (seed, tag). */
+/* 24-bit stochastic-rounding draw for flat element index e: stream (seed, tag),
+ * block e/4, word e mod 4, top 24 bits.  A stream (seed, tag) is Philox4x32-10
+ * with key (seed low, seed high) and counter (block low, block high, tag low,
+ * tag high). */
 uint32_t oracle_sr_u24(uint64_t seed, uint64_t tag, uint64_t e);
 
 /* Canonical fp32 Walsh-Hadamard of one block of n floats, in place:

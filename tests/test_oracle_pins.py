@@ -1,5 +1,5 @@
 """Pins for the CPU oracle: each check ties the oracle to something other than
-itself -- a library routine (numpy's Philox, scipy's Hadamard matrix, numpy
+itself -- a library routine (Triton's Philox, scipy's Hadamard matrix, numpy
 matmul), a closed form, an invariant the pages state, or brute force on tiny
 inputs.  Each test names the plausible oracle mistake it would catch.
 """
@@ -68,43 +68,99 @@ def test_h16_block_size_supported():
 
 
 # ---------------------------------------------------------------------------
-# Philox4x64-10 against numpy's implementation (library routine)
+# Philox4x32-10: the published known-answer vectors and a library implementation
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("key", [(0, 0), (1, 0), (0x1234, 0x5678), (2**64 - 1, 7)])
-@pytest.mark.parametrize("ctr0", [0, 1, 5, 2**40 + 3])
-def test_philox_matches_numpy(key, ctr0):
-    # numpy increments the counter before each block, so counter c-1 yields philox(c)
-    prev = (ctr0 - 1) % 2**64
-    ctr = [prev, 0, 0, 0] if ctr0 > 0 else [2**64 - 1] * 4
-    bg = np.random.Philox(counter=np.array(ctr, dtype=np.uint64), key=np.array(key, dtype=np.uint64))
-    ref = bg.random_raw(4)
-    got = oracle.philox4x64_10([ctr0, 0, 0, 0], key)
-    assert [int(v) for v in got] == [int(v) for v in ref]
+# Known-answer vectors of Philox4x32-10 (Salmon et al., SC'11, as distributed with
+# the authors' Random123 library): (counter, key) -> output.
+PHILOX4X32_KAT = [
+    ((0, 0, 0, 0), (0, 0), (0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8)),
+    ((0xFFFFFFFF,) * 4, (0xFFFFFFFF,) * 2, (0x408F276D, 0x41C83B0E, 0xA20BC7C6, 0x6D5451FD)),
+    ((0x243F6A88, 0x85A308D3, 0x13198A2E, 0x03707344), (0xA4093822, 0x299F31D0),
+     (0xD16CFE09, 0x94FDCCEB, 0x5001E420, 0x24126EA1)),
+]
 
 
-def _numpy_philox_block(q, key):
-    prev = (q - 1) % 2**64
-    ctr = [prev, 0, 0, 0] if q > 0 else [2**64 - 1] * 4
-    return np.random.Philox(counter=np.array(ctr, dtype=np.uint64),
-                            key=np.array(key, dtype=np.uint64)).random_raw(4)
+@pytest.mark.parametrize("ctr,key,want", PHILOX4X32_KAT)
+def test_philox_known_answers(ctr, key, want):
+    # catches a swapped multiplier, a wrong hi/lo half, a key bump in the wrong place
+    assert [int(v) for v in oracle.philox4x32_10(ctr, key)] == list(want)
+
+
+_TRITON_PHILOX = r"""
+import os, sys, json
+os.environ["TRITON_INTERPRET"] = "1"
+import torch, triton, triton.language as tl
+
+@triton.jit
+def k(out_ptr, seed, c_ptr, N: tl.constexpr):
+    i = tl.arange(0, N)
+    c0 = tl.load(c_ptr + 4 * i)
+    c1 = tl.load(c_ptr + 4 * i + 1)
+    c2 = tl.load(c_ptr + 4 * i + 2)
+    c3 = tl.load(c_ptr + 4 * i + 3)
+    a, b, c, d = tl.philox(seed, c0, c1, c2, c3, 10)
+    tl.store(out_ptr + 4 * i, a)
+    tl.store(out_ptr + 4 * i + 1, b)
+    tl.store(out_ptr + 4 * i + 2, c)
+    tl.store(out_ptr + 4 * i + 3, d)
+
+cases = json.loads(sys.stdin.read())
+res = []
+for seed, ctrs in cases:
+    c = torch.tensor(ctrs, dtype=torch.int64).to(torch.int32).to(torch.uint32).reshape(-1)
+    out = torch.zeros(c.numel(), dtype=torch.uint32)
+    k[(1,)](out, seed, c, N=c.numel() // 4)
+    res.append([int(v) & 0xFFFFFFFF for v in out.view(torch.int32).tolist()])
+print(json.dumps(res))
+"""
+
+
+def test_philox_matches_triton():
+    """Triton's own Philox4x32-10 (tl.philox, key = the seed's low and high halves), run by its
+    CPU interpreter in a child process, on random counters and keys."""
+    pytest.importorskip("triton")
+    import json
+    import subprocess
+    import sys
+    rng = np.random.default_rng(5)
+    cases = []
+    for _ in range(4):
+        seed = int(rng.integers(0, 2**63)) * 2 + int(rng.integers(0, 2))
+        ctrs = [[int(w) for w in rng.integers(0, 2**32, size=4)] for _ in range(8)]
+        ctrs[0] = [0, 0, 0, 0]
+        cases.append((seed, [w for c in ctrs for w in c]))
+    r = subprocess.run([sys.executable, "-c", _TRITON_PHILOX], input=json.dumps(cases),
+                       capture_output=True, text=True, timeout=300)
+    if r.returncode != 0:
+        pytest.skip("triton interpreter unavailable: " + r.stderr.strip().splitlines()[-1][:200])
+    got_all = json.loads(r.stdout.strip().splitlines()[-1])
+    for (seed, flat), ref in zip(cases, got_all):
+        key = (seed & 0xFFFFFFFF, seed >> 32)
+        for n in range(len(flat) // 4):
+            out = oracle.philox4x32_10(flat[4 * n:4 * n + 4], key)
+            assert [int(v) for v in out] == ref[4 * n:4 * n + 4]
+
+
+def _philox_block(seed, tag, n):
+    """Block n of the stream (seed, tag): key = seed halves, counter = (n, tag) halves."""
+    return oracle.philox4x32_10([n & 0xFFFFFFFF, n >> 32, tag & 0xFFFFFFFF, tag >> 32],
+                                [seed & 0xFFFFFFFF, seed >> 32])
 
 
 def test_sign_vector_bits_follow_documented_mapping():
     # catches an off-by-one in word/bit selection of the random sign
-    for seed in (0, 1, 99):
-        for t in (0, 1, 63, 64, 127, 200, 255, 256, 1000, 4097):
-            words = _numpy_philox_block(t // 256, (seed, 0))
-            b = t % 256
-            bit = (int(words[b // 64]) >> (b % 64)) & 1
+    for seed in (0, 1, 99, 2**40 + 7):
+        for t in (0, 1, 31, 32, 63, 64, 127, 128, 200, 255, 256, 1000, 4097, 2**33 + 5):
+            words = _philox_block(seed, 0, t // 128)
+            b = t % 128
+            bit = (int(words[b // 32]) >> (b % 32)) & 1
             assert oracle.sign(seed, t) == (-1 if bit else 1)
 
 
 def test_sr_draw_follows_documented_mapping():
-    for seed, tag in ((0, 1), (5, 2)):
-        for e in (0, 1, 7, 8, 9, 1023, 123457):
-            words = _numpy_philox_block(e // 8, (seed, tag))
-            j = e % 8
-            w = (int(words[j // 2]) >> (32 * (j % 2))) & 0xFFFFFFFF
+    for seed, tag in ((0, 1), (5, 2), (2**35 + 1, 1)):
+        for e in (0, 1, 3, 4, 7, 8, 9, 1023, 123457, 2**34 + 6):
+            w = int(_philox_block(seed, tag, e // 4)[e % 4])
             assert oracle.sr_u24(seed, tag, e) == w >> 8
 
 
