@@ -139,7 +139,7 @@ mx_status mx_quantize(const void *d_src, int64_t rows, int64_t cols, int contrac
  * mx_quantize_pair -- encode the two operands of a Wgrad in ONE launch: both
  * d_src0[rows0][cols0] and d_src1[rows1][cols1] are encoded down their rows
  * (MX_CONTRACT_ROWS: contraction length rows0 == rows1) with the same rotation,
- * rounding and seed; SR draws use key (seed, 1) for operand 0 and (seed, 2)
+ * rounding and seed; SR draws use stream (seed, 1) for operand 0 and (seed, 2)
  * for operand 1 (as mx_linear_wgrad does).  Outputs, layouts and argument rules
  * are those of mx_quantize for each operand.  One launch instead of two lets
  * the two HBM-bound encodes share one pipeline ramp-up and tail.
@@ -161,7 +161,7 @@ mx_status mx_quantize_pair(const void *d_src0, int64_t rows0, int64_t cols0, con
  *                           MX_CONTRACT_COLS, MX_ROT_NONE, 32, rnd, seed)
  *                           (T lines, contraction N, no rotation).
  * Both encodings are bit-identical to the two separate calls; SR draws use
- * key (seed, 1) for both (dY is operand A of both GEMMs), each with its own
+ * stream (seed, 1) for both (dY is operand A of both GEMMs), each with its own
  * line*k + position counter.  Argument rules are the union of the two calls
  * (T % 32, T % rot_block, N % 32, N % 8).  T == 0 or N == 0: MX_OK, nothing
  * launched.
@@ -195,7 +195,7 @@ size_t mx_linear_workspace_bytes(int op, int64_t T, int64_t N, int64_t K);
 /*
  * mx_linear_wgrad -- dW[N][K] = dY^T X.  Both operands are rotated along T
  * with the same rotation (same sign vector in MX_ROT_HADAMARD_RAND) and
- * encoded along T; operand dY uses SR key (seed, 1), X uses (seed, 2).
+ * encoded along T; operand dY uses SR stream (seed, 1), X uses (seed, 2).
  * T % 32 == 0 (and % rot_block); N, K % 8 == 0.
  */
 mx_status mx_linear_wgrad(const void *d_dY, const void *d_X, float *d_dW, int64_t T,

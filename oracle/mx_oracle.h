@@ -109,7 +109,7 @@ void oracle_e4m3_rne_vec(const float *v, int64_t n, uint8_t *out);
  *      codes[r][cols/2], scales[r][cols/32].
  * Codes: element 2i in bits [3:0], element 2i+1 in bits [7:4].
  * Scales: canonical layout, one E8M0 byte per block.
- * SR draws use key (seed, sr_tag) and flat index line*L + t.
+ * SR draws use stream (seed, sr_tag) and flat index line*L + t.
  * Only the lines listed in `lines` (nlines of them) are produced when lines
  * is non-NULL; outputs are then [nlines][...] in that order.
  * Returns 0, or -1 on bad arguments. */
