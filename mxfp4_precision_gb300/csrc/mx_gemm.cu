@@ -767,7 +767,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Variant<FUSED>::kThr
             int mb, nb;
             tile_coords(g, it.tile, mb, nb);
             staged += it.ks1 - it.ks0;
-            // One lane waits; the verdict is broadcast so the warp stays
+            // One lane waits; its result is broadcast so the warp stays
             // converged for the .sync.aligned tensor-memory loads.
             int ok = 1;
             if (lane == 0) ok = mbar_wait_inl(&ctl->acc_full, acc_phase, g.status, abort) ? 1 : 0;

@@ -218,7 +218,7 @@ __device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t 
                  : "memory");
 }
 // Named barrier over `nthreads` threads (whole warps) that also ANDs a
-// predicate across them: every participant gets the same verdict.
+// predicate across them: every participant gets the same result.
 __device__ __forceinline__ bool bar_and(int id, int nthreads, bool v) {
     uint32_t r;
     asm volatile(

@@ -278,7 +278,7 @@ constexpr int kFmtMX4 = 0, kFmtMX8 = 1, kFmtNVAmax = 2, kFmtNV4 = 3;
 // tensor store and the atom with a bulk copy: whole lines reach L2 instead of
 // 16-byte pieces of 64 lines and single bytes.  Two staging buffers
 // alternate; the barrier that opens a tile also ANDs the warps' wait
-// verdicts, so an abort leaves every warp the same way and no warp waits at
+// results, so an abort leaves every warp the same way and no warp waits at
 // a barrier the others have left.
 template <int FMT>
 struct ColStage {
@@ -727,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, SR ? 1 : kColMinBlocks) mxq_colwise_
         ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
         if constexpr (kStagedW) {
             // The staging image was last stored one tile ago; the barrier also
-            // ANDs the warps' wait verdicts (see the column kernel).
+            // ANDs the warps' wait results (see the column kernel).
             if (threadIdx.x == 0) bulk_wait_group_read<0>();
             if (!bar_and(kStageBarrier, kThreads, ok != 0)) break;
         } else if (!ok) {
