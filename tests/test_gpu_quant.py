@@ -66,6 +66,18 @@ def test_rowwise_parity(rot, nb, rnd):
     check_against_oracle(_rand_bits((200, 1280), 2), mx.CONTRACT_COLS, rot, nb, rnd, seed=5)
 
 
+@pytest.mark.parametrize("seed", [2**40 + 12345, 2**64 - 3])
+@pytest.mark.parametrize("contract", [mx.CONTRACT_ROWS, mx.CONTRACT_COLS])
+@pytest.mark.parametrize("rot,nb,rnd", [(mx.ROT_NONE, 32, mx.ROUND_SR),
+                                        (mx.ROT_HADAMARD_RAND, 32, mx.ROUND_RNE),
+                                        (mx.ROT_HADAMARD_RAND, 128, mx.ROUND_SR)])
+def test_random_streams_use_the_whole_seed(seed, contract, rot, nb, rnd):
+    """Seeds of more than 32 bits: the seed's high half is the second Philox key word of the
+    random-sign and SR streams, in the column, wide and row kernels alike."""
+    shape = (1280, 200) if contract == mx.CONTRACT_ROWS else (200, 1280)
+    check_against_oracle(_rand_bits(shape, 3), contract, rot, nb, rnd, seed=seed)
+
+
 @pytest.mark.parametrize("contract", [mx.CONTRACT_ROWS, mx.CONTRACT_COLS])
 @pytest.mark.parametrize("rot,nb", [(mx.ROT_NONE, 32), (mx.ROT_HADAMARD_DET, 16),
                                     (mx.ROT_HADAMARD_DET, 32)])

@@ -157,6 +157,15 @@ def test_sign_vector_bits_follow_documented_mapping():
             assert oracle.sign(seed, t) == (-1 if bit else 1)
 
 
+def test_random_streams_depend_on_the_seed_high_half():
+    # catches a seed truncated to 32 bits on its way into the Philox key
+    lo = 12345
+    for hi in (1, 2**31, 2**32 - 1):
+        seed = (hi << 32) | lo
+        assert [oracle.sr_u24(seed, 1, e) for e in range(8)] != [oracle.sr_u24(lo, 1, e) for e in range(8)]
+        assert [oracle.sign(seed, t) for t in range(128)] != [oracle.sign(lo, t) for t in range(128)]
+
+
 def test_sr_draw_follows_documented_mapping():
     for seed, tag in ((0, 1), (5, 2), (2**35 + 1, 1)):
         for e in (0, 1, 3, 4, 7, 8, 9, 1023, 123457, 2**34 + 6):
