@@ -296,6 +296,12 @@ constexpr int kStageBarrier = 1;   // named barrier of the 8 compute warps
 #ifndef MXQ_L2_HINTS
 #define MXQ_L2_HINTS 1
 #endif
+// The column kernel waits for its staging buffer (and votes on its tile's
+// load) after the tile's arithmetic, not before it (o_proj operands, Hadamard
+// 32: 37.5 -> 35.5 us; random-sign Hadamard 32 on down_proj: 78.5 -> 74.4 us).
+#ifndef MXQ_LATE_STAGE_WAIT
+#define MXQ_LATE_STAGE_WAIT 1
+#endif
 
 template <int ROTN, bool RAND, bool SR, bool DUAL, int FMT = kFmtMX4>
 __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads,
@@ -305,6 +311,9 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads,
     const __grid_constant__ CUtensorMap cmap0, const __grid_constant__ CUtensorMap cmap1,
     const QuantArgs a0, const QuantArgs a1, const QuantArgs ar) {
     constexpr bool kStaged = FMT != kFmtNVAmax;
+    // (Hadamard 16 measured 70.3 us with the early wait against 72.4 us with
+    // the late one on the down_proj operands; 32 and the random signs gain.)
+    constexpr bool kLateStageWait = !DUAL && MXQ_LATE_STAGE_WAIT && ROTN != 16;
     using S = ColStage<FMT>;
     // The dual variant stages two images (column and row direction) and
     // keeps a 2-deep ring so that two CTAs still fit.
@@ -419,11 +428,19 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads,
         int ok = 1;
         if (lane == 0) ok = mbar_wait(&full[s], parity, a0.status, &abort_flag) ? 1 : 0;
         ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-        if constexpr (kStaged) {
-            // The staging buffer of this tile was last stored kStageBufs tiles
-            // ago: that store has read it once at most kStageBufs - 1 are pending.
+        // The staging buffer of this tile was last stored kStageBufs tiles
+        // ago: that store has read it once at most kStageBufs - 1 are pending.
+        // The same CTA barrier ANDs the warps' wait results.  It sits right
+        // before the first staging write, so that the tile's loads and
+        // arithmetic overlap the previous store's read (the dual variant
+        // writes its row image first and takes it here).
+        auto staging_free = [&]() -> bool {
             if (threadIdx.x == 0) bulk_wait_group_read<kStageBufs - 1>();
-            if (!bar_and(kStageBarrier, kThreads, ok != 0)) break;
+            return bar_and(kStageBarrier, kThreads, ok != 0);
+        };
+        if constexpr (kStaged && kLateStageWait) {
+        } else if constexpr (kStaged) {
+            if (!staging_free()) break;
         } else if (!ok) {
             break;
         }
@@ -445,7 +462,7 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads,
         if constexpr (DUAL)
             dual_rows_staged<SR>(tw, t0, c0, a0, ar, stc + S::kBytes, stc + S::kBytes + S::kCodeBytes);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        if (lane == 0 && ok) mbar_arrive(&empty[s]);
         if (DUAL && threadIdx.x == 0) {
             const int nt = tile + kColRing * gridDim.x;
             if (nt < total && mbar_wait(&empty[s], parity, a0.status, &abort_flag)) issue(nt, s);
@@ -490,6 +507,8 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads,
         const int r0 = 64 * chalf + 2 * lane;                 // line of the tile (r0, r0 + 1)
         if constexpr (FMT == kFmtNV4) {
             static_assert(!SR && !DUAL, "NVFP4: round to nearest, one direction");
+            if constexpr (kLateStageWait)
+                if (!staging_free()) break;
             const float s_enc = nv_tensor_scale(__uint_as_float(*(second ? a1.amax : a0.amax)));
             float l[32], h[32];
 #pragma unroll
@@ -517,6 +536,8 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads,
             static_assert(ROTN == 0 && !RAND && !SR && !DUAL, "MXFP8: plain encode only");
             uint4 p0[2], p1[2];
             encode_pair_e4m3(x, p0, p1, s0, s1);
+            if constexpr (kLateStageWait)
+                if (!staging_free()) break;
             // 128-byte lines, 128-byte swizzle: chunk j of line r at j ^ (r & 7).
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
@@ -535,6 +556,8 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads,
         } else {
             encode_pair_rne<(ROTN > 0)>(x, ROTN > 0 ? hadamard_norm<ROTN>() : 1.0f, q0, q1, s0, s1);
         }
+        if constexpr (kLateStageWait)
+            if (!staging_free()) break;
 
         // 64-byte swizzle: 16-byte chunk j of line r at j ^ ((r >> 1) & 3).
         const int sw = tbi ^ ((r0 >> 1) & 3);
