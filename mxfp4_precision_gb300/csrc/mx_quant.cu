@@ -9,8 +9,7 @@
 // (nearest-even, or stochastically) and packed two per byte.
 //
 // Three kernels, all persistent with a ring of 32 KB TMA tiles (3 deep for the
-// column kernel and the wide kernel's Hadamard 64, 2 for the others; two
-// resident CTAs per SM):
+// wide kernel's Hadamard 64, 2 for the others; two resident CTAs per SM):
 //   mxq_colwise       contraction down the rows of src[T][C] (Wgrad operands,
 //                     Dgrad's W), no rotation or Hadamard 16/32: a 128-token
 //                     x 128-channel tile; each thread owns 2 adjacent
@@ -54,17 +53,20 @@ using namespace enc;
 #define MXQ_STAGES 2
 #endif
 constexpr int kStages = MXQ_STAGES;  // TMA ring depth per CTA (wide and row kernels)
-// The column kernel: a 3-deep ring and one output staging buffer (measured
-// best of ring 2/3 x buffers 1/2 at two CTAs per SM; MXFP8's larger staging
-// box keeps a 2-deep ring so that two CTAs still fit).
+// The column kernel: a 2-deep ring and two output staging buffers, so that a
+// tile's staged outputs need not wait for the previous tile's store (down_proj
+// operands: 68.3 us against 70.3 us for a 3-deep ring and one buffer, 66.2
+// against 70.3 us without rotation; o_proj equal; three buffers no better).
 #ifndef MXQ_COL_RING
-#define MXQ_COL_RING 3
+#define MXQ_COL_RING 2
 #endif
 #ifndef MXQ_STAGE_BUFS
-#define MXQ_STAGE_BUFS 1
+#define MXQ_STAGE_BUFS 2
 #endif
 constexpr int kColRing = MXQ_COL_RING;      // TMA ring depth of the column kernel
 constexpr int kStageBufs = MXQ_STAGE_BUFS;  // its output staging buffers
+// The dual variant stages two images per tile and keeps one buffer of each
+// (39.6 us on o_proj's dY against 41.6 us with two).
 // Two resident CTAs per SM (shared memory allows no more with two stages):
 // the round-to-nearest colwise kernels are held to 128 registers so that the
 // random-sign variants do not fall to one CTA per SM.
@@ -276,10 +278,10 @@ constexpr int kFmtMX4 = 0, kFmtMX8 = 1, kFmtNVAmax = 2, kFmtNV4 = 3;
 // 512-byte scale atom (two atoms for NVFP4), which the tiled layout stores
 // contiguously.  After a named barrier, one thread stores the box with a TMA
 // tensor store and the atom with a bulk copy: whole lines reach L2 instead of
-// 16-byte pieces of 64 lines and single bytes.  Two staging buffers
-// alternate; the barrier that opens a tile also ANDs the warps' wait
-// results, so an abort leaves every warp the same way and no warp waits at
-// a barrier the others have left.
+// 16-byte pieces of 64 lines and single bytes.  The staging buffers
+// alternate; the barrier before a tile's first staging write also ANDs the
+// warps' wait results, so an abort leaves every warp the same way and no
+// warp waits at a barrier the others have left.
 template <int FMT>
 struct ColStage {
     static constexpr uint32_t kCodeBytes = FMT == kFmtMX8 ? 16384u : 8192u;  // 128 lines
@@ -330,7 +332,8 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads,
     // thread that issues the stage's load before it arms the stage barrier:
     // one Philox call per tile instead of one per warp.
     uint32_t *signw = reinterpret_cast<uint32_t *>(empty + kColRing);
-    uint8_t *staging = smem + kColRing * kTileBytes + 1024;  // kStageBufs x kImages x S::kBytes
+    constexpr int kBufs = DUAL ? 1 : kStageBufs;
+    uint8_t *staging = smem + kColRing * kTileBytes + 1024;  // kBufs x kImages x S::kBytes
     __shared__ int abort_flag;
 
     using G = ColTile<ROTN>;
@@ -428,14 +431,14 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads,
         int ok = 1;
         if (lane == 0) ok = mbar_wait(&full[s], parity, a0.status, &abort_flag) ? 1 : 0;
         ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-        // The staging buffer of this tile was last stored kStageBufs tiles
-        // ago: that store has read it once at most kStageBufs - 1 are pending.
+        // The staging buffer of this tile was last stored kBufs tiles ago:
+        // that store has read it once at most kBufs - 1 are pending.
         // The same CTA barrier ANDs the warps' wait results.  It sits right
         // before the first staging write, so that the tile's loads and
         // arithmetic overlap the previous store's read (the dual variant
         // writes its row image first and takes it here).
         auto staging_free = [&]() -> bool {
-            if (threadIdx.x == 0) bulk_wait_group_read<kStageBufs - 1>();
+            if (threadIdx.x == 0) bulk_wait_group_read<kBufs - 1>();
             return bar_and(kStageBarrier, kThreads, ok != 0);
         };
         if constexpr (kStaged && kLateStageWait) {
@@ -457,7 +460,7 @@ __global__ void __launch_bounds__(DUAL ? kThreads : kColProducerThreads,
         const uint32_t sbits = RAND ? signw[s * G::TOKEN_BLOCKS + tbi] : 0u;
         // This tile's staging buffer: the column image (codes box, scale
         // atoms), then with DUAL the row image.
-        uint8_t *stc = staging + (it % kStageBufs) * kImages * S::kBytes;
+        uint8_t *stc = staging + (it % kBufs) * kImages * S::kBytes;
         uint8_t *sts = stc + S::kCodeBytes;
         if constexpr (DUAL)
             dual_rows_staged<SR>(tw, t0, c0, a0, ar, stc + S::kBytes, stc + S::kBytes + S::kCodeBytes);
@@ -1056,7 +1059,7 @@ struct Operands {
 template <int FMT, bool DUAL = false>
 constexpr size_t col_smem() {
     return (DUAL ? 2 : ColStage<FMT>::kRing) * kTileBytes + 1024 + 1024 +
-           kStageBufs * (DUAL ? 2 : 1) * ColStage<FMT>::kBytes;
+           (DUAL ? 1 : kStageBufs) * (DUAL ? 2 : 1) * ColStage<FMT>::kBytes;
 }
 
 template <bool COLWISE, int ROTN, bool RAND>
